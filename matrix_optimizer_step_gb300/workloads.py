@@ -1,0 +1,268 @@
+"""Seeded synthetic inputs for the owner-side Muon / AdamW step.
+
+This module only draws inputs and counts work: it holds none of the
+optimizer's arithmetic, so both the CUDA path and the float64 oracle can take
+their inputs from it without sharing any of the method.
+
+Five workloads, named for what they are:
+
+* ``single_256x512``  one fp32 matrix W 256x512 (W~N(0,0.02^2), G~N(0,1),
+  momentum zeros), plus tiny 3x4 and 8x16 matrices for closed-form checks;
+* ``gpt2_small``      12 layers x {q,k,v,o 768x768, fc 3072x768, proj
+  768x3072} = 72 Muon matrices with bf16 grads N(0,1e-2^2) plus a rank-16
+  spike whose Frobenius norm is 10x the noise's; 50 LayerNorm vectors (768)
+  on AdamW; three consecutive steps with fresh grads;
+* ``many_small``      4096 bf16-grad matrices, m and n drawn independently
+  and uniformly from {64,...,2048}, grads N(0,1) times a per-matrix scale
+  with log10 uniform in [-4,-1];
+* ``llama3_8b``       32 layers x {q 4096^2, k 1024x4096, v 1024x4096,
+  o 4096^2, gate 14336x4096, up 14336x4096, down 4096x14336} = 224 Muon
+  matrices, bf16 grads 1e-3*Student-t(3) plus a rank-8 part of equal
+  Frobenius norm; embedding and lm_head 128256x4096 and 65 RMSNorm vectors
+  (4096) on AdamW;
+* ``moe_experts``     4 layers x {w1 [8,14336,4096], w3 [8,14336,4096],
+  w2 [8,4096,14336]}, bf16 grads N(0,1e-3^2) times a per-expert scale
+  U[0.1,10].
+
+Random draws use ``torch.Generator`` seeded per tensor, so every tensor can
+be regenerated alone (that is how the oracle gets sampled matrices of the
+full-size workloads).
+"""
+
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+
+import torch
+
+NS_COEFFS = (3.4445, -4.7750, 2.0315)
+
+WORKLOADS = ("single_256x512", "gpt2_small", "many_small", "llama3_8b", "moe_experts")
+
+_SMALL_SIDES = (64, 128, 256, 512, 1024, 2048)
+
+
+@dataclass(frozen=True)
+class MatrixSpec:
+    """One Muon tensor (rank >= 2; NS acts on the last two dims)."""
+
+    name: str
+    shape: tuple
+    grad_dtype: torch.dtype = torch.bfloat16
+    grad_scale: float = 1.0          # many_small: per-matrix scale
+    slice_scales: tuple = ()         # moe_experts: per-leading-index scale
+
+    @property
+    def numel(self):
+        return math.prod(self.shape)
+
+    @property
+    def mn(self):
+        return self.shape[-2], self.shape[-1]
+
+    @property
+    def n_slices(self):
+        return math.prod(self.shape[:-2]) if len(self.shape) > 2 else 1
+
+
+@dataclass(frozen=True)
+class VectorSpec:
+    """One AdamW-route tensor (flattened)."""
+
+    name: str
+    shape: tuple
+
+    @property
+    def numel(self):
+        return math.prod(self.shape)
+
+
+@dataclass
+class Workload:
+    name: str
+    matrices: list
+    vectors: list
+    hyper: dict = field(default_factory=dict)
+    grad_kind: str = "normal"
+    steps: int = 1
+
+    @property
+    def muon_numel(self):
+        return sum(s.numel for s in self.matrices)
+
+    @property
+    def adamw_numel(self):
+        return sum(v.numel for v in self.vectors)
+
+
+def _hyper(**kw):
+    h = dict(lr=0.02, momentum=0.95, wd=0.01, ns_steps=5, a=NS_COEFFS[0],
+             b=NS_COEFFS[1], c=NS_COEFFS[2], nesterov=True, fp32_ns=False,
+             adam_lr=1e-3, beta1=0.9, beta2=0.95, adam_eps=1e-8, adam_wd=0.0)
+    h.update(kw)
+    return h
+
+
+def workload(name, tiny_extra=True):
+    """Return the spec of one named workload."""
+    if name == "single_256x512":
+        mats = [MatrixSpec("W", (256, 512), torch.float32)]
+        if tiny_extra:
+            mats += [MatrixSpec("tiny_3x4", (3, 4), torch.float32),
+                     MatrixSpec("tiny_8x16", (8, 16), torch.float32)]
+        return Workload(name, mats, [], _hyper(fp32_ns=True), grad_kind="normal")
+    if name == "gpt2_small":
+        mats, vecs = [], []
+        for l in range(12):
+            for p in ("q", "k", "v", "o"):
+                mats.append(MatrixSpec(f"h{l}.attn.{p}", (768, 768)))
+            mats.append(MatrixSpec(f"h{l}.mlp.fc", (3072, 768)))
+            mats.append(MatrixSpec(f"h{l}.mlp.proj", (768, 3072)))
+            for ln in ("ln_1", "ln_2"):
+                vecs.append(VectorSpec(f"h{l}.{ln}.weight", (768,)))
+                vecs.append(VectorSpec(f"h{l}.{ln}.bias", (768,)))
+        vecs += [VectorSpec("ln_f.weight", (768,)), VectorSpec("ln_f.bias", (768,))]
+        return Workload(name, mats, vecs, _hyper(), grad_kind="spiked16", steps=3)
+    if name == "many_small":
+        g = torch.Generator().manual_seed(0)
+        idx = torch.randint(0, len(_SMALL_SIDES), (4096, 2), generator=g)
+        logs = torch.rand(4096, generator=g, dtype=torch.float64) * 3.0 - 4.0
+        mats = [MatrixSpec(f"m{i}", (_SMALL_SIDES[int(idx[i, 0])], _SMALL_SIDES[int(idx[i, 1])]),
+                           grad_scale=float(10.0 ** logs[i]))
+                for i in range(4096)]
+        return Workload(name, mats, [], _hyper(), grad_kind="normal")
+    if name == "llama3_8b":
+        mats, vecs = [], []
+        shapes = (("q", (4096, 4096)), ("k", (1024, 4096)), ("v", (1024, 4096)),
+                  ("o", (4096, 4096)), ("gate", (14336, 4096)), ("up", (14336, 4096)),
+                  ("down", (4096, 14336)))
+        for l in range(32):
+            for p, s in shapes:
+                mats.append(MatrixSpec(f"layers.{l}.{p}", s))
+            vecs.append(VectorSpec(f"layers.{l}.input_norm", (4096,)))
+            vecs.append(VectorSpec(f"layers.{l}.post_norm", (4096,)))
+        vecs += [VectorSpec("norm", (4096,)),
+                 VectorSpec("embed_tokens", (128256, 4096)),
+                 VectorSpec("lm_head", (128256, 4096))]
+        return Workload(name, mats, vecs, _hyper(), grad_kind="student_t_rank8")
+    if name == "moe_experts":
+        g = torch.Generator().manual_seed(5)
+        mats = []
+        for l in range(4):
+            for w, s in (("w1", (8, 14336, 4096)), ("w3", (8, 14336, 4096)), ("w2", (8, 4096, 14336))):
+                scales = tuple(float(x) for x in (torch.rand(8, generator=g, dtype=torch.float64) * 9.9 + 0.1))
+                mats.append(MatrixSpec(f"layers.{l}.experts.{w}", s, slice_scales=scales))
+        return Workload(name, mats, [], _hyper(), grad_kind="normal_1e-3")
+    raise KeyError(name)
+
+
+# --------------------------------------------------------------------------
+# Seeded tensor draws
+# --------------------------------------------------------------------------
+
+def _gen(device, seed):
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed))
+    return g
+
+
+def master_init(spec, index, device="cpu"):
+    """fp32 master weight ~ N(0, 0.02^2), seed 1_000_000 + index."""
+    g = _gen(device, 1_000_000 + index)
+    return torch.randn(spec.shape, generator=g, device=device, dtype=torch.float32) * 0.02
+
+
+def vector_init(spec, index, device="cpu"):
+    """AdamW-route master: RMS/LayerNorm-like vectors start near 1, big tables ~N(0,0.02^2)."""
+    g = _gen(device, 2_000_000 + index)
+    x = torch.randn(spec.shape, generator=g, device=device, dtype=torch.float32) * 0.02
+    if len(spec.shape) == 1:
+        x += 1.0
+    return x.reshape(-1)
+
+
+def _orthonormal(rows, k, g, device):
+    q, _ = torch.linalg.qr(torch.randn(rows, k, generator=g, device=device, dtype=torch.float32))
+    return q
+
+
+def muon_grad(wl, spec, index, step=0, device="cpu"):
+    """Gradient of one Muon tensor for step ``step`` (fresh per step)."""
+    seed = index + 1000 * step
+    g = _gen(device, seed)
+    shape = spec.shape
+    kind = wl.grad_kind
+    if kind == "normal":
+        x = torch.randn(shape, generator=g, device=device, dtype=torch.float32) * spec.grad_scale
+    elif kind == "normal_1e-3":
+        x = torch.randn(shape, generator=g, device=device, dtype=torch.float32) * 1e-3
+        if spec.slice_scales:
+            sc = torch.tensor(spec.slice_scales, device=device, dtype=torch.float32)
+            x = x * sc.reshape((-1,) + (1,) * (len(shape) - 1))
+    elif kind == "spiked16":
+        m, n = shape
+        noise = torch.randn(shape, generator=g, device=device, dtype=torch.float32) * 1e-2
+        u = _orthonormal(m, 16, g, device)
+        v = _orthonormal(n, 16, g, device)
+        spike = u @ v.T  # 16 unit singular values, Frobenius norm 4
+        x = noise + spike * (10.0 * noise.norm() / 4.0)
+    elif kind == "student_t_rank8":
+        m, n = shape
+        z = torch.randn(shape, generator=g, device=device, dtype=torch.float32)
+        chi = torch.zeros(shape, device=device, dtype=torch.float32)
+        for _ in range(3):
+            e = torch.randn(shape, generator=g, device=device, dtype=torch.float32)
+            chi.addcmul_(e, e)
+        t = z * torch.rsqrt(chi / 3.0) * 1e-3
+        del z, chi
+        lo = torch.randn(m, 8, generator=g, device=device, dtype=torch.float32) @ \
+            torch.randn(8, n, generator=g, device=device, dtype=torch.float32)
+        x = t + lo * (t.norm() / lo.norm())
+        del t, lo
+    else:
+        raise KeyError(kind)
+    return x.to(spec.grad_dtype)
+
+
+def vector_grad(spec, index, step=0, device="cpu"):
+    """bf16 gradient of one AdamW-route tensor, N(0, 1e-2^2), flattened."""
+    g = _gen(device, 3_000_000 + index + 1000 * step)
+    return (torch.randn(spec.numel, generator=g, device=device, dtype=torch.float32) * 1e-2).to(torch.bfloat16)
+
+
+# --------------------------------------------------------------------------
+# Work accounting (used for roofline figures; not part of the method)
+# --------------------------------------------------------------------------
+
+def ns_flops(m, n, steps):
+    """Dense flop count of ``steps`` NS iterations on one m x n matrix.
+
+    Per iteration with p = min(m,n), q = max(m,n): the Gram product
+    2p^2q, the square of the Gram 2p^3 and the final product 2p^2q.
+    """
+    p, q = min(m, n), max(m, n)
+    return steps * (4 * p * p * q + 2 * p ** 3)
+
+
+def workload_ns_flops(wl):
+    return sum(ns_flops(*s.mn, wl.hyper["ns_steps"]) * s.n_slices for s in wl.matrices)
+
+
+def muon_elementwise_bytes(wl):
+    """Minimal HBM bytes of the two streaming passes of the Muon step.
+
+    Momentum pass: grad read, momentum read+write, bf16 X0 write.
+    Update pass: X read (bf16), master read+write, bf16 param write.
+    """
+    total = 0
+    for s in wl.matrices:
+        gb = 2 if s.grad_dtype == torch.bfloat16 else 4
+        xb = 4 if wl.hyper["fp32_ns"] else 2
+        total += s.numel * (gb + 8 + xb) + s.numel * (xb + 8 + 2)
+    return total
+
+
+def adamw_bytes(wl):
+    """bf16 grad read, fp32 master/m/v read+write, bf16 param write."""
+    return wl.adamw_numel * (2 + 24 + 2)

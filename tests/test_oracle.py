@@ -1,0 +1,342 @@
+"""Pins for the float64 oracle, against things other than the oracle itself.
+
+Each test ties one oracle function to the mathematics or to a library
+routine: the SVD closed form of the Newton-Schulz polynomial, the pages'
+unfactored NS equation, torch's own SGD/AdamW on the CPU, Graham's tight LPT
+instance, and the worked examples the pages print (``tests/golden``).
+CPU only.
+"""
+
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import adamw as oadamw
+from oracle import lpt as olpt
+from oracle import muon as omuon
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+A, B, C = 3.4445, -4.7750, 2.0315
+
+
+def _rng(seed):
+    return np.random.default_rng(seed)
+
+
+# ---------------------------------------------------------------- bf16 cast
+
+def test_bf16_round_matches_torch_cast():
+    r = _rng(0)
+    x = np.concatenate([
+        r.standard_normal(20000) * 10.0 ** r.uniform(-30, 30, 20000),
+        # exact ties between two bf16 neighbours, both parities
+        (np.arange(1, 2001, dtype=np.float64) * 2.0 + 1.0) * 2.0 ** -8,
+        np.array([0.0, -0.0, 1.0, -1.0, 65504.0, 1e-40]),
+    ])
+    want = torch.from_numpy(x.astype(np.float32)).to(torch.bfloat16).to(torch.float64).numpy()
+    got = omuon.bf16_round(x)
+    np.testing.assert_array_equal(got, want)
+
+
+# ---------------------------------------------------------- Newton-Schulz
+
+def _closed_form(G, steps, eps=omuon.NS_EPS):
+    """U p^k(S/(||G||+eps)) V^T via the SVD: the polynomial acts on singular values."""
+    U, S, Vt = np.linalg.svd(G, full_matrices=False)
+    s = S / (np.linalg.norm(G) + eps)
+    for _ in range(steps):
+        s = A * s + B * s ** 3 + C * s ** 5
+    return (U * s) @ Vt
+
+
+@pytest.mark.parametrize("shape", [(3, 4), (8, 16), (4, 3), (16, 8), (17, 17), (64, 128), (128, 40), (33, 70)])
+@pytest.mark.parametrize("steps", [1, 2, 5])
+def test_ns_matches_svd_closed_form(shape, steps):
+    G = _rng(hash(shape) % 1000 + steps).standard_normal(shape)
+    got = omuon.newton_schulz(G, A, B, C, steps)
+    want = _closed_form(G, steps)
+    assert got.shape == G.shape
+    np.testing.assert_allclose(got, want, rtol=0, atol=1e-12 * max(1.0, np.abs(want).max()))
+
+
+def test_ns_matches_unfactored_equation():
+    # "架构设计" §1: X <- aX + b X X^T X + c X (X^T X)^2, written term by term.
+    r = _rng(3)
+    for p, q in [(5, 9), (32, 48), (20, 20)]:
+        X = r.standard_normal((p, q))
+        X /= np.linalg.norm(X)
+        Y = X.copy()
+        for _ in range(5):
+            Y = A * Y + B * (Y @ Y.T @ Y) + C * (Y @ (Y.T @ Y) @ (Y.T @ Y))
+        got = omuon.ns_iterate(X, A, B, C, 5)
+        np.testing.assert_allclose(got, Y, rtol=0, atol=1e-12)
+
+
+def test_ns_band_invariant():
+    # p^5 maps [0.0015, 1] into about [0.68, 1.21]: every output singular value of
+    # a well-conditioned normalised input lies in that band.
+    grid = np.linspace(0.0015, 1.0, 200001)
+    s = grid.copy()
+    for _ in range(5):
+        s = A * s + B * s ** 3 + C * s ** 5
+    lo, hi = s.min(), s.max()
+    assert 0.67 < lo < 0.69 and 1.20 < hi < 1.21
+    r = _rng(4)
+    for shape in [(64, 128), (100, 60), (256, 256)]:
+        G = r.standard_normal(shape)
+        sv = np.linalg.svd(G, compute_uv=False) / np.linalg.norm(G)
+        if sv.min() < 0.0015:
+            continue
+        out = np.linalg.svd(omuon.newton_schulz(G, A, B, C, 5), compute_uv=False)
+        assert out.min() >= lo - 1e-9 and out.max() <= hi + 1e-9
+
+
+def test_ns_transpose_equivariance_and_scale_invariance():
+    r = _rng(5)
+    G = r.standard_normal((24, 56))
+    O = omuon.newton_schulz(G, A, B, C, 5)
+    np.testing.assert_allclose(omuon.newton_schulz(G.T, A, B, C, 5), O.T, atol=1e-13)
+    # With eps = 0 the normalisation makes the output exactly scale-free.
+    O0 = omuon.newton_schulz(G, A, B, C, 5, eps=0.0)
+    for s in (1e-3, 1e3):
+        np.testing.assert_allclose(omuon.newton_schulz(s * G, A, B, C, 5, eps=0.0), O0, atol=1e-12)
+
+
+def test_ns_orthonormal_rows_map_to_scaled_copy():
+    # Rows orthonormal: every singular value of X0 is 1/sqrt(p), so the output
+    # is p^5(1/sqrt(p)) times the input (singular vectors untouched).
+    r = _rng(6)
+    Q, _ = np.linalg.qr(r.standard_normal((40, 10)))
+    G = Q.T  # 10 x 40, orthonormal rows
+    s = 1.0 / math.sqrt(10)
+    for _ in range(5):
+        s = A * s + B * s ** 3 + C * s ** 5
+    out = omuon.newton_schulz(G, A, B, C, 5, eps=0.0)
+    np.testing.assert_allclose(out, s * G, atol=1e-12)
+
+
+def test_ns_zero_matrix():
+    out = omuon.newton_schulz(np.zeros((6, 9)), A, B, C, 5)
+    assert np.all(out == 0)
+
+
+def test_ns_emulated_bf16_close_to_exact():
+    r = _rng(7)
+    G = r.standard_normal((64, 128))
+    exact = omuon.newton_schulz(G, A, B, C, 5)
+    emu = omuon.newton_schulz(G, A, B, C, 5, emulate_bf16=True)
+    rel = np.linalg.norm(emu - exact) / np.linalg.norm(exact)
+    assert 1e-4 < rel < 2e-2
+    assert np.all(omuon.bf16_round(emu) == emu)
+
+
+# ----------------------------------------------------------------- momentum
+
+def test_momentum_matches_torch_sgd_nesterov():
+    # torch.optim.SGD(nesterov=True, dampening=0): buf <- mu*buf + g and the
+    # step direction g + mu*buf, the reading the oracle takes.
+    r = _rng(8)
+    mu, lr = 0.95, 0.1
+    p = torch.zeros(5, 7, dtype=torch.float64, requires_grad=True)
+    opt = torch.optim.SGD([p], lr=lr, momentum=mu, nesterov=True)
+    buf = np.zeros((5, 7))
+    for _ in range(4):
+        g = r.standard_normal((5, 7))
+        before = p.detach().clone().numpy()
+        p.grad = torch.from_numpy(g.copy())
+        opt.step()
+        buf, u = omuon.momentum_update(buf, g, mu)
+        np.testing.assert_allclose(opt.state[p]["momentum_buffer"].numpy(), buf, rtol=1e-15, atol=0)
+        np.testing.assert_allclose((before - p.detach().numpy()) / lr, u, rtol=1e-12, atol=1e-15)
+
+
+def test_momentum_closed_forms():
+    g = _rng(9).standard_normal((3, 5))
+    buf, u = omuon.momentum_update(np.zeros_like(g), g, 0.95)
+    np.testing.assert_array_equal(buf, g)
+    np.testing.assert_allclose(u, 1.95 * g, rtol=1e-15)
+    buf, u = omuon.momentum_update(np.ones_like(g), g, 0.0)
+    np.testing.assert_array_equal(u, g)
+    buf, u = omuon.momentum_update(np.zeros_like(g), g, 0.9, nesterov=False)
+    np.testing.assert_array_equal(u, g)
+
+
+# ------------------------------------------------------------------ update
+
+def test_update_closed_forms():
+    r = _rng(10)
+    W = r.standard_normal((4, 6))
+    O = r.standard_normal((4, 6))
+    np.testing.assert_array_equal(omuon.apply_update(W, O, 0.0, 0.5, 4, 6), W)
+    np.testing.assert_allclose(omuon.apply_update(W, O, 0.1, 0.0, 4, 6), W - 0.1 * O, rtol=1e-15)
+    np.testing.assert_allclose(omuon.apply_update(W, np.zeros_like(O), 0.1, 0.2, 4, 6), W * 0.98, rtol=1e-15)
+    assert omuon.shape_scale(1024, 4096) == 1.0
+    assert omuon.shape_scale(14336, 4096) == pytest.approx(math.sqrt(3.5), rel=1e-15)
+    assert omuon.shape_scale(4096, 14336) == 1.0
+
+
+def test_muon_step_zero_grad_is_weight_decay_only():
+    r = _rng(11)
+    W = r.standard_normal((8, 16))
+    out = omuon.muon_step(W, np.zeros_like(W), np.zeros_like(W), 0.02, 0.95, 0.01, 5, A, B, C)
+    np.testing.assert_allclose(out["W"], W * (1 - 0.02 * 0.01), rtol=1e-15)
+    assert np.all(out["O"] == 0)
+
+
+def test_muon_step_last_two_dims_rule_golden():
+    with open(os.path.join(GOLDEN, "last_two_dims.json")) as f:
+        gold = json.load(f)
+    r = _rng(12)
+    for case in gold["cases"]:
+        shape = tuple(case["shape"])
+        W = r.standard_normal(shape)
+        g = r.standard_normal(shape)
+        if not case["accepted"]:
+            with pytest.raises(ValueError):
+                omuon.muon_step(W, np.zeros_like(W), g, 0.02, 0.95, 0.01, 5, A, B, C)
+            continue
+        out = omuon.muon_step(W, np.zeros_like(W), g, 0.02, 0.95, 0.01, 5, A, B, C)
+        m, n = (shape[d] for d in case["matrix_dims"])
+        slices = g.reshape(-1, m, n)
+        assert slices.shape[0] == case["n_matrices"]
+        for s in range(slices.shape[0]):
+            want = _closed_form(1.95 * slices[s], 5)
+            np.testing.assert_allclose(out["O"].reshape(-1, m, n)[s], want, atol=1e-12)
+
+
+def test_muon_step_full_composition():
+    # W' = W(1-lr wd) - lr sqrt(max(1,m/n)) * U p^5(S) V^T of the Nesterov
+    # direction, for a tall matrix (m > n, scale sqrt(2)).
+    r = _rng(13)
+    W = r.standard_normal((32, 16))
+    buf = r.standard_normal((32, 16))
+    g = r.standard_normal((32, 16))
+    lr, mu, wd = 0.02, 0.9, 0.1
+    nb = mu * buf + g
+    u = g + mu * nb
+    want = W * (1 - lr * wd) - lr * math.sqrt(2.0) * _closed_form(u, 5)
+    out = omuon.muon_step(W, buf, g, lr, mu, wd, 5, A, B, C)
+    np.testing.assert_allclose(out["W"], want, atol=1e-13)
+    np.testing.assert_allclose(out["buf"], nb, atol=0)
+
+
+# ------------------------------------------------------------------- AdamW
+
+@pytest.mark.parametrize("wd", [0.0, 0.1])
+def test_adamw_matches_torch_adamw(wd):
+    r = _rng(14)
+    lr, b1, b2, eps = 1e-2, 0.9, 0.95, 1e-8
+    W0 = r.standard_normal(300)
+    p = torch.tensor(W0.copy(), dtype=torch.float64, requires_grad=True)
+    opt = torch.optim.AdamW([p], lr=lr, betas=(b1, b2), eps=eps, weight_decay=wd)
+    W, m, v = W0.copy(), np.zeros(300), np.zeros(300)
+    for t in range(1, 6):
+        g = r.standard_normal(300) * 10.0 ** r.uniform(-4, 1)
+        p.grad = torch.from_numpy(g.copy())
+        opt.step()
+        out = oadamw.adamw_step(W, m, v, g, lr, b1, b2, eps, wd, t)
+        W, m, v = out["W"], out["m"], out["v"]
+        st = opt.state[p]
+        # torch forms m with lerp, a different rounding order: compare at 1e-10.
+        np.testing.assert_allclose(st["exp_avg"].numpy(), m, rtol=1e-10, atol=1e-18)
+        np.testing.assert_allclose(st["exp_avg_sq"].numpy(), v, rtol=1e-10, atol=1e-24)
+        np.testing.assert_allclose(p.detach().numpy(), W, rtol=1e-13, atol=1e-16)
+
+
+def test_adamw_constant_gradient_closed_form():
+    # Constant g: bias-corrected moments are exactly g and g^2, so every step
+    # moves W by lr*g/(|g|+eps) (wd = 0).
+    g = np.array([1e-3, -2.0, 0.5, -1e-6])
+    W = np.zeros(4)
+    m = np.zeros(4)
+    v = np.zeros(4)
+    lr, eps = 0.01, 1e-8
+    for t in range(1, 8):
+        out = oadamw.adamw_step(W, m, v, g, lr, 0.9, 0.95, eps, 0.0, t)
+        W, m, v = out["W"], out["m"], out["v"]
+        np.testing.assert_allclose(W, -t * lr * g / (np.abs(g) + eps), rtol=1e-12)
+
+
+def test_adamw_rejects_step_zero():
+    with pytest.raises(ValueError):
+        oadamw.adamw_step(np.zeros(2), np.zeros(2), np.zeros(2), np.ones(2), 0.1, 0.9, 0.9, 1e-8, 0, 0)
+
+
+# --------------------------------------------------------------------- LPT
+
+def _brute_force_opt(sizes, r):
+    best = None
+    for assign in itertools.product(range(r), repeat=len(sizes)):
+        loads = [0] * r
+        for s, a in zip(sizes, assign):
+            loads[a] += s
+        mk = max(loads)
+        best = mk if best is None else min(best, mk)
+    return best
+
+
+def test_lpt_within_graham_bound_of_brute_force():
+    r = _rng(15)
+    for trial in range(60):
+        n = int(r.integers(1, 9))
+        R = int(r.integers(1, 5))
+        sizes = [int(x) for x in r.integers(0, 50, n)]
+        slots, loads = olpt.lpt_assign(sizes, R)
+        assert sorted(set(slots)) <= list(range(R))
+        assert sum(loads) == sum(sizes)
+        for j in range(R):
+            assert loads[j] == sum(s for s, a in zip(sizes, slots) if a == j)
+        opt = _brute_force_opt(sizes, R)
+        assert max(loads) <= olpt.graham_bound(R) * opt + 1e-9
+
+
+@pytest.mark.parametrize("R", [2, 3, 4, 5, 8])
+def test_lpt_graham_tight_instance(R):
+    # Graham's tight family: 2R+1 jobs 2R-1, 2R-1, 2R-2, 2R-2, ..., R+1, R+1,
+    # R, R, R.  LPT reaches 4R-1, the optimum is 3R: ratio 4/3 - 1/(3R).
+    sizes = []
+    for k in range(2 * R - 1, R, -1):
+        sizes += [k, k]
+    sizes += [R, R, R]
+    _, loads = olpt.lpt_assign(sizes, R)
+    assert max(loads) == 4 * R - 1
+    assert max(loads) / (3 * R) == pytest.approx(olpt.graham_bound(R), rel=1e-15)
+
+
+def test_lpt_equal_sizes_balanced_and_ties():
+    slots, loads = olpt.lpt_assign([5] * 23, 4)
+    assert max(loads) - min(loads) <= 5
+    assert slots[:4] == [0, 1, 2, 3]
+    slots, _ = olpt.lpt_assign([3, 9, 3, 9], 2)
+    assert slots == [0, 0, 1, 1]
+
+
+def test_lpt_pages_per_layer_idle_example_golden():
+    with open(os.path.join(GOLDEN, "lpt_per_layer_idle.json")) as f:
+        gold = json.load(f)
+    R, k = gold["n_slots"], gold["items_per_layer"]
+    layers = 32
+    per_layer_loads = [0] * R
+    for _ in range(layers):
+        slots, _ = olpt.lpt_assign([1] * k, R)
+        for s in slots:
+            per_layer_loads[s] += 1
+    idle = sum(1 for x in per_layer_loads if x == 0)
+    assert idle == gold["per_layer_idle_slots"]
+    assert idle / R == pytest.approx(gold["per_layer_idle_fraction"])
+    _, glob = olpt.lpt_assign([1] * (k * layers), R)
+    assert max(glob) - min(glob) == 0 and min(glob) > 0
+    assert max(glob) <= max(per_layer_loads)
+
+
+def test_lpt_rejects_bad_input():
+    with pytest.raises(ValueError):
+        olpt.lpt_assign([1, 2], 0)
+    with pytest.raises(ValueError):
+        olpt.lpt_assign([1, -2], 2)
+    assert olpt.lpt_assign([], 3) == ([], [0, 0, 0])
