@@ -1,0 +1,259 @@
+/*
+ * dmuon.h -- C ABI of the owner-side Muon / AdamW optimizer step on one GPU.
+ *
+ * The operation: a parameter's single owner updates its own full copy with no
+ * communication -- momentum, Newton-Schulz orthogonalisation, weight decay
+ * and the parameter update (DMuon docs, "架构设计" (architecture design),
+ * §2 "专属归属权——原语", optimizer-step bullet, and §3.3 "Owner 步进";
+ * "HSDP 训练（多机）", "底层发生了什么" step 3).  The Newton-Schulz iteration is
+ * the one of "架构设计" §1 (X <- aX + bXX^T X + cX(X^T X)^2), applied to the
+ * last two dimensions of tensors of rank >= 2 (MindSpore hyper-parallel
+ * "分布式 Muon 优化器 — 参数分组设计文档（v2）" §2.1-§2.2).  Non-matrix
+ * parameters take the element-wise AdamW routes ("Pure DMuon 路由", route
+ * table).  Work units are balanced by the LPT greedy of "架构设计" §3.1.
+ *
+ * Conventions shared by every entry point:
+ *  - Plain pointers and sizes only.  "Device pointer" means memory the
+ *    current CUDA device can address (cudaMalloc, or a torch CUDA tensor's
+ *    data pointer); "host pointer" means ordinary process memory.
+ *  - The caller owns every tensor.  The library owns only what a context
+ *    allocates for itself (Newton-Schulz workspace, plan tables), which it
+ *    frees in dmuon_context_destroy.
+ *  - Device work is enqueued on the caller's stream (a cudaStream_t passed
+ *    as void*, NULL = the legacy default stream) and returns without waiting.
+ *  - All arguments are validated on the host before anything is enqueued:
+ *    a call that returns an error has changed no tensor.
+ *  - Results are deterministic: the same inputs give bit-identical outputs
+ *    (no floating-point atomics; reductions run in a fixed order).
+ *  - Errors are returned as dmuon_status codes; dmuon_last_error() gives a
+ *    one-line message for the calling thread's last failure.
+ */
+#ifndef DMUON_H
+#define DMUON_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define DMUON_API __attribute__((visibility("default")))
+#else
+#define DMUON_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum dmuon_status {
+  DMUON_OK = 0,
+  DMUON_ERR_INVALID_ARG = 1, /* null pointer, bad count, bad hyper-parameter      */
+  DMUON_ERR_RANK_LT2 = 2,    /* a Muon tensor of rank < 2 (route it to AdamW)     */
+  DMUON_ERR_SHAPE = 3,       /* zero or negative dimension, or rank > 4           */
+  DMUON_ERR_DTYPE = 4,       /* unsupported gradient dtype                        */
+  DMUON_ERR_CUDA = 5,        /* a CUDA runtime/driver call failed                 */
+  DMUON_ERR_TIMEOUT = 6,     /* a bounded device-side wait ran out (see below)    */
+  DMUON_ERR_NOMEM = 7,       /* device or pinned host allocation failed           */
+  DMUON_ERR_UNSUPPORTED = 8  /* no usable device (e.g. not sm_100-family)         */
+} dmuon_status;
+
+/* Gradient dtypes. */
+enum { DMUON_DTYPE_F32 = 0, DMUON_DTYPE_BF16 = 1 };
+
+/* dmuon_muon_step flags. */
+enum {
+  DMUON_FLAG_NESTEROV = 1u, /* u = g + mu*buf (else u = buf)                      */
+  DMUON_FLAG_FP32_NS = 2u   /* validation mode: fp32 Newton-Schulz on CUDA cores  */
+};
+
+/* One-line description of a status code.  Never NULL. */
+DMUON_API const char* dmuon_status_string(int status);
+
+/* Message of the calling thread's last failed call ("" if none).  Never NULL. */
+DMUON_API const char* dmuon_last_error(void);
+
+/*
+ * dmuon_lpt_assign -- longest-processing-time greedy assignment.
+ *
+ * "架构设计" §3.1 "分区（全局 LPT）": one global greedy pass over all work
+ * units; on identical slots its makespan is at most 4/3 - 1/(3R) times the
+ * optimum.  Tie rules (the page gives none): items in descending size, equal
+ * sizes by ascending index; each item to the slot with the smallest load,
+ * equal loads to the lowest slot index.  The result is therefore unique.
+ *
+ *   sizes     host, n_items int64 costs, each >= 0 (read only)
+ *   n_items   >= 0
+ *   n_slots   >= 1
+ *   out_slot  host, n_items int32: slot of each item (written)
+ *   out_load  host, n_slots int64: total cost per slot (written), or NULL
+ *
+ * Pure host code; no CUDA call.  Errors: DMUON_ERR_INVALID_ARG for a null
+ * required pointer, n_items < 0, n_slots < 1, a negative size, or a slot
+ * load that would overflow int64.
+ */
+DMUON_API int dmuon_lpt_assign(const int64_t* sizes, int32_t n_items, int32_t n_slots,
+                     int32_t* out_slot, int64_t* out_load);
+
+/*
+ * One Muon-route tensor.  shape[0..rank-1] is row-major and contiguous; the
+ * Newton-Schulz iteration acts on the last two dimensions (m rows, n cols)
+ * and every leading index is a separate matrix.  All pointers are device
+ * pointers to rank-shaped contiguous arrays:
+ *   master      fp32, read and written (the fp32 master weight W)
+ *   momentum    fp32, read and written (the momentum buffer)
+ *   grad        fp32 or bf16 per grad_dtype, read only
+ *   param_bf16  bf16 (raw uint16 bits), written, may be NULL (no bf16 copy)
+ * master, momentum and param_bf16 must not overlap one another or grad.
+ */
+typedef struct dmuon_matrix {
+  int32_t rank;          /* 2..4 */
+  int32_t grad_dtype;    /* DMUON_DTYPE_F32 or DMUON_DTYPE_BF16 */
+  int64_t shape[4];
+  float* master;
+  float* momentum;
+  const void* grad;
+  uint16_t* param_bf16;
+} dmuon_matrix;
+
+/* One AdamW-route tensor, flattened: numel contiguous elements, all device
+ * pointers.  master/exp_avg/exp_avg_sq fp32 read+write, grad read only,
+ * param_bf16 written (may be NULL). */
+typedef struct dmuon_vector {
+  int64_t numel;
+  int32_t grad_dtype;    /* DMUON_DTYPE_F32 or DMUON_DTYPE_BF16 */
+  int32_t reserved;
+  float* master;
+  float* exp_avg;
+  float* exp_avg_sq;
+  const void* grad;
+  uint16_t* param_bf16;
+} dmuon_vector;
+
+typedef struct dmuon_context dmuon_context;
+
+/*
+ * dmuon_context_create -- a context bound to one CUDA device.
+ *   out     host, receives the new context
+ *   device  CUDA device ordinal (>= 0)
+ * Makes no allocation on the device; workspace is sized on first use and
+ * grows as needed.  Errors: DMUON_ERR_INVALID_ARG (null out, device < 0),
+ * DMUON_ERR_NOMEM (host allocation).
+ */
+DMUON_API int dmuon_context_create(dmuon_context** out, int32_t device);
+
+/* Frees every allocation of the context after waiting for its device work.
+ * NULL is accepted and ignored. */
+DMUON_API int dmuon_context_destroy(dmuon_context* ctx);
+
+/*
+ * dmuon_muon_step -- one owner-side Muon step over n tensors.
+ *
+ * For every 2-D slice (m x n) of every tensor, in fp32 unless noted:
+ *   buf <- mu*buf + g;  u <- g + mu*buf (NESTEROV) or u <- buf
+ *   X   <- u / (||u||_F + 1e-7), held as X (m <= n) or X^T (m > n) so that
+ *          the Gram matrix is p x p with p = min(m, n)
+ *   ns_steps times:  A = X X^T;  B = b*A + c*A*A;  X <- a*X + B X
+ *          (bf16 operands, fp32 accumulation; fp32 throughout with
+ *           DMUON_FLAG_FP32_NS)
+ *   W   <- W*(1 - lr*wd) - lr*sqrt(max(1, m/n))*X (in the original
+ *          orientation);  param_bf16 <- round-to-nearest-even(W)
+ *
+ *   ctx       from dmuon_context_create
+ *   mats      host array of n descriptors (read during the call only)
+ *   n         >= 0 (0 is a no-op)
+ *   lr, momentum, wd   finite; ns_steps in [0, 100]; a, b, c finite
+ *   flags     DMUON_FLAG_* bits
+ *   stream    cudaStream_t of the caller (void*)
+ *
+ * Errors: DMUON_ERR_INVALID_ARG, DMUON_ERR_RANK_LT2 (rank < 2),
+ * DMUON_ERR_SHAPE (rank > 4 or a dimension < 1), DMUON_ERR_DTYPE,
+ * DMUON_ERR_NOMEM (workspace), DMUON_ERR_CUDA, DMUON_ERR_UNSUPPORTED.
+ * Device-side waits inside the kernels are bounded; if one runs out the
+ * kernel records it and returns, and the next dmuon_sync() reports
+ * DMUON_ERR_TIMEOUT.  Calls on one context must not run concurrently on
+ * different streams (they share the context's workspace).
+ */
+DMUON_API int dmuon_muon_step(dmuon_context* ctx, const dmuon_matrix* mats, int32_t n,
+                    float lr, float momentum, float wd, int32_t ns_steps,
+                    float a, float b, float c, uint32_t flags, void* stream);
+
+/*
+ * dmuon_adamw_step -- one AdamW step over n flattened tensors ("Pure DMuon
+ * 路由": routes "adamw" and "sharded_adamw" both run AdamW; the shard
+ * placement is outside this call).  In fp32, per element:
+ *   m <- b1*m + (1-b1)*g;  v <- b2*v + (1-b2)*g^2
+ *   W <- W*(1 - lr*wd) - (lr/(1-b1^t)) * m / (sqrt(v)/sqrt(1-b2^t) + eps)
+ *   param_bf16 <- round-to-nearest-even(W)
+ *   step = t >= 1.  beta1, beta2 in [0, 1); eps >= 0; lr, wd finite.
+ * Errors as dmuon_muon_step.
+ */
+DMUON_API int dmuon_adamw_step(dmuon_context* ctx, const dmuon_vector* ts, int32_t n,
+                     float lr, float beta1, float beta2, float eps, float wd,
+                     int64_t step, void* stream);
+
+/*
+ * dmuon_sync -- wait for the stream and report device-side errors.
+ * Synchronises `stream`, then reads and clears the context's device error
+ * word.  Returns DMUON_ERR_TIMEOUT if a bounded wait ran out since the last
+ * call, DMUON_ERR_CUDA if the stream reported an error, else DMUON_OK.
+ */
+DMUON_API int dmuon_sync(dmuon_context* ctx, void* stream);
+
+/*
+ * dmuon_selftest_wait_timeout -- exercise the bounded-wait failure path.
+ * Launches one block that waits on a barrier nothing will complete, giving
+ * up after timeout_us microseconds (1..2,000,000); the kernel records the
+ * timeout and returns normally, leaving the context usable.  A following
+ * dmuon_sync() returns DMUON_ERR_TIMEOUT.  Used by the failure-detection
+ * tests; never part of an optimizer step.
+ */
+DMUON_API int dmuon_selftest_wait_timeout(dmuon_context* ctx, int32_t timeout_us, void* stream);
+
+/*
+ * dmuon_set_tuning -- process-wide tuning switches of the kernels.
+ *   key 1: operand-descriptor variant of the tcgen05 path for M/N-contiguous
+ *          operands (0 = LBO spans 64-element MN blocks, the default;
+ *          1 = the two offsets exchanged).  Kept for layout bring-up tests.
+ * Returns DMUON_ERR_INVALID_ARG for an unknown key.  Not thread-safe with
+ * respect to concurrent steps.
+ */
+DMUON_API int dmuon_set_tuning(int32_t key, int32_t value);
+
+/* Kernel kinds reported by dmuon_profile_read. */
+enum {
+  DMUON_KERNEL_MOMENTUM = 0, /* momentum + X0 + sum of squares      */
+  DMUON_KERNEL_NORM = 1,     /* per-slice 1/(||u|| + eps)            */
+  DMUON_KERNEL_NS_GRAM = 2,  /* A = X X^T (or X^T X)                 */
+  DMUON_KERNEL_NS_POLY = 3,  /* B = b A + c A A                      */
+  DMUON_KERNEL_NS_COMBINE = 4, /* X <- a X + B X (or a X + X B)      */
+  DMUON_KERNEL_UPDATE = 5,   /* weight decay + update + bf16 copy    */
+  DMUON_KERNEL_ADAMW = 6,
+  DMUON_KERNEL_KINDS = 7
+};
+
+/*
+ * dmuon_profile -- per-kernel device timing (tracing).
+ * With enable != 0 every later launch of the context is bracketed by two
+ * CUDA events recorded on the launching stream; with enable == 0 no events
+ * are recorded.  Errors: DMUON_ERR_INVALID_ARG for a null context.
+ */
+DMUON_API int dmuon_profile(dmuon_context* ctx, int32_t enable);
+
+/*
+ * dmuon_profile_read -- totals since the previous read, then reset.
+ *   ms_out     host, DMUON_KERNEL_KINDS doubles: summed device milliseconds
+ *   count_out  host, DMUON_KERNEL_KINDS int64: launches (may be NULL)
+ * Waits for the recorded events (host blocks until those launches finish).
+ * Errors: DMUON_ERR_INVALID_ARG (null ctx or ms_out), DMUON_ERR_CUDA.
+ */
+DMUON_API int dmuon_profile_read(dmuon_context* ctx, double* ms_out, int64_t* count_out);
+
+/*
+ * dmuon_kernel_launches -- number of kernels the context has launched since
+ * it was created (host-side count, for benchmarking).  Returns -1 for NULL.
+ */
+DMUON_API int64_t dmuon_kernel_launches(const dmuon_context* ctx);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DMUON_H */

@@ -1,0 +1,950 @@
+// C ABI of the owner-side Muon / AdamW step: validation, planning, workspace
+// and launch sequencing.  Every arithmetic step runs in the kernels of
+// k_stream.cu, k_ns_tc.cu and k_ns_simt.cu; this file only decides what runs
+// where.
+//
+// Plan (cached per shape set, rebuilt when the shapes or the precision mode
+// change):
+//  * every tensor of rank >= 2 is split into its 2-D slices (MindSpore
+//    hyper-parallel "分布式 Muon 优化器 — 参数分组设计文档（v2）" §2.2: the last
+//    two dims); slices of one shape form a class whose Newton-Schulz
+//    workspace is a contiguous [count, rows, ld] array, so one 3-D TMA
+//    tensor map covers the whole class;
+//  * X keeps the orientation of the gradient.  For m <= n the Gram matrix is
+//    X X^T and the last product B X; for m > n it is X^T X and X B.  The
+//    two forms are the same iteration (transpose equivariance), and no
+//    transpose pass is needed on the way in or out;
+//  * the tiles of each phase are spread over one persistent CTA per SM with
+//    the LPT greedy ("架构设计" §3.1), cost = k-blocks + epilogue.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <algorithm>
+#include <cmath>
+#include <new>
+#include <string>
+#include <vector>
+
+#include "../../include/dmuon.h"
+#include "host_util.h"
+#include "internal.h"
+
+namespace dmuon {
+
+void set_tc_mn_swap(int v);
+
+// ------------------------------------------------------------------ errors
+namespace {
+thread_local std::string g_last_error;
+}
+
+int set_error(int status, const char* msg) {
+  g_last_error = msg ? msg : "";
+  return status;
+}
+void clear_error() { g_last_error.clear(); }
+
+static int cuda_fail(cudaError_t e, const char* where) {
+  std::string m = std::string(where) + ": " + cudaGetErrorString(e);
+  return set_error(DMUON_ERR_CUDA, m.c_str());
+}
+
+#define DM_CUDA(call)                                        \
+  do {                                                       \
+    cudaError_t e_ = (call);                                 \
+    if (e_ != cudaSuccess) return cuda_fail(e_, #call);      \
+  } while (0)
+
+// ------------------------------------------------------- driver entry point
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn get_encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// ------------------------------------------------------------- device mem
+struct DevBuf {
+  void* p = nullptr;
+  size_t bytes = 0;
+  void release() {
+    if (p) cudaFree(p);
+    p = nullptr;
+    bytes = 0;
+  }
+};
+
+static int dev_alloc(DevBuf& b, size_t bytes) {
+  b.release();
+  if (bytes == 0) return DMUON_OK;
+  cudaError_t e = cudaMalloc(&b.p, bytes);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    b.p = nullptr;
+    std::string m = "cudaMalloc(" + std::to_string(bytes) + " bytes) failed: " + cudaGetErrorString(e);
+    return set_error(DMUON_ERR_NOMEM, m.c_str());
+  }
+  b.bytes = bytes;
+  return DMUON_OK;
+}
+
+template <class T>
+static int upload(DevBuf& b, const std::vector<T>& v) {
+  int st = dev_alloc(b, std::max<size_t>(v.size() * sizeof(T), 16));
+  if (st != DMUON_OK) return st;
+  if (!v.empty()) DM_CUDA(cudaMemcpy(b.p, v.data(), v.size() * sizeof(T), cudaMemcpyHostToDevice));
+  return DMUON_OK;
+}
+
+// Host table uploaded on the caller's stream through a pinned staging copy,
+// skipped when the contents did not change since the last upload.
+struct StagedTable {
+  DevBuf dev;
+  void* pinned = nullptr;
+  size_t cap = 0;
+  cudaEvent_t done = nullptr;
+  std::vector<uint8_t> last;
+  void release() {
+    dev.release();
+    if (pinned) cudaFreeHost(pinned);
+    pinned = nullptr;
+    cap = 0;
+    if (done) cudaEventDestroy(done);
+    done = nullptr;
+    last.clear();
+  }
+  int put(const void* data, size_t bytes, cudaStream_t st) {
+    if (bytes == last.size() && bytes > 0 && memcmp(data, last.data(), bytes) == 0) return DMUON_OK;
+    if (bytes > cap) {
+      if (done) DM_CUDA(cudaEventSynchronize(done));
+      if (pinned) cudaFreeHost(pinned);
+      pinned = nullptr;
+      cudaError_t e = cudaMallocHost(&pinned, bytes);
+      if (e != cudaSuccess) {
+        cudaGetLastError();
+        pinned = nullptr;
+        cap = 0;
+        return set_error(DMUON_ERR_NOMEM, "cudaMallocHost for a descriptor table failed");
+      }
+      cap = bytes;
+      int s = dev_alloc(dev, bytes);
+      if (s != DMUON_OK) return s;
+      last.clear();
+    }
+    if (!done) DM_CUDA(cudaEventCreateWithFlags(&done, cudaEventDisableTiming));
+    DM_CUDA(cudaEventSynchronize(done));  // previous copy out of `pinned` finished
+    memcpy(pinned, data, bytes);
+    DM_CUDA(cudaMemcpyAsync(dev.p, pinned, bytes, cudaMemcpyHostToDevice, st));
+    DM_CUDA(cudaEventRecord(done, st));
+    last.assign(static_cast<const uint8_t*>(data), static_cast<const uint8_t*>(data) + bytes);
+    return DMUON_OK;
+  }
+};
+
+// ------------------------------------------------------------------- plan
+struct SliceRef {
+  int32_t mat;
+  int64_t elem_offset;  // offset of the slice inside its tensor
+  int32_t cls;
+  int32_t z;            // index within the class
+};
+
+struct ShapeClass {
+  int32_t m, n, count;
+  bool tall;            // m > n: Gram is X^T X, last product X B
+  int64_t ld, ldp;      // workspace row pitch (elements) for X and for A/B
+  size_t off_x[2], off_a, off_b;  // byte offsets in the workspace
+  int32_t map_xk[2], map_xmn[2], map_a, map_b;
+};
+
+struct PhaseTiles {
+  int32_t n_tiles = 0;
+  int32_t n_ctas = 0;
+  DevBuf tiles, cta_begin;
+};
+
+struct MuonPlan {
+  std::string key;
+  bool fp32 = false;
+  std::vector<SliceRef> slices;
+  std::vector<ShapeClass> classes;
+  std::vector<Chunk> chunks;
+  std::vector<int32_t> slice_chunk_begin, slice_chunk_end;
+  size_t ws_bytes = 0;
+  DevBuf chunks_dev, partials, inv_norm, maps;
+  DevBuf probs[3][2];
+  PhaseTiles phase[3];
+  void release() {
+    chunks_dev.release();
+    partials.release();
+    inv_norm.release();
+    maps.release();
+    for (auto& k : probs)
+      for (auto& p : k) p.release();
+    for (auto& p : phase) {
+      p.tiles.release();
+      p.cta_begin.release();
+      p.n_tiles = p.n_ctas = 0;
+    }
+    slices.clear();
+    classes.clear();
+    chunks.clear();
+    key.clear();
+  }
+};
+
+struct AdamPlan {
+  std::string key;
+  std::vector<Chunk> chunks;
+  DevBuf chunks_dev;
+  void release() {
+    chunks_dev.release();
+    chunks.clear();
+    key.clear();
+  }
+};
+
+// Per-kernel device timing: events recorded around each launch on the
+// launching stream, resolved and summed on read.
+struct Profiler {
+  bool on = false;
+  std::vector<cudaEvent_t> pool;
+  struct Pending {
+    int kind;
+    cudaEvent_t a, b;
+  };
+  std::vector<Pending> pending;
+  double ms[DMUON_KERNEL_KINDS] = {};
+  int64_t count[DMUON_KERNEL_KINDS] = {};
+  cudaEvent_t get() {
+    if (!pool.empty()) {
+      cudaEvent_t e = pool.back();
+      pool.pop_back();
+      return e;
+    }
+    cudaEvent_t e = nullptr;
+    if (cudaEventCreate(&e) != cudaSuccess) {
+      cudaGetLastError();
+      return nullptr;
+    }
+    return e;
+  }
+  void release() {
+    for (auto& p : pending) {
+      cudaEventDestroy(p.a);
+      cudaEventDestroy(p.b);
+    }
+    pending.clear();
+    for (auto e : pool) cudaEventDestroy(e);
+    pool.clear();
+  }
+};
+
+}  // namespace dmuon
+
+struct dmuon_context {
+  int device = 0;
+  bool dev_ready = false;
+  int num_sms = 0;
+  int64_t launches = 0;
+  dmuon::DevBuf err;
+  dmuon::DevBuf ws;
+  dmuon::MuonPlan plan;
+  dmuon::AdamPlan adam;
+  dmuon::StagedTable slice_table, vec_table;
+  dmuon::Profiler prof;
+};
+
+namespace dmuon {
+namespace {
+
+struct DeviceGuard {
+  int prev = -1;
+  bool changed = false;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) == cudaSuccess && prev != dev) {
+      if (cudaSetDevice(dev) == cudaSuccess) changed = true;
+    }
+  }
+  ~DeviceGuard() {
+    if (changed) cudaSetDevice(prev);
+  }
+};
+
+bool finite(float x) { return std::isfinite(x); }
+
+int64_t round_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int ensure_device(dmuon_context* ctx) {
+  if (ctx->dev_ready) return DMUON_OK;
+  int count = 0;
+  cudaError_t e = cudaGetDeviceCount(&count);
+  if (e != cudaSuccess || count <= ctx->device) {
+    cudaGetLastError();
+    return set_error(DMUON_ERR_UNSUPPORTED, "no CUDA device with the context's ordinal");
+  }
+  cudaDeviceProp prop;
+  DM_CUDA(cudaGetDeviceProperties(&prop, ctx->device));
+  if (prop.major != 10)
+    return set_error(DMUON_ERR_UNSUPPORTED,
+                     "device is not of the sm_100 family (this library is built for sm_103a)");
+  ctx->num_sms = prop.multiProcessorCount;
+  int st = dev_alloc(ctx->err, 16);
+  if (st != DMUON_OK) return st;
+  DM_CUDA(cudaMemset(ctx->err.p, 0, 16));
+  ctx->dev_ready = true;
+  return DMUON_OK;
+}
+
+int validate_matrix(const dmuon_matrix& M, int idx) {
+  char buf[160];
+  if (M.rank < 2) {
+    snprintf(buf, sizeof buf, "tensor %d has rank %d; Muon needs rank >= 2 (route it to AdamW)", idx, M.rank);
+    return set_error(DMUON_ERR_RANK_LT2, buf);
+  }
+  if (M.rank > 4) {
+    snprintf(buf, sizeof buf, "tensor %d has rank %d > 4", idx, M.rank);
+    return set_error(DMUON_ERR_SHAPE, buf);
+  }
+  int64_t numel = 1;
+  for (int d = 0; d < M.rank; ++d) {
+    if (M.shape[d] < 1 || M.shape[d] > (int64_t(1) << 31)) {
+      snprintf(buf, sizeof buf, "tensor %d: dimension %d is %lld", idx, d, (long long)M.shape[d]);
+      return set_error(DMUON_ERR_SHAPE, buf);
+    }
+    numel *= M.shape[d];
+    if (numel > (int64_t(1) << 40)) {
+      snprintf(buf, sizeof buf, "tensor %d: more than 2^40 elements", idx);
+      return set_error(DMUON_ERR_SHAPE, buf);
+    }
+  }
+  const int64_t m = M.shape[M.rank - 2], n = M.shape[M.rank - 1];
+  if (m * n >= (int64_t(1) << 31) || m > 65535 * kTcBM || n > 65535 * kTcBM) {
+    snprintf(buf, sizeof buf, "tensor %d: a %lld x %lld slice is too large", idx, (long long)m, (long long)n);
+    return set_error(DMUON_ERR_SHAPE, buf);
+  }
+  if (!M.master || !M.momentum || !M.grad) {
+    snprintf(buf, sizeof buf, "tensor %d: null master, momentum or grad pointer", idx);
+    return set_error(DMUON_ERR_INVALID_ARG, buf);
+  }
+  if (M.grad_dtype != DMUON_DTYPE_F32 && M.grad_dtype != DMUON_DTYPE_BF16) {
+    snprintf(buf, sizeof buf, "tensor %d: grad dtype %d", idx, M.grad_dtype);
+    return set_error(DMUON_ERR_DTYPE, buf);
+  }
+  return DMUON_OK;
+}
+
+std::string plan_key(const dmuon_matrix* mats, int n, bool fp32) {
+  std::string k = fp32 ? "f32|" : "bf16|";
+  for (int i = 0; i < n; ++i) {
+    k += std::to_string(mats[i].rank);
+    for (int d = 0; d < mats[i].rank; ++d) k += ":" + std::to_string(mats[i].shape[d]);
+    k += ";";
+  }
+  return k;
+}
+
+int make_map(EncodeTiledFn enc, CUtensorMap* out, void* base, int64_t inner, int64_t rows,
+             int64_t count, int64_t ld, uint32_t box_inner, uint32_t box_rows) {
+  cuuint64_t dims[3] = {(cuuint64_t)inner, (cuuint64_t)rows, (cuuint64_t)count};
+  cuuint64_t strides[2] = {(cuuint64_t)(ld * 2), (cuuint64_t)(rows * ld * 2)};
+  cuuint32_t box[3] = {box_inner, box_rows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    char buf[200];
+    snprintf(buf, sizeof buf, "cuTensorMapEncodeTiled failed (%d) for a %lld x %lld x %lld map", (int)r,
+             (long long)inner, (long long)rows, (long long)count);
+    return set_error(DMUON_ERR_CUDA, buf);
+  }
+  return DMUON_OK;
+}
+
+// Build the tile list of one phase and balance it over persistent CTAs.
+int build_phase_tiles(const std::vector<NsProblem>& probs, bool fp32, int num_sms, PhaseTiles& out) {
+  const int bm = fp32 ? kSimtBM : kTcBM, bn = fp32 ? kSimtBN : kTcBN;
+  std::vector<uint2> tiles;
+  std::vector<int64_t> cost;
+  for (size_t p = 0; p < probs.size(); ++p) {
+    const NsProblem& P = probs[p];
+    const int tm = (P.M + bm - 1) / bm, tn = (P.N + bn - 1) / bn;
+    const int64_t c = (P.K + kTcBK - 1) / kTcBK + 2;
+    for (int i = 0; i < tm; ++i)
+      for (int j = 0; j < tn; ++j) {
+        tiles.push_back(make_uint2(static_cast<uint32_t>(p), (static_cast<uint32_t>(i) << 16) | static_cast<uint32_t>(j)));
+        cost.push_back(c);
+      }
+  }
+  out.n_tiles = static_cast<int32_t>(tiles.size());
+  if (fp32) {
+    out.n_ctas = out.n_tiles;
+    int st = upload(out.tiles, tiles);
+    if (st != DMUON_OK) return st;
+    return upload(out.cta_begin, std::vector<int32_t>{0, out.n_tiles});
+  }
+  const int R = std::max(1, std::min(num_sms, out.n_tiles));
+  std::vector<int32_t> slot(tiles.size());
+  std::vector<int32_t> order;
+  int st = lpt_assign_impl(cost.data(), out.n_tiles, R, slot.data(), nullptr, &order);
+  if (st != DMUON_OK) return st;
+  std::vector<int32_t> counts(static_cast<size_t>(R) + 1, 0);
+  for (int32_t t = 0; t < out.n_tiles; ++t) counts[static_cast<size_t>(slot[t]) + 1]++;
+  for (int r = 0; r < R; ++r) counts[r + 1] += counts[r];
+  std::vector<int32_t> fill(counts.begin(), counts.end() - 1);
+  std::vector<uint2> ordered(tiles.size());
+  for (int32_t t : order) ordered[static_cast<size_t>(fill[slot[t]]++)] = tiles[static_cast<size_t>(t)];
+  out.n_ctas = R;
+  st = upload(out.tiles, ordered);
+  if (st != DMUON_OK) return st;
+  return upload(out.cta_begin, counts);
+}
+
+int build_muon_plan(dmuon_context* ctx, const dmuon_matrix* mats, int n, bool fp32,
+                    const std::string& key) {
+  MuonPlan& P = ctx->plan;
+  P.release();
+  P.fp32 = fp32;
+  const int64_t es = fp32 ? 4 : 2;
+
+  // Slices and shape classes.
+  for (int i = 0; i < n; ++i) {
+    const dmuon_matrix& M = mats[i];
+    const int32_t m = static_cast<int32_t>(M.shape[M.rank - 2]);
+    const int32_t nn = static_cast<int32_t>(M.shape[M.rank - 1]);
+    int64_t lead = 1;
+    for (int d = 0; d < M.rank - 2; ++d) lead *= M.shape[d];
+    int cls = -1;
+    for (size_t c = 0; c < P.classes.size(); ++c)
+      if (P.classes[c].m == m && P.classes[c].n == nn) cls = static_cast<int>(c);
+    if (cls < 0) {
+      ShapeClass C{};
+      C.m = m;
+      C.n = nn;
+      C.count = 0;
+      C.tall = m > nn;
+      P.classes.push_back(C);
+      cls = static_cast<int>(P.classes.size()) - 1;
+    }
+    for (int64_t s = 0; s < lead; ++s) {
+      SliceRef r;
+      r.mat = i;
+      r.elem_offset = s * static_cast<int64_t>(m) * nn;
+      r.cls = cls;
+      r.z = P.classes[static_cast<size_t>(cls)].count++;
+      P.slices.push_back(r);
+    }
+  }
+  if (P.slices.size() > (size_t(1) << 30)) return set_error(DMUON_ERR_SHAPE, "too many slices");
+
+  // Workspace layout: per class X0, X1 [count, m, ld] and A, B [count, p, ldp].
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off += (bytes + 1023) & ~size_t(1023);
+    return o;
+  };
+  for (auto& C : P.classes) {
+    const int64_t p = std::min(C.m, C.n);
+    C.ld = round_up(C.n, 8);
+    C.ldp = round_up(p, 8);
+    for (int t = 0; t < 2; ++t) C.off_x[t] = take(static_cast<size_t>(C.count) * C.m * C.ld * es);
+    C.off_a = take(static_cast<size_t>(C.count) * p * C.ldp * es);
+    C.off_b = take(static_cast<size_t>(C.count) * p * C.ldp * es);
+  }
+  P.ws_bytes = std::max<size_t>(off, 1024);
+  if (ctx->ws.bytes < P.ws_bytes) {
+    ctx->ws.release();
+    int st = dev_alloc(ctx->ws, P.ws_bytes);
+    if (st != DMUON_OK) return st;
+  }
+  uint8_t* ws = static_cast<uint8_t*>(ctx->ws.p);
+
+  // Chunk table of the streaming passes.
+  P.slice_chunk_begin.resize(P.slices.size());
+  P.slice_chunk_end.resize(P.slices.size());
+  for (size_t s = 0; s < P.slices.size(); ++s) {
+    const ShapeClass& C = P.classes[static_cast<size_t>(P.slices[s].cls)];
+    const int64_t numel = static_cast<int64_t>(C.m) * C.n;
+    P.slice_chunk_begin[s] = static_cast<int32_t>(P.chunks.size());
+    for (int64_t st = 0; st < numel; st += kChunkElems) {
+      Chunk ch;
+      ch.slice = static_cast<int32_t>(s);
+      ch.start = st;
+      ch.count = static_cast<int32_t>(std::min<int64_t>(kChunkElems, numel - st));
+      P.chunks.push_back(ch);
+    }
+    P.slice_chunk_end[s] = static_cast<int32_t>(P.chunks.size());
+  }
+  if (P.chunks.size() > size_t(INT32_MAX)) return set_error(DMUON_ERR_SHAPE, "too many chunks");
+  int st = upload(P.chunks_dev, P.chunks);
+  if (st != DMUON_OK) return st;
+  st = dev_alloc(P.partials, std::max<size_t>(P.chunks.size(), 1) * sizeof(float));
+  if (st != DMUON_OK) return st;
+  st = dev_alloc(P.inv_norm, std::max<size_t>(P.slices.size(), 1) * sizeof(float));
+  if (st != DMUON_OK) return st;
+
+  // Tensor maps (tcgen05 path): per class X0/X1 K-major and MN-major, A, B.
+  std::vector<CUtensorMap> maps;
+  if (!fp32) {
+    EncodeTiledFn enc = get_encode_fn();
+    if (!enc) return set_error(DMUON_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    for (auto& C : P.classes) {
+      const int64_t p = std::min(C.m, C.n);
+      for (int t = 0; t < 2; ++t) {
+        CUtensorMap mk, mm;
+        st = make_map(enc, &mk, ws + C.off_x[t], C.n, C.m, C.count, C.ld, 64, 128);
+        if (st != DMUON_OK) return st;
+        st = make_map(enc, &mm, ws + C.off_x[t], C.n, C.m, C.count, C.ld, 64, 64);
+        if (st != DMUON_OK) return st;
+        C.map_xk[t] = static_cast<int32_t>(maps.size());
+        maps.push_back(mk);
+        C.map_xmn[t] = static_cast<int32_t>(maps.size());
+        maps.push_back(mm);
+      }
+      CUtensorMap ma, mb;
+      st = make_map(enc, &ma, ws + C.off_a, p, p, C.count, C.ldp, 64, 128);
+      if (st != DMUON_OK) return st;
+      st = make_map(enc, &mb, ws + C.off_b, p, p, C.count, C.ldp, 64, 128);
+      if (st != DMUON_OK) return st;
+      C.map_a = static_cast<int32_t>(maps.size());
+      maps.push_back(ma);
+      C.map_b = static_cast<int32_t>(maps.size());
+      maps.push_back(mb);
+    }
+    st = upload(P.maps, maps);
+    if (st != DMUON_OK) return st;
+  }
+
+  // Problems of the three phases, for X in buffer t (t = iteration parity).
+  for (int par = 0; par < 2; ++par) {
+    std::vector<NsProblem> gram, poly, comb;
+    for (size_t s = 0; s < P.slices.size(); ++s) {
+      const SliceRef& R = P.slices[s];
+      const ShapeClass& C = P.classes[static_cast<size_t>(R.cls)];
+      const int32_t p = std::min(C.m, C.n), q = std::max(C.m, C.n);
+      uint8_t* X = ws + C.off_x[par] + static_cast<size_t>(R.z) * C.m * C.ld * es;
+      uint8_t* Xn = ws + C.off_x[par ^ 1] + static_cast<size_t>(R.z) * C.m * C.ld * es;
+      uint8_t* A = ws + C.off_a + static_cast<size_t>(R.z) * p * C.ldp * es;
+      uint8_t* B = ws + C.off_b + static_cast<size_t>(R.z) * p * C.ldp * es;
+      NsProblem g{}, y{}, c{};
+      g.slice = y.slice = c.slice = static_cast<int32_t>(s);
+      g.z = y.z = c.z = R.z;
+      // Gram: p x p, K = q.
+      g.M = g.N = p;
+      g.K = q;
+      g.a = g.b = X;
+      g.out = A;
+      g.ld_out = C.ldp;
+      g.aux = nullptr;
+      if (!C.tall) {  // A = X X^T: A_op(i,k) = X[i,k], B_op(k,j) = X[j,k]
+        g.a_si = C.ld; g.a_sk = 1; g.b_sk = 1; g.b_sj = C.ld;
+        g.map_a = g.map_b = C.map_xk[par];
+        g.majors = 0;
+      } else {        // A = X^T X: A_op(i,k) = X[k,i], B_op(k,j) = X[k,j]
+        g.a_si = 1; g.a_sk = C.ld; g.b_sk = C.ld; g.b_sj = 1;
+        g.map_a = g.map_b = C.map_xmn[par];
+        g.majors = 3;
+      }
+      // Poly: B = b A + c A A, A symmetric so B_op(k,j) = A[k,j] = A[j,k].
+      y.M = y.N = y.K = p;
+      y.a = y.b = A;
+      y.a_si = C.ldp; y.a_sk = 1; y.b_sk = C.ldp; y.b_sj = 1;
+      y.map_a = y.map_b = C.map_a;
+      y.majors = 0;
+      y.out = B;
+      y.ld_out = C.ldp;
+      y.aux = A;
+      y.ld_aux = C.ldp;
+      // Combine: X' = a X + B X (wide) or a X + X B (tall).
+      c.out = Xn;
+      c.ld_out = C.ld;
+      c.aux = X;
+      c.ld_aux = C.ld;
+      if (!C.tall) {  // M = p, N = q, K = p: A_op = B, B_op(k,j) = X[k,j]
+        c.M = p; c.N = q; c.K = p;
+        c.a = B; c.a_si = C.ldp; c.a_sk = 1;
+        c.b = X; c.b_sk = C.ld; c.b_sj = 1;
+        c.map_a = C.map_b;
+        c.map_b = C.map_xmn[par];
+        c.majors = 2;
+      } else {        // M = q, N = p, K = p: A_op = X, B_op(k,j) = B[k,j] = B[j,k]
+        c.M = q; c.N = p; c.K = p;
+        c.a = X; c.a_si = C.ld; c.a_sk = 1;
+        c.b = B; c.b_sk = C.ldp; c.b_sj = 1;
+        c.map_a = C.map_xk[par];
+        c.map_b = C.map_b;
+        c.majors = 0;
+      }
+      gram.push_back(g);
+      poly.push_back(y);
+      comb.push_back(c);
+    }
+    st = upload(P.probs[kGram][par], gram);
+    if (st != DMUON_OK) return st;
+    st = upload(P.probs[kPoly][par], poly);
+    if (st != DMUON_OK) return st;
+    st = upload(P.probs[kCombine][par], comb);
+    if (st != DMUON_OK) return st;
+    if (par == 0) {
+      st = build_phase_tiles(gram, fp32, ctx->num_sms, P.phase[kGram]);
+      if (st != DMUON_OK) return st;
+      st = build_phase_tiles(poly, fp32, ctx->num_sms, P.phase[kPoly]);
+      if (st != DMUON_OK) return st;
+      st = build_phase_tiles(comb, fp32, ctx->num_sms, P.phase[kCombine]);
+      if (st != DMUON_OK) return st;
+    }
+  }
+  P.key = key;
+  return DMUON_OK;
+}
+
+// Run one launch, counting it and (when profiling) bracketing it with events.
+template <class F>
+int timed_launch(dmuon_context* ctx, int kind, cudaStream_t s, F&& launch) {
+  Profiler& P = ctx->prof;
+  cudaEvent_t a = nullptr, b = nullptr;
+  if (P.on) {
+    a = P.get();
+    b = P.get();
+    if (a) cudaEventRecord(a, s);
+  }
+  cudaError_t e = launch();
+  if (e != cudaSuccess) {
+    if (a) P.pool.push_back(a);
+    if (b) P.pool.push_back(b);
+    return cuda_fail(e, "kernel launch");
+  }
+  ctx->launches++;
+  if (P.on && a && b) {
+    cudaEventRecord(b, s);
+    P.pending.push_back({kind, a, b});
+  }
+  return DMUON_OK;
+}
+
+}  // namespace
+}  // namespace dmuon
+
+using namespace dmuon;
+
+extern "C" {
+
+const char* dmuon_status_string(int status) {
+  switch (status) {
+    case DMUON_OK: return "ok";
+    case DMUON_ERR_INVALID_ARG: return "invalid argument";
+    case DMUON_ERR_RANK_LT2: return "Muon tensor of rank < 2";
+    case DMUON_ERR_SHAPE: return "unsupported shape";
+    case DMUON_ERR_DTYPE: return "unsupported dtype";
+    case DMUON_ERR_CUDA: return "CUDA error";
+    case DMUON_ERR_TIMEOUT: return "device-side wait timed out";
+    case DMUON_ERR_NOMEM: return "out of memory";
+    case DMUON_ERR_UNSUPPORTED: return "unsupported device";
+    default: return "unknown status";
+  }
+}
+
+const char* dmuon_last_error(void) { return g_last_error.c_str(); }
+
+int dmuon_context_create(dmuon_context** out, int32_t device) {
+  clear_error();
+  if (!out || device < 0) return set_error(DMUON_ERR_INVALID_ARG, "context_create: null out or negative device");
+  dmuon_context* c = new (std::nothrow) dmuon_context();
+  if (!c) return set_error(DMUON_ERR_NOMEM, "context_create: host allocation failed");
+  c->device = device;
+  *out = c;
+  return DMUON_OK;
+}
+
+int dmuon_context_destroy(dmuon_context* ctx) {
+  clear_error();
+  if (!ctx) return DMUON_OK;
+  if (ctx->dev_ready) {
+    DeviceGuard g(ctx->device);
+    cudaDeviceSynchronize();
+    ctx->plan.release();
+    ctx->adam.release();
+    ctx->slice_table.release();
+    ctx->vec_table.release();
+    ctx->prof.release();
+    ctx->ws.release();
+    ctx->err.release();
+  }
+  delete ctx;
+  return DMUON_OK;
+}
+
+int64_t dmuon_kernel_launches(const dmuon_context* ctx) { return ctx ? ctx->launches : -1; }
+
+int dmuon_muon_step(dmuon_context* ctx, const dmuon_matrix* mats, int32_t n, float lr,
+                    float momentum, float wd, int32_t ns_steps, float a, float b, float c,
+                    uint32_t flags, void* stream) {
+  clear_error();
+  if (!ctx) return set_error(DMUON_ERR_INVALID_ARG, "muon_step: null context");
+  if (n < 0 || (n > 0 && !mats)) return set_error(DMUON_ERR_INVALID_ARG, "muon_step: bad tensor list");
+  if (!finite(lr) || !finite(momentum) || !finite(wd) || !finite(a) || !finite(b) || !finite(c))
+    return set_error(DMUON_ERR_INVALID_ARG, "muon_step: non-finite hyper-parameter");
+  if (ns_steps < 0 || ns_steps > 100) return set_error(DMUON_ERR_INVALID_ARG, "muon_step: ns_steps outside [0, 100]");
+  if (flags & ~uint32_t(DMUON_FLAG_NESTEROV | DMUON_FLAG_FP32_NS))
+    return set_error(DMUON_ERR_INVALID_ARG, "muon_step: unknown flag bits");
+  for (int i = 0; i < n; ++i) {
+    int st = validate_matrix(mats[i], i);
+    if (st != DMUON_OK) return st;
+  }
+  if (n == 0) return DMUON_OK;
+
+  DeviceGuard guard(ctx->device);
+  int st = ensure_device(ctx);
+  if (st != DMUON_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const bool fp32 = (flags & DMUON_FLAG_FP32_NS) != 0;
+  const std::string key = plan_key(mats, n, fp32);
+  MuonPlan& P = ctx->plan;
+  if (key != P.key) {
+    st = build_muon_plan(ctx, mats, n, fp32, key);
+    if (st != DMUON_OK) {
+      P.release();
+      return st;
+    }
+  }
+  const int64_t es = fp32 ? 4 : 2;
+  uint8_t* ws = static_cast<uint8_t*>(ctx->ws.p);
+
+  // Per-call pointer table.
+  std::vector<SliceDesc> table(P.slices.size());
+  for (size_t i = 0; i < P.slices.size(); ++i) {
+    const SliceRef& R = P.slices[i];
+    const ShapeClass& C = P.classes[static_cast<size_t>(R.cls)];
+    const dmuon_matrix& M = mats[R.mat];
+    SliceDesc& D = table[i];
+    memset(&D, 0, sizeof D);
+    D.master = M.master + R.elem_offset;
+    D.momentum = M.momentum + R.elem_offset;
+    D.grad_bf16 = M.grad_dtype == DMUON_DTYPE_BF16;
+    D.grad = static_cast<const uint8_t*>(M.grad) + R.elem_offset * (D.grad_bf16 ? 2 : 4);
+    D.param = M.param_bf16 ? M.param_bf16 + R.elem_offset : nullptr;
+    const size_t xoff = static_cast<size_t>(R.z) * C.m * C.ld * es;
+    D.x0 = ws + C.off_x[0] + xoff;
+    D.xk = ws + C.off_x[ns_steps & 1] + xoff;
+    D.ld = C.ld;
+    D.m = C.m;
+    D.n = C.n;
+    D.vec_ok = (C.n % 8 == 0) && aligned16(D.master) && aligned16(D.momentum) &&
+               aligned16(D.grad) && (!D.param || aligned16(D.param));
+    D.shape_scale = static_cast<float>(std::sqrt(std::max(1.0, double(C.m) / double(C.n))));
+    D.chunk_begin = P.slice_chunk_begin[i];
+    D.chunk_end = P.slice_chunk_end[i];
+  }
+  st = ctx->slice_table.put(table.data(), table.size() * sizeof(SliceDesc), s);
+  if (st != DMUON_OK) return st;
+  const SliceDesc* d_slices = static_cast<const SliceDesc*>(ctx->slice_table.dev.p);
+  const Chunk* d_chunks = static_cast<const Chunk*>(P.chunks_dev.p);
+  float* partials = static_cast<float*>(P.partials.p);
+  float* inv_norm = static_cast<float*>(P.inv_norm.p);
+  const int n_chunks = static_cast<int>(P.chunks.size());
+
+  const int nesterov = (flags & DMUON_FLAG_NESTEROV) ? 1 : 0;
+  st = timed_launch(ctx, DMUON_KERNEL_MOMENTUM, s, [&] {
+    return launch_momentum(d_slices, d_chunks, n_chunks, momentum, nesterov, fp32 ? 1 : 0, partials, s);
+  });
+  if (st != DMUON_OK) return st;
+  st = timed_launch(ctx, DMUON_KERNEL_NORM, s, [&] {
+    return launch_norm(d_slices, static_cast<int>(P.slices.size()), partials, inv_norm, s);
+  });
+  if (st != DMUON_OK) return st;
+  for (int it = 0; it < ns_steps; ++it) {
+    const int par = it & 1;
+    for (int kind = kGram; kind <= kCombine; ++kind) {
+      NsLaunch L{};
+      L.probs = static_cast<const NsProblem*>(P.probs[kind][par].p);
+      L.tiles = static_cast<const uint2*>(P.phase[kind].tiles.p);
+      L.cta_begin = static_cast<const int32_t*>(P.phase[kind].cta_begin.p);
+      L.maps = static_cast<const CUtensorMap*>(P.maps.p);
+      L.gscale = (it == 0 && kind != kPoly) ? inv_norm : nullptr;
+      L.gpow = (kind == kGram) ? 2 : 1;
+      L.kind = kind;
+      L.a = a;
+      L.b = b;
+      L.c = c;
+      L.err = static_cast<int*>(ctx->err.p);
+      const PhaseTiles& T = P.phase[kind];
+      st = timed_launch(ctx, DMUON_KERNEL_NS_GRAM + kind, s, [&] {
+        return fp32 ? launch_ns_simt(L, T.n_tiles, s) : launch_ns_tc(L, T.n_ctas, s);
+      });
+      if (st != DMUON_OK) return st;
+    }
+  }
+  return timed_launch(ctx, DMUON_KERNEL_UPDATE, s, [&] {
+    return launch_update(d_slices, d_chunks, n_chunks, lr, wd, fp32 ? 1 : 0,
+                         ns_steps == 0 ? inv_norm : nullptr, s);
+  });
+}
+
+int dmuon_adamw_step(dmuon_context* ctx, const dmuon_vector* ts, int32_t n, float lr, float beta1,
+                     float beta2, float eps, float wd, int64_t step, void* stream) {
+  clear_error();
+  if (!ctx) return set_error(DMUON_ERR_INVALID_ARG, "adamw_step: null context");
+  if (n < 0 || (n > 0 && !ts)) return set_error(DMUON_ERR_INVALID_ARG, "adamw_step: bad tensor list");
+  if (!finite(lr) || !finite(wd) || !finite(eps) || eps < 0.f || !(beta1 >= 0.f && beta1 < 1.f) ||
+      !(beta2 >= 0.f && beta2 < 1.f))
+    return set_error(DMUON_ERR_INVALID_ARG, "adamw_step: bad hyper-parameter");
+  if (step < 1) return set_error(DMUON_ERR_INVALID_ARG, "adamw_step: step counter must be >= 1");
+  for (int i = 0; i < n; ++i) {
+    const dmuon_vector& V = ts[i];
+    char buf[120];
+    if (V.numel < 0 || V.numel > (int64_t(1) << 40)) {
+      snprintf(buf, sizeof buf, "adamw tensor %d: numel %lld", i, (long long)V.numel);
+      return set_error(DMUON_ERR_SHAPE, buf);
+    }
+    if (V.numel > 0 && (!V.master || !V.exp_avg || !V.exp_avg_sq || !V.grad)) {
+      snprintf(buf, sizeof buf, "adamw tensor %d: null pointer", i);
+      return set_error(DMUON_ERR_INVALID_ARG, buf);
+    }
+    if (V.grad_dtype != DMUON_DTYPE_F32 && V.grad_dtype != DMUON_DTYPE_BF16) {
+      snprintf(buf, sizeof buf, "adamw tensor %d: grad dtype %d", i, V.grad_dtype);
+      return set_error(DMUON_ERR_DTYPE, buf);
+    }
+  }
+  if (n == 0) return DMUON_OK;
+  DeviceGuard guard(ctx->device);
+  int st = ensure_device(ctx);
+  if (st != DMUON_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  std::string key;
+  for (int i = 0; i < n; ++i) key += std::to_string(ts[i].numel) + ";";
+  AdamPlan& A = ctx->adam;
+  if (key != A.key) {
+    A.release();
+    for (int i = 0; i < n; ++i)
+      for (int64_t e = 0; e < ts[i].numel; e += kChunkElems) {
+        Chunk ch;
+        ch.slice = i;
+        ch.start = e;
+        ch.count = static_cast<int32_t>(std::min<int64_t>(kChunkElems, ts[i].numel - e));
+        A.chunks.push_back(ch);
+      }
+    if (A.chunks.size() > size_t(INT32_MAX)) return set_error(DMUON_ERR_SHAPE, "too many chunks");
+    st = upload(A.chunks_dev, A.chunks);
+    if (st != DMUON_OK) {
+      A.release();
+      return st;
+    }
+    A.key = key;
+  }
+  std::vector<VecDesc> table(static_cast<size_t>(n));
+  for (int i = 0; i < n; ++i) {
+    VecDesc& D = table[static_cast<size_t>(i)];
+    memset(&D, 0, sizeof D);
+    D.master = ts[i].master;
+    D.exp_avg = ts[i].exp_avg;
+    D.exp_avg_sq = ts[i].exp_avg_sq;
+    D.grad = ts[i].grad;
+    D.param = ts[i].param_bf16;
+    D.grad_bf16 = ts[i].grad_dtype == DMUON_DTYPE_BF16;
+    D.vec_ok = aligned16(D.master) && aligned16(D.exp_avg) && aligned16(D.exp_avg_sq) &&
+               aligned16(D.grad) && (!D.param || aligned16(D.param));
+  }
+  st = ctx->vec_table.put(table.data(), table.size() * sizeof(VecDesc), s);
+  if (st != DMUON_OK) return st;
+  const double bc1 = 1.0 - std::pow(double(beta1), double(step));
+  const double bc2 = 1.0 - std::pow(double(beta2), double(step));
+  return timed_launch(ctx, DMUON_KERNEL_ADAMW, s, [&] {
+    return launch_adamw(static_cast<const VecDesc*>(ctx->vec_table.dev.p),
+                        static_cast<const Chunk*>(A.chunks_dev.p), static_cast<int>(A.chunks.size()),
+                        lr, beta1, beta2, eps, wd, static_cast<float>(bc1),
+                        static_cast<float>(std::sqrt(bc2)), s);
+  });
+}
+
+int dmuon_sync(dmuon_context* ctx, void* stream) {
+  clear_error();
+  if (!ctx) return set_error(DMUON_ERR_INVALID_ARG, "sync: null context");
+  if (!ctx->dev_ready) return DMUON_OK;
+  DeviceGuard guard(ctx->device);
+  DM_CUDA(cudaStreamSynchronize(static_cast<cudaStream_t>(stream)));
+  int word = 0;
+  DM_CUDA(cudaMemcpy(&word, ctx->err.p, sizeof(int), cudaMemcpyDeviceToHost));
+  if (word != kErrNone) {
+    DM_CUDA(cudaMemset(ctx->err.p, 0, sizeof(int)));
+    char buf[96];
+    snprintf(buf, sizeof buf, "a bounded device-side wait ran out (site %d)", word);
+    return set_error(DMUON_ERR_TIMEOUT, buf);
+  }
+  return DMUON_OK;
+}
+
+int dmuon_selftest_wait_timeout(dmuon_context* ctx, int32_t timeout_us, void* stream) {
+  clear_error();
+  if (!ctx) return set_error(DMUON_ERR_INVALID_ARG, "selftest: null context");
+  if (timeout_us < 1 || timeout_us > 2000000)
+    return set_error(DMUON_ERR_INVALID_ARG, "selftest: timeout_us outside [1, 2000000]");
+  DeviceGuard guard(ctx->device);
+  int st = ensure_device(ctx);
+  if (st != DMUON_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return timed_launch(ctx, -1, s, [&] {
+    return launch_selftest_wait(static_cast<int*>(ctx->err.p), 1000ll * timeout_us, s);
+  });
+}
+
+int dmuon_profile(dmuon_context* ctx, int32_t enable) {
+  clear_error();
+  if (!ctx) return set_error(DMUON_ERR_INVALID_ARG, "profile: null context");
+  ctx->prof.on = enable != 0;
+  return DMUON_OK;
+}
+
+int dmuon_profile_read(dmuon_context* ctx, double* ms_out, int64_t* count_out) {
+  clear_error();
+  if (!ctx || !ms_out) return set_error(DMUON_ERR_INVALID_ARG, "profile_read: null argument");
+  Profiler& P = ctx->prof;
+  DeviceGuard guard(ctx->device);
+  for (auto& p : P.pending) {
+    DM_CUDA(cudaEventSynchronize(p.b));
+    float ms = 0.f;
+    DM_CUDA(cudaEventElapsedTime(&ms, p.a, p.b));
+    if (p.kind >= 0 && p.kind < DMUON_KERNEL_KINDS) {
+      P.ms[p.kind] += ms;
+      P.count[p.kind] += 1;
+    }
+    P.pool.push_back(p.a);
+    P.pool.push_back(p.b);
+  }
+  P.pending.clear();
+  for (int k = 0; k < DMUON_KERNEL_KINDS; ++k) {
+    ms_out[k] = P.ms[k];
+    if (count_out) count_out[k] = P.count[k];
+    P.ms[k] = 0.0;
+    P.count[k] = 0;
+  }
+  return DMUON_OK;
+}
+
+int dmuon_set_tuning(int32_t key, int32_t value) {
+  clear_error();
+  if (key == 1) {
+    set_tc_mn_swap(value ? 1 : 0);
+    return DMUON_OK;
+  }
+  return set_error(DMUON_ERR_INVALID_ARG, "set_tuning: unknown key");
+}
+
+}  // extern "C"

@@ -1,0 +1,19 @@
+// Host-side helpers shared by the C ABI translation units.
+#pragma once
+
+#include <stdint.h>
+
+#include <vector>
+
+namespace dmuon {
+
+// Record `msg` as the calling thread's last error and return `status`.
+int set_error(int status, const char* msg);
+void clear_error();
+
+// LPT core (see lpt.cpp).  When `order_out` is given it receives the order
+// in which items were placed (descending size, ties by index).
+int lpt_assign_impl(const int64_t* sizes, int32_t n_items, int32_t n_slots, int32_t* out_slot,
+                    int64_t* out_load, std::vector<int32_t>* order_out);
+
+}  // namespace dmuon

@@ -1,0 +1,125 @@
+// Internal types shared by the host planner (api.cu) and the kernels.
+// Not part of the public ABI (include/dmuon.h is).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace dmuon {
+
+// Device error word values (written by kernels, read by dmuon_sync).
+enum : int {
+  kErrNone = 0,
+  kErrTimeoutProducer = 1,
+  kErrTimeoutMma = 2,
+  kErrTimeoutEpilogue = 3,
+  kErrTimeoutDrain = 4,
+  kErrTimeoutSelftest = 5,
+};
+
+// One 2-D slice (m x n, row-major, contiguous) of a Muon tensor, as the two
+// streaming passes see it.  Pointers already point at the slice's first
+// element.  The Newton-Schulz workspace holds the slice as m rows of `ld`
+// elements (ld >= n, padded so every row starts on a 16-byte boundary).
+struct SliceDesc {
+  float* master;
+  float* momentum;
+  const void* grad;
+  uint16_t* param;        // may be null
+  void* x0;               // workspace: X before the first iteration
+  const void* xk;         // workspace: X after the last iteration
+  int64_t ld;             // workspace row pitch, elements
+  int32_t m, n;
+  int32_t grad_bf16;      // 1: grad is bf16, 0: fp32
+  int32_t vec_ok;         // 1: n % 8 == 0 and every pointer 16-byte aligned
+  float shape_scale;      // sqrt(max(1, m/n))
+  int32_t chunk_begin;    // first chunk of this slice in the chunk table
+  int32_t chunk_end;
+  int32_t pad_;
+};
+
+// A contiguous run of one slice's elements (row-major element index of the
+// m x n slice).  Start is a multiple of 8.
+struct Chunk {
+  int32_t slice;
+  int32_t count;
+  int64_t start;
+};
+
+// One AdamW tensor for the element-wise kernel.
+struct VecDesc {
+  float* master;
+  float* exp_avg;
+  float* exp_avg_sq;
+  const void* grad;
+  uint16_t* param;
+  int32_t grad_bf16;
+  int32_t vec_ok;
+};
+
+// One product of a Newton-Schulz phase: D(MxN) = A_op(MxK) * B_op(KxN),
+// then an epilogue that depends on the phase kind (see NsKind).
+//  - Raw view (used by the fp32 CUDA-core path): A_op(i,k) = a[i*a_si + k*a_sk],
+//    B_op(k,j) = b[k*b_sk + j*b_sj].
+//  - Tensor-map view (used by the tcgen05 path): operand tiles are loaded with
+//    TMA from maps[map_a] / maps[map_b] at slice coordinate z; bit 0 of
+//    `majors` marks A_op as M-contiguous in memory, bit 1 marks B_op as
+//    N-contiguous (otherwise the operand is K-contiguous).
+struct NsProblem {
+  const void* a;
+  const void* b;
+  int64_t a_si, a_sk, b_sk, b_sj;
+  void* out;
+  const void* aux;
+  int64_t ld_out, ld_aux;
+  int32_t M, N, K;
+  int32_t slice;          // global slice index (norm table)
+  int32_t map_a, map_b;
+  int32_t z;
+  int32_t majors;
+};
+
+// Phase kinds of one Newton-Schulz iteration.
+//   kGram:    out = g^p * acc                 (A = X X^T)
+//   kPoly:    out = c * acc + b * aux          (B = b A + c A A, aux = A)
+//   kCombine: out = g^p * (acc + a * aux)      (X' = a X + B X, aux = X)
+// g = 1/(||u||+eps) of the slice when the fold-in of the normalisation is
+// active (first iteration), p = gpow; g^0 = 1.
+enum NsKind : int { kGram = 0, kPoly = 1, kCombine = 2 };
+
+struct NsLaunch {
+  const NsProblem* probs;
+  const uint2* tiles;       // x = problem index, y = (tile_m << 16) | tile_n
+  const int32_t* cta_begin; // per persistent CTA: tiles[cta_begin[i] .. cta_begin[i+1])
+  const CUtensorMap* maps;  // tcgen05 path only
+  const float* gscale;      // per-slice 1/(||u||+eps), or null
+  int32_t gpow;
+  int32_t kind;
+  float a, b, c;
+  int* err;
+};
+
+// ---- launch wrappers (each returns the cudaError_t of its launch) ----
+cudaError_t launch_momentum(const SliceDesc* slices, const Chunk* chunks, int n_chunks,
+                            float mu, int nesterov, int x_fp32, float* partials,
+                            cudaStream_t st);
+cudaError_t launch_norm(const SliceDesc* slices, int n_slices, const float* partials,
+                        float* inv_norm, cudaStream_t st);
+cudaError_t launch_update(const SliceDesc* slices, const Chunk* chunks, int n_chunks,
+                          float lr, float wd, int x_fp32, const float* xscale,
+                          cudaStream_t st);
+cudaError_t launch_adamw(const VecDesc* vecs, const Chunk* chunks, int n_chunks,
+                         float lr, float beta1, float beta2, float eps, float wd,
+                         float bc1, float bc2_sqrt, cudaStream_t st);
+cudaError_t launch_selftest_wait(int* err, long long timeout_ns, cudaStream_t st);
+
+cudaError_t launch_ns_tc(const NsLaunch& L, int n_ctas, cudaStream_t st);
+cudaError_t launch_ns_simt(const NsLaunch& L, int n_tiles, cudaStream_t st);
+
+// Tile geometry of the two Newton-Schulz GEMM paths.
+constexpr int kTcBM = 128, kTcBN = 256, kTcBK = 64;
+constexpr int kSimtBM = 64, kSimtBN = 64;
+constexpr int kChunkElems = 1 << 16;
+
+}  // namespace dmuon

@@ -1,0 +1,112 @@
+"""User-facing wrapper: one owner's Muon and AdamW tensors on one GPU.
+
+``OwnerStep`` keeps a library context and the descriptor arrays of a fixed
+set of torch tensors, so a training loop calls ``muon_step`` /
+``adamw_step`` without re-marshalling pointers every step.  It only
+marshals: every step runs in the CUDA library through the C ABI.
+"""
+
+from __future__ import annotations
+
+import torch
+
+from . import capi
+
+
+def _check_tensor(t, name, dtypes, like=None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype not in dtypes:
+        raise TypeError(f"{name} has dtype {t.dtype}, expected one of {dtypes}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if like is not None and tuple(t.shape) != tuple(like.shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(like.shape)}")
+
+
+class OwnerStep:
+    """Muon-route matrices and AdamW-route tensors owned by this process."""
+
+    def __init__(self, device=0):
+        self.device = int(device)
+        self.ctx = capi.dmuon_context_create(self.device)
+        self._mats = None
+        self._n_mats = 0
+        self._vecs = None
+        self._n_vecs = 0
+        self._keep = []
+
+    # -------------------------------------------------------------- Muon
+    def set_muon(self, masters, momenta, grads, params=None):
+        """Register the Muon tensors: fp32 masters/momenta, bf16 or fp32 grads,
+        optional bf16 params (same shapes, rank >= 2, contiguous)."""
+        params = params if params is not None else [None] * len(masters)
+        descs = []
+        for i, (w, b, g, p) in enumerate(zip(masters, momenta, grads, params)):
+            _check_tensor(w, f"master[{i}]", (torch.float32,))
+            _check_tensor(b, f"momentum[{i}]", (torch.float32,), like=w)
+            _check_tensor(g, f"grad[{i}]", (torch.float32, torch.bfloat16), like=w)
+            if p is not None:
+                _check_tensor(p, f"param[{i}]", (torch.bfloat16,), like=w)
+            if w.dim() > 4:
+                raise ValueError(f"master[{i}] has rank {w.dim()} > 4")
+            descs.append(capi.matrix_desc(w, b, g, p))
+        self._mats = capi.descriptor_array(descs, capi.DmuonMatrix)
+        self._n_mats = len(descs)
+        self._keep = [masters, momenta, grads, params]
+
+    def muon_step(self, lr, momentum, wd, ns_steps=5, a=3.4445, b=-4.7750, c=2.0315,
+                  nesterov=True, fp32_ns=False, stream=None):
+        if self._mats is None:
+            raise RuntimeError("set_muon() first")
+        flags = (capi.DMUON_FLAG_NESTEROV if nesterov else 0) | (capi.DMUON_FLAG_FP32_NS if fp32_ns else 0)
+        capi._check(capi.load_library().dmuon_muon_step(
+            self.ctx, self._mats, self._n_mats, float(lr), float(momentum), float(wd), int(ns_steps),
+            float(a), float(b), float(c), flags, capi._stream_handle(stream)))
+
+    # ------------------------------------------------------------- AdamW
+    def set_adamw(self, masters, exp_avgs, exp_avg_sqs, grads, params=None):
+        params = params if params is not None else [None] * len(masters)
+        descs = []
+        for i, (w, m, v, g, p) in enumerate(zip(masters, exp_avgs, exp_avg_sqs, grads, params)):
+            _check_tensor(w, f"master[{i}]", (torch.float32,))
+            _check_tensor(m, f"exp_avg[{i}]", (torch.float32,), like=w)
+            _check_tensor(v, f"exp_avg_sq[{i}]", (torch.float32,), like=w)
+            _check_tensor(g, f"grad[{i}]", (torch.float32, torch.bfloat16), like=w)
+            if p is not None:
+                _check_tensor(p, f"param[{i}]", (torch.bfloat16,), like=w)
+            descs.append(capi.vector_desc(w, m, v, g, p))
+        self._vecs = capi.descriptor_array(descs, capi.DmuonVector)
+        self._n_vecs = len(descs)
+        self._keep_adam = [masters, exp_avgs, exp_avg_sqs, grads, params]
+
+    def adamw_step(self, lr, beta1, beta2, eps, wd, step, stream=None):
+        if self._vecs is None:
+            raise RuntimeError("set_adamw() first")
+        capi._check(capi.load_library().dmuon_adamw_step(
+            self.ctx, self._vecs, self._n_vecs, float(lr), float(beta1), float(beta2), float(eps),
+            float(wd), int(step), capi._stream_handle(stream)))
+
+    # ------------------------------------------------------------ misc
+    def sync(self, stream=None):
+        capi.dmuon_sync(self.ctx, stream)
+
+    def profile(self, enable=True):
+        capi.dmuon_profile(self.ctx, enable)
+
+    def profile_read(self):
+        return capi.dmuon_profile_read(self.ctx)
+
+    def kernel_launches(self):
+        return capi.dmuon_kernel_launches(self.ctx)
+
+    def close(self):
+        if self.ctx is not None:
+            capi.dmuon_context_destroy(self.ctx)
+            self.ctx = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

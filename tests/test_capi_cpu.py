@@ -1,0 +1,159 @@
+"""C ABI checks that need no GPU: the library loads, exports every entry
+point the header declares, validates arguments before touching CUDA, and its
+host LPT matches the oracle's bit for bit."""
+
+import os
+import re
+
+import numpy as np
+import pytest
+
+from oracle import lpt as olpt
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def mos():
+    import matrix_optimizer_step_gb300 as m
+    from matrix_optimizer_step_gb300 import build
+
+    build.build()
+    m.load_library()
+    return m
+
+
+def _declared_symbols():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            names |= set(re.findall(r"DMUON_API\s+[\w\s\*]+?\b(dmuon_\w+)\s*\(", text))
+    return names
+
+
+def test_library_exports_every_declared_symbol(mos):
+    lib = mos.load_library()
+    names = _declared_symbols()
+    assert "dmuon_muon_step" in names and "dmuon_lpt_assign" in names and "dmuon_adamw_step" in names
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(mos.capi.EXPORTED) == names
+
+
+def test_status_strings(mos):
+    for s in range(0, 9):
+        assert mos.dmuon_status_string(s)
+    assert mos.dmuon_status_string(99) == "unknown status"
+
+
+def test_lpt_bit_exact_vs_oracle(mos):
+    r = np.random.default_rng(0)
+    for trial in range(200):
+        n = int(r.integers(0, 300))
+        R = int(r.integers(1, 160))
+        hi = int(r.choice([2, 10, 1000, 10 ** 12]))
+        sizes = [int(x) for x in r.integers(0, hi, n)]
+        got = mos.dmuon_lpt_assign(sizes, R)
+        want = olpt.lpt_assign(sizes, R)
+        assert got[0] == want[0] and got[1] == want[1], (trial, n, R)
+
+
+def test_lpt_large_tile_list_vs_oracle(mos):
+    # The size of a real tile list: ~30k tiles of a few distinct costs on 148 slots.
+    r = np.random.default_rng(1)
+    sizes = [int(x) for x in r.choice([18, 66, 226], 30000)]
+    got = mos.dmuon_lpt_assign(sizes, 148)
+    want = olpt.lpt_assign(sizes, 148)
+    assert got == (want[0], want[1])
+
+
+def test_lpt_graham_tight_instance(mos):
+    for R in (2, 4, 8):
+        sizes = []
+        for k in range(2 * R - 1, R, -1):
+            sizes += [k, k]
+        sizes += [R, R, R]
+        _, loads = mos.dmuon_lpt_assign(sizes, R)
+        assert max(loads) == 4 * R - 1
+
+
+def test_lpt_errors(mos):
+    with pytest.raises(mos.DmuonError) as e:
+        mos.dmuon_lpt_assign([1, 2], 0)
+    assert e.value.status == 1
+    with pytest.raises(mos.DmuonError):
+        mos.dmuon_lpt_assign([1, -1], 2)
+    with pytest.raises(mos.DmuonError):
+        mos.dmuon_lpt_assign([2 ** 62, 2 ** 62], 1)
+    assert mos.dmuon_lpt_assign([], 3) == ([], [0, 0, 0])
+
+
+def test_muon_step_host_validation_without_gpu(mos):
+    # Host-side validation runs before any CUDA call, so it works here.
+    capi = mos.capi
+    ctx = mos.dmuon_context_create(0)
+    try:
+        d = capi.DmuonMatrix()
+        d.rank = 1
+        d.shape[0] = 128
+        d.master = d.momentum = d.grad = 256
+        with pytest.raises(mos.DmuonError) as e:
+            mos.dmuon_muon_step(ctx, [d], 0.02, 0.95, 0.01, 5, 3.4445, -4.775, 2.0315, stream=0)
+        assert e.value.status == capi.DMUON_ERR_RANK_LT2
+        d.rank = 2
+        d.shape[0], d.shape[1] = 8, 0
+        with pytest.raises(mos.DmuonError) as e:
+            mos.dmuon_muon_step(ctx, [d], 0.02, 0.95, 0.01, 5, 3.4445, -4.775, 2.0315, stream=0)
+        assert e.value.status == capi.DMUON_ERR_SHAPE
+        d.shape[1] = 16
+        d.grad_dtype = 7
+        with pytest.raises(mos.DmuonError) as e:
+            mos.dmuon_muon_step(ctx, [d], 0.02, 0.95, 0.01, 5, 3.4445, -4.775, 2.0315, stream=0)
+        assert e.value.status == capi.DMUON_ERR_DTYPE
+        d.grad_dtype = capi.DMUON_DTYPE_BF16
+        d.grad = None
+        with pytest.raises(mos.DmuonError) as e:
+            mos.dmuon_muon_step(ctx, [d], 0.02, 0.95, 0.01, 5, 3.4445, -4.775, 2.0315, stream=0)
+        assert e.value.status == capi.DMUON_ERR_INVALID_ARG
+        with pytest.raises(mos.DmuonError) as e:
+            mos.dmuon_muon_step(ctx, [], float("nan"), 0.95, 0.01, 5, 3.4445, -4.775, 2.0315, stream=0)
+        assert e.value.status == capi.DMUON_ERR_INVALID_ARG
+        with pytest.raises(mos.DmuonError):
+            mos.dmuon_muon_step(ctx, [], 0.02, 0.95, 0.01, 101, 3.4445, -4.775, 2.0315, stream=0)
+        mos.dmuon_muon_step(ctx, [], 0.02, 0.95, 0.01, 5, 3.4445, -4.775, 2.0315, stream=0)
+        with pytest.raises(mos.DmuonError):
+            mos.dmuon_adamw_step(ctx, [], 1e-3, 0.9, 0.95, 1e-8, 0.0, 0, stream=0)
+        with pytest.raises(mos.DmuonError):
+            mos.dmuon_adamw_step(ctx, [], 1e-3, 1.0, 0.95, 1e-8, 0.0, 1, stream=0)
+    finally:
+        mos.dmuon_context_destroy(ctx)
+
+
+def test_golden_last_two_dims_accepted_ranks(mos):
+    """The pages' table: [128] is rejected (rank 1); [8,16] and [4,8,16] pass
+    host validation (they only fail later for lack of a device here)."""
+    import json
+
+    capi = mos.capi
+    gold = json.load(open(os.path.join(ROOT, "tests", "golden", "last_two_dims.json")))
+    ctx = mos.dmuon_context_create(0)
+    try:
+        for case in gold["cases"]:
+            d = capi.DmuonMatrix()
+            d.rank = len(case["shape"])
+            for i, s in enumerate(case["shape"]):
+                d.shape[i] = s
+            d.master = d.momentum = d.grad = 256
+            d.grad_dtype = capi.DMUON_DTYPE_BF16
+            try:
+                mos.dmuon_muon_step(ctx, [d], 0.02, 0.95, 0.01, 5, 3.4445, -4.775, 2.0315, stream=0)
+                status = 0
+            except mos.DmuonError as e:
+                status = e.status
+            if case["accepted"]:
+                assert status in (0, capi.DMUON_ERR_UNSUPPORTED, capi.DMUON_ERR_CUDA), case
+            else:
+                assert status == capi.DMUON_ERR_RANK_LT2, case
+    finally:
+        mos.dmuon_context_destroy(ctx)
