@@ -1,0 +1,398 @@
+"""Benchmark of the owner-side Muon / AdamW step (one JSON line on stdout).
+
+A step is one pass of the whole hot path over the workload: the Muon step
+(momentum, Newton-Schulz on every matrix, weight decay + update, bf16 copy)
+and the AdamW step of the AdamW-route tensors, with every input already
+resident in HBM.  Default workload: the Llama-3-8B-shaped set (224 Muon
+matrices, 6.98e9 elements, plus 1.05e9 AdamW elements).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME]
+
+value = dense Newton-Schulz TFLOP per step (all ranks) / step time, so the
+unit is TFLOP/s of the whole step; ms_per_step is the step time itself.
+Under torchrun each rank runs its own copy of the workload (weak scaling)
+and the slowest rank's time counts.  ``--impl reference`` times the float64
+CPU oracle on a bounded sample of the same workload.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "Muon step ms & NS TFLOP/s (% bf16 TC peak), Llama-3-8B-shaped matrix set"
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_burst": d["bf16_tflops"],
+                "bf16_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]), "src": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_burst": 1900.0, "bf16_sustained": 1700.0, "src": "fallback"}
+
+
+def _workload_desc(wl):
+    return (f"{wl.name}: {len(wl.matrices)} Muon tensors, {wl.muon_numel / 1e9:.3f}e9 elements, "
+            f"{len(wl.vectors)} AdamW tensors, {wl.adamw_numel / 1e9:.3f}e9 elements")
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        try:
+            sm = [float(r[1]) for r in rows]
+            mx = max(float(r[2]) for r in rows)
+        except ValueError:
+            return None
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": reasons, "samples": len(rows)}
+
+
+# --------------------------------------------------------------- CPU legs
+def _oracle_sample(wl):
+    """Bounded sample of the workload for the float64 oracle: the named
+    Muon matrices (with their own inputs) and a 4M-element AdamW slice."""
+    from matrix_optimizer_step_gb300 import workloads as W
+
+    picks = {"llama3_8b": ["layers.0.q", "layers.0.k", "layers.0.v"],
+             "llama3_8b_layer": ["layers.0.k"],
+             "moe_experts": [], "many_small": [s.name for s in wl.matrices[:48]],
+             "gpt2_small": [s.name for s in wl.matrices[:12]],
+             "single_256x512": [s.name for s in wl.matrices]}[wl.name]
+    mats = []
+    for i, spec in enumerate(wl.matrices):
+        if spec.name in picks:
+            W0 = W.master_init(spec, i).double().numpy()
+            G = W.muon_grad(wl, spec, i).float().double().numpy()
+            mats.append((spec, W0, G))
+    if wl.name == "moe_experts":  # two expert slices of the first w1
+        spec = wl.matrices[0]
+        W0 = W.master_init(spec, 0)[:2].double().numpy()
+        G = W.muon_grad(wl, spec, 0)[:2].float().double().numpy()
+        mats.append((spec, W0, G))
+    adam = None
+    if wl.vectors:
+        spec = max(wl.vectors, key=lambda v: v.numel)
+        n = min(4 << 20, spec.numel)
+        idx = wl.vectors.index(spec)
+        w = W.vector_init(spec, idx)[:n].double().numpy()
+        g = W.vector_grad(spec, idx)[:n].float().double().numpy()
+        adam = (n, w, g)
+    return mats, adam
+
+
+def _oracle_time(wl, sample):
+    """Run the oracle on the sample once; return (seconds, sample NS flops,
+    extrapolated full-step seconds)."""
+    import numpy as np
+
+    from matrix_optimizer_step_gb300 import workloads as W
+    from oracle import adamw as oadamw
+    from oracle import muon as omuon
+
+    h = wl.hyper
+    mats, adam = sample
+    t0 = time.perf_counter()
+    flops = 0
+    for spec, W0, G in mats:
+        omuon.muon_step(W0, np.zeros_like(W0), G, h["lr"], h["momentum"], h["wd"], h["ns_steps"],
+                        h["a"], h["b"], h["c"])
+        m, n = spec.mn
+        flops += W.ns_flops(m, n, h["ns_steps"]) * (W0.size // (m * n))
+    t_muon = time.perf_counter() - t0
+    t_adam = 0.0
+    if adam is not None:
+        n, w, g = adam
+        t1 = time.perf_counter()
+        oadamw.adamw_step(w, np.zeros(n), np.zeros(n), g, h["adam_lr"], h["beta1"], h["beta2"],
+                          h["adam_eps"], h["adam_wd"], 1)
+        t_adam = time.perf_counter() - t1
+    total_flops = W.workload_ns_flops(wl)
+    est = t_muon * total_flops / max(flops, 1)
+    if adam is not None:
+        est += t_adam * wl.adamw_numel / adam[0]
+    return t_muon + t_adam, flops, est
+
+
+def _sample_desc(wl, sample):
+    mats, adam = sample
+    names = ", ".join(f"{s.name}{'[0:2]' if wl.name == 'moe_experts' else ''}" for s, _, _ in mats[:6])
+    more = f" (+{len(mats) - 6} more)" if len(mats) > 6 else ""
+    ad = f"; AdamW on {adam[0]} elements" if adam else ""
+    return (f"float64 oracle Muon step on {len(mats)} matrices ({names}{more}){ad}; full-step time "
+            f"extrapolated by NS flop share (Muon) and element count (AdamW)")
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+# ---------------------------------------------------------------- main legs
+def run_reference(args, wl, rank, world):
+    if rank != 0:
+        return
+    sample = _oracle_sample(wl)
+    for _ in range(args.warmup):
+        _oracle_time(wl, sample)
+    ests, secs = [], []
+    for _ in range(args.steps):
+        s, flops, est = _oracle_time(wl, sample)
+        ests.append(est)
+        secs.append(s)
+    from matrix_optimizer_step_gb300 import workloads as W
+
+    total = W.workload_ns_flops(wl)
+    ms = 1000.0 * statistics.median(ests)
+    value = total / (ms / 1000.0) / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": _workload_desc(wl), "ns_steps": wl.hyper["ns_steps"]},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
+                         "sample": _sample_desc(wl, sample),
+                         "sample_seconds_per_step": statistics.median(secs)},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, wl, rank, world, local_rank):
+    import torch
+
+    import matrix_optimizer_step_gb300 as mos
+    from matrix_optimizer_step_gb300 import workloads as W
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    mos.load_library()
+    h = wl.hyper
+    mat = W.materialize(wl, dev)
+    step = mos.OwnerStep(local_rank)
+    step.set_muon(mat.masters, mat.momenta, mat.grads, mat.params)
+    if wl.vectors:
+        step.set_adamw(mat.v_masters, mat.v_exp_avg, mat.v_exp_avg_sq, mat.v_grads, mat.v_params)
+    stream = torch.cuda.current_stream()
+    t_counter = [0]
+
+    def one_step():
+        step.muon_step(h["lr"], h["momentum"], h["wd"], h["ns_steps"], h["a"], h["b"], h["c"],
+                       nesterov=h["nesterov"], fp32_ns=h["fp32_ns"], stream=stream)
+        if wl.vectors:
+            t_counter[0] += 1
+            step.adamw_step(h["adam_lr"], h["beta1"], h["beta2"], h["adam_eps"], h["adam_wd"],
+                            t_counter[0], stream=stream)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        one_step()
+    step.sync(stream)
+
+    # ---------------- timed region: K steps, device events on the stream
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    step.profile(True)
+    step.profile_read()
+    launches0 = step.kernel_launches()
+    barrier()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        one_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    launches = step.kernel_launches() - launches0
+    prof = step.profile_read()
+    step.profile(False)
+    clk = clocks.stop()
+    step.sync(stream)
+    ms = e0.elapsed_time(e1) / args.steps
+    if dist is not None:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+
+    # ---------------- end to end: host grads in, host bf16 params out
+    e2e_steps = max(1, min(args.steps, 3))
+    g_flat, p_flat = mat.flats["grad"], mat.flats["param"]
+    host_g = torch.empty(g_flat.shape, dtype=g_flat.dtype, pin_memory=True)
+    host_p = torch.empty(p_flat.shape, dtype=p_flat.dtype, pin_memory=True)
+    host_g.copy_(g_flat)
+    barrier()
+    torch.cuda.synchronize()
+    x0 = torch.cuda.Event(enable_timing=True)
+    x1 = torch.cuda.Event(enable_timing=True)
+    x0.record(stream)
+    for _ in range(e2e_steps):
+        g_flat.copy_(host_g, non_blocking=True)
+        one_step()
+        host_p.copy_(p_flat, non_blocking=True)
+    x1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    e2e_ms = x0.elapsed_time(x1) / e2e_steps
+    if dist is not None:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    h2d = g_flat.numel() * g_flat.element_size()
+    d2h = p_flat.numel() * p_flat.element_size()
+    del host_g, host_p
+
+    if rank != 0:
+        return
+    peaks = _peaks()
+    ns_flops = W.workload_ns_flops(wl)
+    ns_ms = sum(prof[k][0] for k in ("ns_gram", "ns_poly", "ns_combine")) / args.steps
+    ns_launches = sum(prof[k][1] for k in ("ns_gram", "ns_poly", "ns_combine"))
+    ns_tflops = ns_flops / (ns_ms / 1e3) / 1e12 if ns_ms > 0 else None
+    ew_bytes = W.muon_elementwise_bytes(wl) + W.adamw_bytes(wl)
+    ew_ms = sum(prof[k][0] for k in ("momentum", "norm", "update", "adamw")) / args.steps
+    ew_gbs = ew_bytes / (ew_ms / 1e3) / 1e9 if ew_ms > 0 else None
+    peak = peaks["bf16_sustained"]
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", "ns_tc_traffic.json")
+    if os.path.exists(tpath):
+        try:
+            import hashlib
+
+            tj = json.load(open(tpath))
+            src = open(os.path.join(ROOT, "matrix_optimizer_step_gb300", "csrc", "k_ns_tc.cu"), "rb").read()
+            if tj.get("kernel_sha256") == hashlib.sha256(src).hexdigest() and tj.get("workload") == wl.name:
+                traffic = tj.get("bytes_per_step")
+        except (OSError, ValueError, KeyError):
+            traffic = None
+    line = {
+        "metric": METRIC, "value": world * ns_flops / (ms / 1e3) / 1e12, "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": _workload_desc(wl), "ns_steps": h["ns_steps"],
+                   "ns_operands": "fp32 in NS mode" if h["fp32_ns"] else "bf16 operands, fp32 accumulate",
+                   "state": "fp32 master/momentum/AdamW moments, bf16 grads and params",
+                   "l2": "inputs larger than L2 (no flush needed)", "parallelism": f"replicas x{world}"},
+        "ns_tflops": ns_tflops,
+        "ns_frac_of_bf16_sustained": (ns_tflops / peak) if ns_tflops else None,
+        "ns_frac_of_bf16_burst": (ns_tflops / peaks["bf16_burst"]) if ns_tflops else None,
+        "roofline": {"bound": "tensor", "kernel": "ns_tc_kernel (all NS phases)",
+                     "achieved": ns_tflops, "peak": peak, "unit": "TFLOP/s",
+                     "frac": (ns_tflops / peak) if ns_tflops else None,
+                     "peak_src": f"{peaks['src']} bf16 sustained",
+                     "traffic": traffic, "launches_per_step": ns_launches / args.steps},
+        "elementwise": {"bound": "hbm", "achieved": ew_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                        "frac": (ew_gbs / peaks["hbm_gbs"]) if ew_gbs else None,
+                        "bytes_per_step": ew_bytes},
+        "kernel_ms_per_step": {k: v[0] / args.steps for k, v in prof.items()},
+        "gpu_launches": launches,
+        "e2e": {"value": world * ns_flops / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
+                "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "steps": e2e_steps},
+        "clocks": clk,
+    }
+    if not args.no_cpu_baseline:
+        sample = _oracle_sample(wl)
+        secs, flops, est = _oracle_time(wl, sample)
+        line["cpu_baseline"] = {"value": ns_flops / est / 1e12, "unit": "TFLOP/s", "cores": cpu_cores(),
+                                "kind": "oracle", "sample": _sample_desc(wl, sample),
+                                "sample_seconds": secs, "est_ms_per_step": est * 1e3}
+    print(json.dumps(line), flush=True)
+    step.close()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default="llama3_8b")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    from matrix_optimizer_step_gb300 import workloads as W
+
+    wl = W.workload(args.workload)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, wl, rank, world)
+        return
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl")
+    try:
+        run_ours(args, wl, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -167,6 +167,7 @@ struct ShapeClass {
   bool tall;            // m > n: Gram is X^T X, last product X B
   int64_t ld, ldp;      // workspace row pitch (elements) for X and for A/B
   size_t off_x[2], off_a, off_b;  // byte offsets in the workspace
+  size_t off_xf, off_af;          // fp32 side copies of X and A (bf16 path only)
   int32_t map_xk[2], map_xmn[2], map_a, map_b;
 };
 
@@ -185,7 +186,9 @@ struct MuonPlan {
   std::vector<int32_t> slice_chunk_begin, slice_chunk_end;
   size_t ws_bytes = 0;
   DevBuf chunks_dev, partials, inv_norm, maps;
-  DevBuf probs[3][2];
+  // Problem tables per kind and variant: 0/1 = X in buffer 0/1 (later
+  // iterations), 2 = first iteration, 3 = second iteration.
+  DevBuf probs[3][4];
   PhaseTiles phase[3];
   void release() {
     chunks_dev.release();
@@ -388,6 +391,7 @@ int build_phase_tiles(const std::vector<NsProblem>& probs, bool fp32, int num_sm
     const int64_t c = (P.K + kTcBK - 1) / kTcBK + 2;
     for (int i = 0; i < tm; ++i)
       for (int j = 0; j < tn; ++j) {
+        if (P.sym && (i * bm) / kTcBN > j) continue;  // below the diagonal: mirrored
         tiles.push_back(make_uint2(static_cast<uint32_t>(p), (static_cast<uint32_t>(i) << 16) | static_cast<uint32_t>(j)));
         cost.push_back(c);
       }
@@ -467,6 +471,8 @@ int build_muon_plan(dmuon_context* ctx, const dmuon_matrix* mats, int n, bool fp
     for (int t = 0; t < 2; ++t) C.off_x[t] = take(static_cast<size_t>(C.count) * C.m * C.ld * es);
     C.off_a = take(static_cast<size_t>(C.count) * p * C.ldp * es);
     C.off_b = take(static_cast<size_t>(C.count) * p * C.ldp * es);
+    C.off_xf = fp32 ? 0 : take(static_cast<size_t>(C.count) * C.m * C.ld * 4);
+    C.off_af = fp32 ? 0 : take(static_cast<size_t>(C.count) * p * C.ldp * 4);
   }
   P.ws_bytes = std::max<size_t>(off, 1024);
   if (ctx->ws.bytes < P.ws_bytes) {
@@ -532,19 +538,29 @@ int build_muon_plan(dmuon_context* ctx, const dmuon_matrix* mats, int n, bool fp
     if (st != DMUON_OK) return st;
   }
 
-  // Problems of the three phases, for X in buffer t (t = iteration parity).
-  for (int par = 0; par < 2; ++par) {
-    std::vector<NsProblem> gram, poly, comb;
-    for (size_t s = 0; s < P.slices.size(); ++s) {
-      const SliceRef& R = P.slices[s];
-      const ShapeClass& C = P.classes[static_cast<size_t>(R.cls)];
-      const int32_t p = std::min(C.m, C.n), q = std::max(C.m, C.n);
-      uint8_t* X = ws + C.off_x[par] + static_cast<size_t>(R.z) * C.m * C.ld * es;
-      uint8_t* Xn = ws + C.off_x[par ^ 1] + static_cast<size_t>(R.z) * C.m * C.ld * es;
-      uint8_t* A = ws + C.off_a + static_cast<size_t>(R.z) * p * C.ldp * es;
-      uint8_t* B = ws + C.off_b + static_cast<size_t>(R.z) * p * C.ldp * es;
+  // Problems of the three phases.  Variant 0/1: X in buffer 0/1, everything
+  // bf16 (or everything fp32 in validation mode).  Variant 2 (first
+  // iteration, X in buffer 0) and 3 (second iteration, X in buffer 1) add the
+  // fp32 side copies on the bf16 path: the first Gram also writes A in fp32,
+  // the first Poly reads that fp32 A, the first Combine reads the fp32 X0 and
+  // writes X1 in fp32 over it (each element is read before it is written, by
+  // the same thread), and the second Combine reads that fp32 X1.
+  std::vector<NsProblem> var[3][4];
+  for (size_t s_i = 0; s_i < P.slices.size(); ++s_i) {
+    const SliceRef& R = P.slices[s_i];
+    const ShapeClass& C = P.classes[static_cast<size_t>(R.cls)];
+    const int32_t p = std::min(C.m, C.n), q = std::max(C.m, C.n);
+    const size_t xoff = static_cast<size_t>(R.z) * C.m * C.ld;
+    const size_t poff = static_cast<size_t>(R.z) * p * C.ldp;
+    uint8_t* A = ws + C.off_a + poff * es;
+    uint8_t* B = ws + C.off_b + poff * es;
+    float* Xf = fp32 ? nullptr : reinterpret_cast<float*>(ws + C.off_xf) + xoff;
+    float* Af = fp32 ? nullptr : reinterpret_cast<float*>(ws + C.off_af) + poff;
+    for (int par = 0; par < 2; ++par) {
+      uint8_t* X = ws + C.off_x[par] + xoff * es;
+      uint8_t* Xn = ws + C.off_x[par ^ 1] + xoff * es;
       NsProblem g{}, y{}, c{};
-      g.slice = y.slice = c.slice = static_cast<int32_t>(s);
+      g.slice = y.slice = c.slice = static_cast<int32_t>(s_i);
       g.z = y.z = c.z = R.z;
       // Gram: p x p, K = q.
       g.M = g.N = p;
@@ -552,7 +568,6 @@ int build_muon_plan(dmuon_context* ctx, const dmuon_matrix* mats, int n, bool fp
       g.a = g.b = X;
       g.out = A;
       g.ld_out = C.ldp;
-      g.aux = nullptr;
       if (!C.tall) {  // A = X X^T: A_op(i,k) = X[i,k], B_op(k,j) = X[j,k]
         g.a_si = C.ld; g.a_sk = 1; g.b_sk = 1; g.b_sj = C.ld;
         g.map_a = g.map_b = C.map_xk[par];
@@ -572,6 +587,7 @@ int build_muon_plan(dmuon_context* ctx, const dmuon_matrix* mats, int n, bool fp
       y.ld_out = C.ldp;
       y.aux = A;
       y.ld_aux = C.ldp;
+      g.sym = y.sym = fp32 ? 0 : 1;
       // Combine: X' = a X + B X (wide) or a X + X B (tall).
       c.out = Xn;
       c.ld_out = C.ld;
@@ -592,24 +608,31 @@ int build_muon_plan(dmuon_context* ctx, const dmuon_matrix* mats, int n, bool fp
         c.map_b = C.map_b;
         c.majors = 0;
       }
-      gram.push_back(g);
-      poly.push_back(y);
-      comb.push_back(c);
+      var[kGram][par].push_back(g);
+      var[kPoly][par].push_back(y);
+      var[kCombine][par].push_back(c);
+      if (!fp32 && par == 0) {
+        g.out2 = Af;
+        g.ld_out2 = C.ldp;
+        y.aux = Af;
+        c.aux = Xf;
+        c.out2 = Xf;
+        c.ld_out2 = C.ld;
+      }
+      if (!fp32 && par == 1) c.aux = Xf;
+      var[kGram][2 + par].push_back(g);
+      var[kPoly][2 + par].push_back(y);
+      var[kCombine][2 + par].push_back(c);
     }
-    st = upload(P.probs[kGram][par], gram);
-    if (st != DMUON_OK) return st;
-    st = upload(P.probs[kPoly][par], poly);
-    if (st != DMUON_OK) return st;
-    st = upload(P.probs[kCombine][par], comb);
-    if (st != DMUON_OK) return st;
-    if (par == 0) {
-      st = build_phase_tiles(gram, fp32, ctx->num_sms, P.phase[kGram]);
-      if (st != DMUON_OK) return st;
-      st = build_phase_tiles(poly, fp32, ctx->num_sms, P.phase[kPoly]);
-      if (st != DMUON_OK) return st;
-      st = build_phase_tiles(comb, fp32, ctx->num_sms, P.phase[kCombine]);
+  }
+  for (int kind = 0; kind < 3; ++kind)
+    for (int v = 0; v < 4; ++v) {
+      st = upload(P.probs[kind][v], var[kind][v]);
       if (st != DMUON_OK) return st;
     }
+  for (int kind = 0; kind < 3; ++kind) {
+    st = build_phase_tiles(var[kind][0], fp32, ctx->num_sms, P.phase[kind]);
+    if (st != DMUON_OK) return st;
   }
   P.key = key;
   return DMUON_OK;
@@ -742,6 +765,7 @@ int dmuon_muon_step(dmuon_context* ctx, const dmuon_matrix* mats, int32_t n, flo
     D.param = M.param_bf16 ? M.param_bf16 + R.elem_offset : nullptr;
     const size_t xoff = static_cast<size_t>(R.z) * C.m * C.ld * es;
     D.x0 = ws + C.off_x[0] + xoff;
+    D.x0f = fp32 ? nullptr : reinterpret_cast<float*>(ws + C.off_xf) + static_cast<size_t>(R.z) * C.m * C.ld;
     D.xk = ws + C.off_x[ns_steps & 1] + xoff;
     D.ld = C.ld;
     D.m = C.m;
@@ -770,10 +794,11 @@ int dmuon_muon_step(dmuon_context* ctx, const dmuon_matrix* mats, int32_t n, flo
   });
   if (st != DMUON_OK) return st;
   for (int it = 0; it < ns_steps; ++it) {
-    const int par = it & 1;
+    const int variant = it < 2 ? 2 + it : (it & 1);
     for (int kind = kGram; kind <= kCombine; ++kind) {
       NsLaunch L{};
-      L.probs = static_cast<const NsProblem*>(P.probs[kind][par].p);
+      L.probs = static_cast<const NsProblem*>(P.probs[kind][variant].p);
+      L.aux_f32 = (!fp32 && ((it == 0 && kind != kGram) || (it == 1 && kind == kCombine))) ? 1 : 0;
       L.tiles = static_cast<const uint2*>(P.phase[kind].tiles.p);
       L.cta_begin = static_cast<const int32_t*>(P.phase[kind].cta_begin.p);
       L.maps = static_cast<const CUtensorMap*>(P.maps.p);

@@ -27,7 +27,8 @@ struct SliceDesc {
   float* momentum;
   const void* grad;
   uint16_t* param;        // may be null
-  void* x0;               // workspace: X before the first iteration
+  void* x0;               // workspace: X before the first iteration (NS operand dtype)
+  float* x0f;             // workspace: fp32 copy of X0 for the first epilogues (bf16 path), or null
   const void* xk;         // workspace: X after the last iteration
   int64_t ld;             // workspace row pitch, elements
   int32_t m, n;
@@ -73,11 +74,18 @@ struct NsProblem {
   void* out;
   const void* aux;
   int64_t ld_out, ld_aux;
+  float* out2;            // optional fp32 copy of the output (tcgen05 path), or null
+  int64_t ld_out2;
   int32_t M, N, K;
   int32_t slice;          // global slice index (norm table)
   int32_t map_a, map_b;
   int32_t z;
   int32_t majors;
+  // 1: the output is symmetric (Gram, Poly on the tcgen05 path).  Only tiles
+  // whose 256-row block is on or above the diagonal 256-column block are
+  // scheduled; tiles strictly above the diagonal also write their transpose.
+  int32_t sym;
+  int32_t pad_;
 };
 
 // Phase kinds of one Newton-Schulz iteration.
@@ -86,6 +94,11 @@ struct NsProblem {
 //   kCombine: out = g^p * (acc + a * aux)      (X' = a X + B X, aux = X)
 // g = 1/(||u||+eps) of the slice when the fold-in of the normalisation is
 // active (first iteration), p = gpow; g^0 = 1.
+// On the bf16 path the MMA operands are always bf16, but the first
+// iteration keeps fp32 copies of X0, A and X1 for the epilogue terms b*A and
+// a*X (aux_f32 = 1 and out2 set): those terms carry the weak directions of a
+// gradient dominated by a few large singular values, and rounding them to
+// bf16 before the iteration amplifies them is what costs accuracy.
 enum NsKind : int { kGram = 0, kPoly = 1, kCombine = 2 };
 
 struct NsLaunch {
@@ -96,6 +109,7 @@ struct NsLaunch {
   const float* gscale;      // per-slice 1/(||u||+eps), or null
   int32_t gpow;
   int32_t kind;
+  int32_t aux_f32;          // aux is fp32 (tcgen05 path; the fp32 path is always fp32)
   float a, b, c;
   int* err;
 };

@@ -18,10 +18,16 @@
 //   warps 2..5  epilogue: each warp owns one 32-lane quarter of TMEM
 //               (warp % 4), reads its rows 32 columns at a time with
 //               tcgen05.ld, applies the phase's fused epilogue (scale;
-//               b*A + c*acc; a*X + acc) and stores bf16 to global memory,
-//               then releases the accumulator (`tempty[a]`).
+//               b*A + c*acc; a*X + acc) and stores bf16 (plus an fp32 copy
+//               where the problem asks for one) to global memory, then
+//               releases the accumulator (`tempty[a]`).
 // The two accumulators let the epilogue of tile i overlap the main loop of
 // tile i+1.
+//
+// X X^T and B = b A + c A A are symmetric: for them only the 256 x 256
+// blocks on or above the diagonal are computed (two 128-row tiles per
+// block) and the epilogue of an off-diagonal block also stores its transpose
+// (NsProblem::sym), which removes close to half of those two phases' work.
 //
 // Operand layouts: a K-contiguous operand tile is one TMA box of
 // 64 (k) x rows; an M/N-contiguous operand tile is a row of boxes of
@@ -274,6 +280,10 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_kernel(const NsLaunch L, in
       uint16_t* out_row = reinterpret_cast<uint16_t*>(P.out) + static_cast<int64_t>(row) * P.ld_out;
       const uint16_t* aux_row =
           reinterpret_cast<const uint16_t*>(P.aux) + static_cast<int64_t>(row) * P.ld_aux;
+      const float* auxf_row = reinterpret_cast<const float*>(P.aux) + static_cast<int64_t>(row) * P.ld_aux;
+      float* out2_row = P.out2 ? P.out2 + static_cast<int64_t>(row) * P.ld_out2 : nullptr;
+      const bool aux_f32 = L.aux_f32 != 0;
+      const bool mirror = P.sym && ((m0 >> 8) < (n0 >> 8));
       const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                               static_cast<uint32_t>(acc * BN);
 #pragma unroll 1
@@ -284,37 +294,75 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_kernel(const NsLaunch L, in
         uint32_t r[32];
         tmem_ld_32x32b_x32(t_lane + static_cast<uint32_t>(cc * 32), r);
         const bool full_chunk = (col0 + 32 <= P.N);
-        uint4 auxv[4];
+        float auxf[32];
         if (beta != 0.f && row_ok && full_chunk) {
-          const uint4* src = reinterpret_cast<const uint4*>(aux_row + col0);
+          if (aux_f32) {
+            const float4* src = reinterpret_cast<const float4*>(auxf_row + col0);
 #pragma unroll
-          for (int i = 0; i < 4; ++i) auxv[i] = __ldg(src + i);
+            for (int i = 0; i < 8; ++i) {
+              const float4 q = __ldg(src + i);
+              auxf[4 * i] = q.x; auxf[4 * i + 1] = q.y; auxf[4 * i + 2] = q.z; auxf[4 * i + 3] = q.w;
+            }
+          } else {
+            const uint4* src = reinterpret_cast<const uint4*>(aux_row + col0);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const uint4 q = __ldg(src + i);
+              const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                auxf[8 * i + 2 * j] = __uint_as_float(w[j] << 16);
+                auxf[8 * i + 2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+              }
+            }
+          }
         }
         tmem_ld_wait();
         if (!row_ok) {
           // rows past M: nothing to store
         } else if (full_chunk) {
-          uint32_t packed[16];
+          float v[32];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            float v0 = alpha * __uint_as_float(r[2 * i]);
-            float v1 = alpha * __uint_as_float(r[2 * i + 1]);
-            if (beta != 0.f) {
-              const uint32_t w = (&auxv[i >> 2].x)[i & 3];
-              v0 = fmaf(beta, __uint_as_float(w << 16), v0);
-              v1 = fmaf(beta, __uint_as_float(w & 0xFFFF0000u), v1);
-            }
-            packed[i] = pack_bf16x2(v0, v1);
+          for (int j = 0; j < 32; ++j) {
+            v[j] = alpha * __uint_as_float(r[j]);
+            if (beta != 0.f) v[j] = fmaf(beta, auxf[j], v[j]);
           }
           uint4* dst = reinterpret_cast<uint4*>(out_row + col0);
 #pragma unroll
           for (int i = 0; i < 4; ++i)
-            dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+            dst[i] = make_uint4(pack_bf16x2(v[8 * i], v[8 * i + 1]), pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
+                                pack_bf16x2(v[8 * i + 4], v[8 * i + 5]), pack_bf16x2(v[8 * i + 6], v[8 * i + 7]));
+          if (out2_row) {
+            float4* d2 = reinterpret_cast<float4*>(out2_row + col0);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) d2[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+          }
+          if (mirror) {
+            // Transposed copy: for each column j the warp's 32 lanes hold 32
+            // consecutive rows, so every store instruction writes one
+            // contiguous 64-byte (bf16) or 128-byte (fp32) run.
+            uint16_t* mo = reinterpret_cast<uint16_t*>(P.out) + row;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) mo[static_cast<int64_t>(col0 + j) * P.ld_out] = to_bf16_bits(v[j]);
+            if (P.out2) {
+              float* m2 = P.out2 + row;
+#pragma unroll
+              for (int j = 0; j < 32; ++j) m2[static_cast<int64_t>(col0 + j) * P.ld_out2] = v[j];
+            }
+          }
         } else {
           for (int j = 0; j < 32 && col0 + j < P.N; ++j) {
             float v = alpha * __uint_as_float(r[j]);
-            if (beta != 0.f) v = fmaf(beta, bf16_bits_to_f32(aux_row[col0 + j]), v);
-            out_row[col0 + j] = to_bf16_bits(v);
+            if (beta != 0.f)
+              v = fmaf(beta, aux_f32 ? auxf_row[col0 + j] : bf16_bits_to_f32(aux_row[col0 + j]), v);
+            const uint16_t vb = to_bf16_bits(v);
+            out_row[col0 + j] = vb;
+            if (out2_row) out2_row[col0 + j] = v;
+            if (mirror) {
+              const int64_t mi = static_cast<int64_t>(col0 + j);
+              reinterpret_cast<uint16_t*>(P.out)[mi * P.ld_out + row] = vb;
+              if (P.out2) P.out2[mi * P.ld_out2 + row] = v;
+            }
           }
         }
       }

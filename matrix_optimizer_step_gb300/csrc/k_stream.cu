@@ -1,6 +1,7 @@
 // Streaming (HBM-bound) kernels of the owner-side step:
 //   momentum  -- buf <- mu*buf + g, u <- g + mu*buf (Nesterov), X0 <- u into
-//                the Newton-Schulz workspace, per-chunk sum of u^2
+//                the Newton-Schulz workspace (operand dtype, plus an fp32
+//                copy on the bf16 path), per-chunk sum of u^2
 //   norm      -- per-slice 1/(||u||_F + 1e-7) from the chunk partials
 //   update    -- W <- W*(1 - lr*wd) - lr*scale*X, bf16 copy of W
 //   adamw     -- the element-wise AdamW step
@@ -124,6 +125,7 @@ __global__ void __launch_bounds__(kThreads) momentum_kernel(const SliceDesc* __r
         store8_f32(reinterpret_cast<float*>(S.x0) + xi, u);
       else
         store8_bf16(reinterpret_cast<uint16_t*>(S.x0) + xi, u);
+      if (S.x0f) store8_f32(S.x0f + xi, u);
     }
   } else {
     for (int64_t e = ch.start + threadIdx.x; e < end; e += kThreads) {
@@ -133,7 +135,9 @@ __global__ void __launch_bounds__(kThreads) momentum_kernel(const SliceDesc* __r
       S.momentum[e] = b;
       ss = fmaf(u, u, ss);
       const int64_t row = e / S.n;
-      store1(S.x0, row * S.ld + (e - row * S.n), u, !x_fp32);
+      const int64_t xi = row * S.ld + (e - row * S.n);
+      store1(S.x0, xi, u, !x_fp32);
+      if (S.x0f) S.x0f[xi] = u;
     }
   }
   const float tot = block_sum(ss, red);

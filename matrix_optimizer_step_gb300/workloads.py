@@ -39,6 +39,9 @@ import torch
 NS_COEFFS = (3.4445, -4.7750, 2.0315)
 
 WORKLOADS = ("single_256x512", "gpt2_small", "many_small", "llama3_8b", "moe_experts")
+# Small stand-in used only to profile kernels on Llama-3-8B's shapes: one layer
+# (7 matrices, 2.18e8 elements) plus its two norm vectors.
+PROFILE_WORKLOADS = ("llama3_8b_layer",)
 
 _SMALL_SIDES = (64, 128, 256, 512, 1024, 2048)
 
@@ -132,19 +135,21 @@ def workload(name, tiny_extra=True):
                            grad_scale=float(10.0 ** logs[i]))
                 for i in range(4096)]
         return Workload(name, mats, [], _hyper(), grad_kind="normal")
-    if name == "llama3_8b":
+    if name in ("llama3_8b", "llama3_8b_layer"):
+        layers = 32 if name == "llama3_8b" else 1
         mats, vecs = [], []
         shapes = (("q", (4096, 4096)), ("k", (1024, 4096)), ("v", (1024, 4096)),
                   ("o", (4096, 4096)), ("gate", (14336, 4096)), ("up", (14336, 4096)),
                   ("down", (4096, 14336)))
-        for l in range(32):
+        for l in range(layers):
             for p, s in shapes:
                 mats.append(MatrixSpec(f"layers.{l}.{p}", s))
             vecs.append(VectorSpec(f"layers.{l}.input_norm", (4096,)))
             vecs.append(VectorSpec(f"layers.{l}.post_norm", (4096,)))
-        vecs += [VectorSpec("norm", (4096,)),
-                 VectorSpec("embed_tokens", (128256, 4096)),
-                 VectorSpec("lm_head", (128256, 4096))]
+        if layers == 32:
+            vecs += [VectorSpec("norm", (4096,)),
+                     VectorSpec("embed_tokens", (128256, 4096)),
+                     VectorSpec("lm_head", (128256, 4096))]
         return Workload(name, mats, vecs, _hyper(), grad_kind="student_t_rank8")
     if name == "moe_experts":
         g = torch.Generator().manual_seed(5)
@@ -266,3 +271,78 @@ def muon_elementwise_bytes(wl):
 def adamw_bytes(wl):
     """bf16 grad read, fp32 master/m/v read+write, bf16 param write."""
     return wl.adamw_numel * (2 + 24 + 2)
+
+
+# --------------------------------------------------------------------------
+# Device-resident materialisation (flat buffers, per-tensor views)
+# --------------------------------------------------------------------------
+
+@dataclass
+class Materialized:
+    """A workload's tensors as views into a few flat device buffers.
+
+    One flat buffer per role keeps every gradient in one contiguous block
+    (one host-to-device copy per step) and every bf16 parameter in another
+    (one device-to-host copy).  Views start on 256-byte boundaries.
+    """
+
+    wl: Workload
+    masters: list
+    momenta: list
+    grads: list
+    params: list
+    v_masters: list
+    v_exp_avg: list
+    v_exp_avg_sq: list
+    v_grads: list
+    v_params: list
+    flats: dict
+
+
+def _layout(sizes, align=128):
+    offs, o = [], 0
+    for s in sizes:
+        offs.append(o)
+        o += (s + align - 1) // align * align
+    return offs, max(o, align)
+
+
+def _views(flat, offs, shapes):
+    return [flat[o:o + math.prod(s)].view(s) for o, s in zip(offs, shapes)]
+
+
+def materialize(wl, device="cuda", step=0, progress=None):
+    """Allocate and fill every tensor of ``wl`` on ``device`` (seeded)."""
+    mshapes = [s.shape for s in wl.matrices]
+    vshapes = [(v.numel,) for v in wl.vectors]
+    gdt = wl.matrices[0].grad_dtype if wl.matrices else torch.bfloat16
+    moffs, mtot = _layout([math.prod(s) for s in mshapes])
+    voffs, vtot = _layout([math.prod(s) for s in vshapes])
+    f32 = dict(device=device, dtype=torch.float32)
+    flats = {
+        "master": torch.empty(mtot, **f32),
+        "momentum": torch.zeros(mtot, **f32),
+        "grad": torch.empty(mtot + vtot, device=device, dtype=gdt),
+        "param": torch.empty(mtot + vtot, device=device, dtype=torch.bfloat16),
+        "v_master": torch.empty(vtot, **f32),
+        "v_m": torch.zeros(vtot, **f32),
+        "v_v": torch.zeros(vtot, **f32),
+    }
+    masters = _views(flats["master"], moffs, mshapes)
+    momenta = _views(flats["momentum"], moffs, mshapes)
+    grads = _views(flats["grad"], moffs, mshapes)
+    params = _views(flats["param"], moffs, mshapes)
+    v_grads = _views(flats["grad"][mtot:], voffs, vshapes)
+    v_params = _views(flats["param"][mtot:], voffs, vshapes)
+    for i, spec in enumerate(wl.matrices):
+        masters[i].copy_(master_init(spec, i, device))
+        grads[i].copy_(muon_grad(wl, spec, i, step, device))
+        if progress:
+            progress(i)
+    v_masters = _views(flats["v_master"], voffs, vshapes)
+    for i, spec in enumerate(wl.vectors):
+        v_masters[i].copy_(vector_init(spec, i, device))
+        v_grads[i].copy_(vector_grad(spec, i, step, device).to(gdt))
+    return Materialized(wl, masters, momenta, grads, params, v_masters,
+                        _views(flats["v_m"], voffs, vshapes), _views(flats["v_v"], voffs, vshapes),
+                        v_grads, v_params, flats)
