@@ -176,6 +176,43 @@ DMUON_API int dmuon_muon_step(dmuon_context* ctx, const dmuon_matrix* mats, int3
                     float a, float b, float c, uint32_t flags, void* stream);
 
 /*
+ * dmuon_muon_step_noalloc -- the Muon step of one tensor, allocating nothing.
+ *
+ * The pages have no counterpart: this entry exists for callers that cannot
+ * call cudaMalloc -- code inside a framework that owns every device
+ * allocation through its own pool, code that must not grow its memory after
+ * start-up, or code that must not risk the implicit device synchronisation
+ * of cudaMalloc/cudaFree.  It computes what dmuon_muon_step computes for
+ * `mat` on the bf16 tensor-core path, but needs no context: all scratch
+ * (Newton-Schulz buffers, norm partials, descriptor tables, tensor maps)
+ * lives in one static device array of 64 MiB that every GPU loading this
+ * library holds until the process exits, and the host tables are built in a
+ * static 1 MiB host buffer.  No cudaMalloc, cudaFree or other allocating
+ * routine is called.
+ *
+ *   mat      host pointer to one descriptor (rank 2..4; leading dims are
+ *            separate matrices), device tensors as for dmuon_muon_step
+ *   flags    0 or DMUON_FLAG_NESTEROV (DMUON_FLAG_FP32_NS is rejected)
+ *   others   as for dmuon_muon_step; stream = cudaStream_t of the caller
+ *
+ * Limits: the tensor's scratch (about 8 bytes per element of every m x n
+ * slice plus 8 bytes per element of every p x p Gram, p = min(m, n), plus
+ * tables) must fit in 64 MiB -- e.g. one 2048 x 2048 matrix -- else
+ * DMUON_ERR_SHAPE with the byte counts in dmuon_last_error().
+ * The first call on a device looks up the array's device address with
+ * cudaGetSymbolAddress (once per device, with that device current); make
+ * that first call before any stream capture.  Every call shares the one
+ * array and it keeps the previous call's contents: calls whose work
+ * overlaps on the GPU (different streams, or different host threads without
+ * ordering) race on it.  The device error word lives in the array too; it
+ * is cleared at the start of each call and is not reported.
+ * Errors: as dmuon_muon_step, plus DMUON_ERR_SHAPE for the size limit.
+ */
+DMUON_API int dmuon_muon_step_noalloc(const dmuon_matrix* mat, float lr, float momentum, float wd,
+                                      int32_t ns_steps, float a, float b, float c, uint32_t flags,
+                                      void* stream);
+
+/*
  * dmuon_adamw_step -- one AdamW step over n flattened tensors ("Pure DMuon
  * 路由": routes "adamw" and "sharded_adamw" both run AdamW; the shard
  * placement is outside this call).  In fp32, per element:

@@ -24,6 +24,7 @@ from .capi import (  # noqa: F401
     dmuon_kernel_launches,
     dmuon_lpt_assign,
     dmuon_muon_step,
+    dmuon_muon_step_noalloc,
     dmuon_profile,
     dmuon_profile_read,
     dmuon_selftest_wait_timeout,

@@ -37,7 +37,7 @@ EXPORTED = (
     "dmuon_status_string", "dmuon_last_error", "dmuon_lpt_assign", "dmuon_context_create",
     "dmuon_context_destroy", "dmuon_muon_step", "dmuon_adamw_step", "dmuon_sync",
     "dmuon_selftest_wait_timeout", "dmuon_set_tuning", "dmuon_kernel_launches", "dmuon_profile",
-    "dmuon_profile_read",
+    "dmuon_profile_read", "dmuon_muon_step_noalloc",
 )
 
 KERNEL_KINDS = ("momentum", "norm", "ns_gram", "ns_poly", "ns_combine", "update", "adamw")
@@ -104,6 +104,8 @@ def load_library(path=LIB_PATH):
         "dmuon_kernel_launches": (i64, [vp]),
         "dmuon_profile": (ctypes.c_int, [vp, i32]),
         "dmuon_profile_read": (ctypes.c_int, [vp, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(i64)]),
+        "dmuon_muon_step_noalloc": (ctypes.c_int, [ctypes.POINTER(DmuonMatrix), f32, f32, f32, i32, f32, f32,
+                                                   f32, ctypes.c_uint32, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -252,3 +254,12 @@ def dmuon_profile_read(ctx):
     cnt = (ctypes.c_int64 * n)()
     _check(load_library().dmuon_profile_read(ctx, ms, cnt))
     return {k: (ms[i], cnt[i]) for i, k in enumerate(KERNEL_KINDS)}
+
+
+def dmuon_muon_step_noalloc(mat, lr, momentum, wd, ns_steps, a, b, c, flags=DMUON_FLAG_NESTEROV,
+                            stream=None):
+    """Muon step of one tensor with all scratch in the library's static device
+    array (no device allocation).  ``mat`` is one DmuonMatrix."""
+    _check(load_library().dmuon_muon_step_noalloc(
+        ctypes.byref(mat), float(lr), float(momentum), float(wd), int(ns_steps), float(a), float(b),
+        float(c), int(flags), _stream_handle(stream)))
