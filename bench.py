@@ -179,6 +179,17 @@ def cpu_cores():
         return os.cpu_count()
 
 
+def reduce_max_over_ranks(value, dist, device):
+    """Slowest rank's value (every rank gets it); identity without a process group."""
+    if dist is None:
+        return value
+    import torch
+
+    t = torch.tensor([float(value)], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 # ---------------------------------------------------------------- main legs
 def run_reference(args, wl, rank, world):
     if rank != 0:
@@ -222,6 +233,9 @@ def run_ours(args, wl, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     mos.load_library()
+    for kv in args.tuning:
+        k, v = kv.split("=")
+        mos.dmuon_set_tuning(int(k), int(v))
     h = wl.hyper
     mat = W.materialize(wl, dev)
     step = mos.OwnerStep(local_rank)
@@ -268,11 +282,7 @@ def run_ours(args, wl, rank, world, local_rank):
     step.profile(False)
     clk = clocks.stop()
     step.sync(stream)
-    ms = e0.elapsed_time(e1) / args.steps
-    if dist is not None:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = reduce_max_over_ranks(e0.elapsed_time(e1) / args.steps, dist, dev)
 
     # ---------------- end to end: host grads in, host bf16 params out
     e2e_steps = max(1, min(args.steps, 3))
@@ -292,11 +302,7 @@ def run_ours(args, wl, rank, world, local_rank):
     x1.record(stream)
     torch.cuda.synchronize()
     barrier()
-    e2e_ms = x0.elapsed_time(x1) / e2e_steps
-    if dist is not None:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = reduce_max_over_ranks(x0.elapsed_time(x1) / e2e_steps, dist, dev)
     h2d = g_flat.numel() * g_flat.element_size()
     d2h = p_flat.numel() * p_flat.element_size()
     del host_g, host_p
@@ -308,6 +314,10 @@ def run_ours(args, wl, rank, world, local_rank):
     ns_ms = sum(prof[k][0] for k in ("ns_gram", "ns_poly", "ns_combine")) / args.steps
     ns_launches = sum(prof[k][1] for k in ("ns_gram", "ns_poly", "ns_combine"))
     ns_tflops = ns_flops / (ns_ms / 1e3) / 1e12 if ns_ms > 0 else None
+    # Roofline on the flops the symmetric kernels execute (upper triangles of
+    # X X^T and A A), not the dense count, so the fraction is not inflated.
+    ns_exec = W.workload_ns_flops_executed(wl) if not h["fp32_ns"] else ns_flops
+    ns_exec_tflops = ns_exec / (ns_ms / 1e3) / 1e12 if ns_ms > 0 else None
     ew_bytes = W.muon_elementwise_bytes(wl) + W.adamw_bytes(wl)
     ew_ms = sum(prof[k][0] for k in ("momentum", "norm", "update", "adamw")) / args.steps
     ew_gbs = ew_bytes / (ew_ms / 1e3) / 1e9 if ew_ms > 0 else None
@@ -319,7 +329,7 @@ def run_ours(args, wl, rank, world, local_rank):
             import hashlib
 
             tj = json.load(open(tpath))
-            src = open(os.path.join(ROOT, "matrix_optimizer_step_gb300", "csrc", "k_ns_tc.cu"), "rb").read()
+            src = open(os.path.join(ROOT, "matrix_optimizer_step_gb300", "csrc", "k_ns_tc2.cu"), "rb").read()
             if tj.get("kernel_sha256") == hashlib.sha256(src).hexdigest() and tj.get("workload") == wl.name:
                 traffic = tj.get("bytes_per_step")
         except (OSError, ValueError, KeyError):
@@ -333,12 +343,14 @@ def run_ours(args, wl, rank, world, local_rank):
                    "ns_operands": "fp32 in NS mode" if h["fp32_ns"] else "bf16 operands, fp32 accumulate",
                    "state": "fp32 master/momentum/AdamW moments, bf16 grads and params",
                    "l2": "inputs larger than L2 (no flush needed)", "parallelism": f"replicas x{world}"},
-        "ns_tflops": ns_tflops,
-        "ns_frac_of_bf16_sustained": (ns_tflops / peak) if ns_tflops else None,
-        "ns_frac_of_bf16_burst": (ns_tflops / peaks["bf16_burst"]) if ns_tflops else None,
-        "roofline": {"bound": "tensor", "kernel": "ns_tc_kernel (all NS phases)",
-                     "achieved": ns_tflops, "peak": peak, "unit": "TFLOP/s",
-                     "frac": (ns_tflops / peak) if ns_tflops else None,
+        "ns_tflops_dense_count": ns_tflops,
+        "ns_tflops_executed": ns_exec_tflops,
+        "ns_tflop_per_step": {"dense_count": ns_flops / 1e12, "executed": ns_exec / 1e12},
+        "ns_dense_count_frac_of_bf16_sustained": (ns_tflops / peak) if ns_tflops else None,
+        "roofline": {"bound": "tensor", "kernel": "ns_tc2_kernel (all NS phases, executed flops)",
+                     "achieved": ns_exec_tflops, "peak": peak, "unit": "TFLOP/s",
+                     "frac": (ns_exec_tflops / peak) if ns_exec_tflops else None,
+                     "frac_of_burst": (ns_exec_tflops / peaks["bf16_burst"]) if ns_exec_tflops else None,
                      "peak_src": f"{peaks['src']} bf16 sustained",
                      "traffic": traffic, "launches_per_step": ns_launches / args.steps},
         "elementwise": {"bound": "hbm", "achieved": ew_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
@@ -369,6 +381,8 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default="llama3_8b")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--tuning", action="append", default=[],
+                    help="KEY=VALUE passed to dmuon_set_tuning before the run")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

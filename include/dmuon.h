@@ -249,6 +249,9 @@ DMUON_API int dmuon_selftest_wait_timeout(dmuon_context* ctx, int32_t timeout_us
  *   key 1: operand-descriptor variant of the tcgen05 path for M/N-contiguous
  *          operands (0 = LBO spans 64-element MN blocks, the default;
  *          1 = the two offsets exchanged).  Kept for layout bring-up tests.
+ *   key 2: tensor-core kernel of the Newton-Schulz phases (1 = CTA pairs,
+ *          cta_group::2, on 256 x 256 tiles, the default; 0 = one CTA per
+ *          128 x 256 tile).
  * Returns DMUON_ERR_INVALID_ARG for an unknown key.  Not thread-safe with
  * respect to concurrent steps.
  */

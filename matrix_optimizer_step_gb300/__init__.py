@@ -33,4 +33,4 @@ from .capi import (  # noqa: F401
     dmuon_sync,
     load_library,
 )
-from .optim import OwnerStep  # noqa: F401
+from .optim import OwnerStep, owner_partition  # noqa: F401

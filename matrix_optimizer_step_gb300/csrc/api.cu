@@ -35,6 +35,10 @@ namespace dmuon {
 
 void set_tc_mn_swap(int v);
 
+// Which tensor-core kernel runs the NS phases: 1 = CTA pairs on 256 x 256
+// tiles (default), 0 = one CTA per 128 x 256 tile.
+static int g_ns_pairs = 1;
+
 // ------------------------------------------------------------------ errors
 namespace {
 thread_local std::string g_last_error;
@@ -189,7 +193,8 @@ struct MuonPlan {
   // Problem tables per kind and variant: 0/1 = X in buffer 0/1 (later
   // iterations), 2 = first iteration, 3 = second iteration.
   DevBuf probs[3][4];
-  PhaseTiles phase[3];
+  PhaseTiles phase[3];   // fp32 path or one-CTA tensor-core tiles
+  PhaseTiles phase2[3];  // CTA-pair tensor-core tiles (bf16 path only)
   void release() {
     chunks_dev.release();
     partials.release();
@@ -197,11 +202,12 @@ struct MuonPlan {
     maps.release();
     for (auto& k : probs)
       for (auto& p : k) p.release();
-    for (auto& p : phase) {
-      p.tiles.release();
-      p.cta_begin.release();
-      p.n_tiles = p.n_ctas = 0;
-    }
+    for (auto* ph : {phase, phase2})
+      for (int k = 0; k < 3; ++k) {
+        ph[k].tiles.release();
+        ph[k].cta_begin.release();
+        ph[k].n_tiles = ph[k].n_ctas = 0;
+      }
     slices.clear();
     classes.clear();
     chunks.clear();
@@ -381,8 +387,12 @@ int make_map(EncodeTiledFn enc, CUtensorMap* out, void* base, int64_t inner, int
 }
 
 // Build the tile list of one phase and balance it over persistent CTAs.
-int build_phase_tiles(const std::vector<NsProblem>& probs, bool fp32, int num_sms, PhaseTiles& out) {
-  const int bm = fp32 ? kSimtBM : kTcBM, bn = fp32 ? kSimtBN : kTcBN;
+// Tile geometry: 0 = fp32 CUDA-core tiles, 1 = one-CTA tcgen05 tiles,
+// 2 = CTA-pair tcgen05 tiles.  `slots` = persistent CTAs (or CTA pairs).
+int build_phase_tiles(const std::vector<NsProblem>& probs, int geometry, int slots, PhaseTiles& out) {
+  const bool fp32 = geometry == 0;
+  const int bm = geometry == 0 ? kSimtBM : geometry == 1 ? kTcBM : kTc2Tile;
+  const int bn = geometry == 0 ? kSimtBN : geometry == 1 ? kTcBN : kTc2Tile;
   std::vector<uint2> tiles;
   std::vector<int64_t> cost;
   for (size_t p = 0; p < probs.size(); ++p) {
@@ -391,7 +401,7 @@ int build_phase_tiles(const std::vector<NsProblem>& probs, bool fp32, int num_sm
     const int64_t c = (P.K + kTcBK - 1) / kTcBK + 2;
     for (int i = 0; i < tm; ++i)
       for (int j = 0; j < tn; ++j) {
-        if (P.sym && (i * bm) / kTcBN > j) continue;  // below the diagonal: mirrored
+        if (P.sym && (i * bm) / bn > j) continue;  // below the diagonal: mirrored
         tiles.push_back(make_uint2(static_cast<uint32_t>(p), (static_cast<uint32_t>(i) << 16) | static_cast<uint32_t>(j)));
         cost.push_back(c);
       }
@@ -403,7 +413,7 @@ int build_phase_tiles(const std::vector<NsProblem>& probs, bool fp32, int num_sm
     if (st != DMUON_OK) return st;
     return upload(out.cta_begin, std::vector<int32_t>{0, out.n_tiles});
   }
-  const int R = std::max(1, std::min(num_sms, out.n_tiles));
+  const int R = std::max(1, std::min(slots, out.n_tiles));
   std::vector<int32_t> slot(tiles.size());
   std::vector<int32_t> order;
   int st = lpt_assign_impl(cost.data(), out.n_tiles, R, slot.data(), nullptr, &order);
@@ -631,8 +641,13 @@ int build_muon_plan(dmuon_context* ctx, const dmuon_matrix* mats, int n, bool fp
       if (st != DMUON_OK) return st;
     }
   for (int kind = 0; kind < 3; ++kind) {
-    st = build_phase_tiles(var[kind][0], fp32, ctx->num_sms, P.phase[kind]);
+    st = build_phase_tiles(var[kind][0], fp32 ? 0 : 1, ctx->num_sms, P.phase[kind]);
     if (st != DMUON_OK) return st;
+    if (!fp32) {
+      const int pairs = std::max(1, std::min(ctx->num_sms / 2, ns_tc2_max_pairs()));
+      st = build_phase_tiles(var[kind][0], 2, pairs, P.phase2[kind]);
+      if (st != DMUON_OK) return st;
+    }
   }
   P.key = key;
   return DMUON_OK;
@@ -809,9 +824,13 @@ int dmuon_muon_step(dmuon_context* ctx, const dmuon_matrix* mats, int32_t n, flo
       L.b = b;
       L.c = c;
       L.err = static_cast<int*>(ctx->err.p);
-      const PhaseTiles& T = P.phase[kind];
+      const bool pairs = !fp32 && g_ns_pairs;
+      const PhaseTiles& T = pairs ? P.phase2[kind] : P.phase[kind];
+      L.tiles = static_cast<const uint2*>(T.tiles.p);
+      L.cta_begin = static_cast<const int32_t*>(T.cta_begin.p);
       st = timed_launch(ctx, DMUON_KERNEL_NS_GRAM + kind, s, [&] {
-        return fp32 ? launch_ns_simt(L, T.n_tiles, s) : launch_ns_tc(L, T.n_ctas, s);
+        if (fp32) return launch_ns_simt(L, T.n_tiles, s);
+        return pairs ? launch_ns_tc2(L, T.n_ctas, s) : launch_ns_tc(L, T.n_ctas, s);
       });
       if (st != DMUON_OK) return st;
     }
@@ -967,6 +986,10 @@ int dmuon_set_tuning(int32_t key, int32_t value) {
   clear_error();
   if (key == 1) {
     set_tc_mn_swap(value ? 1 : 0);
+    return DMUON_OK;
+  }
+  if (key == 2) {
+    g_ns_pairs = value ? 1 : 0;
     return DMUON_OK;
   }
   return set_error(DMUON_ERR_INVALID_ARG, "set_tuning: unknown key");

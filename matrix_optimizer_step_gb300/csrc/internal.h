@@ -129,10 +129,14 @@ cudaError_t launch_adamw(const VecDesc* vecs, const Chunk* chunks, int n_chunks,
 cudaError_t launch_selftest_wait(int* err, long long timeout_ns, cudaStream_t st);
 
 cudaError_t launch_ns_tc(const NsLaunch& L, int n_ctas, cudaStream_t st);
+// CTA-pair variant: tiles are kTc2Tile x kTc2Tile, cta_begin is indexed by pair.
+cudaError_t launch_ns_tc2(const NsLaunch& L, int n_pairs, cudaStream_t st);
+int ns_tc2_max_pairs();
 cudaError_t launch_ns_simt(const NsLaunch& L, int n_tiles, cudaStream_t st);
 
 // Tile geometry of the two Newton-Schulz GEMM paths.
 constexpr int kTcBM = 128, kTcBN = 256, kTcBK = 64;
+constexpr int kTc2Tile = 256;
 constexpr int kSimtBM = 64, kSimtBN = 64;
 constexpr int kChunkElems = 1 << 16;
 

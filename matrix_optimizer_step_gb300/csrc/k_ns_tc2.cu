@@ -1,0 +1,284 @@
+// Newton-Schulz phase GEMM on tcgen05 with CTA pairs (cta_group::2).
+//
+// Same phases, problems and epilogues as k_ns_tc.cu ("架构设计" §1: A = X X^T,
+// B = b A + c A A, X <- a X + B X), but each output tile is 256 x 256 and is
+// computed by a cluster of two CTAs on two SMs:
+//   * CTA r of the pair loads rows [128r, 128r+128) of the tile's A operand
+//     and columns [128r, 128r+128) of its B operand (K-contiguous: one
+//     64 x 128 TMA box; M/N-contiguous: two 64 x 64 boxes) into its own
+//     shared memory, and the completion of both CTAs' copies is counted on
+//     the leader CTA's `full` barrier;
+//   * one thread of the leader (rank 0) issues tcgen05.mma.cta_group::2
+//     with M = 256, N = 256, K = 16: the tensor cores read A from both CTAs
+//     and B from both CTAs, and each CTA's TMEM receives its own 128 rows of
+//     the fp32 accumulator;
+//   * tcgen05.commit with a two-CTA multicast frees the ring slot in both
+//     CTAs and hands the accumulator to both CTAs' epilogue warps, which run
+//     the shared fused epilogue on their own 128 rows and then arrive on the
+//     leader's `tempty` barrier (8 arrivals: 4 warps per CTA).
+// Per SM and per 16-deep k-step the operands are 128 x 16 of A and 128 x 16
+// of B (8 KiB) for 128 x 256 x 16 multiply-adds, against 12 KiB in the
+// one-CTA kernel: two thirds of the shared-memory fill and L2 read traffic
+// per flop.
+//
+// Every spin-wait is bounded; on a timeout the CTA records the error, stops
+// issuing, and both CTAs meet at the final cluster barrier before the pair
+// frees its TMEM.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "internal.h"
+#include "ns_epilogue.cuh"
+#include "ptx.cuh"
+
+namespace dmuon {
+namespace {
+
+constexpr int TILE = kTc2Tile;  // 256 x 256 per CTA pair
+constexpr int BK = 64;
+constexpr int STAGES = 6;
+constexpr uint32_t HALF_BYTES = 128 * BK * 2;         // 16 KiB: 128 rows x 64 k, bf16
+constexpr uint32_t STAGE_BYTES = 2 * HALF_BYTES;      // A half + B half per CTA
+constexpr uint32_t MN_BOX_BYTES = 64 * 64 * 2;        // 8 KiB
+constexpr int kThreads = 192;
+constexpr uint32_t kTmemCols = 512;
+constexpr int kNumBars = 2 * STAGES + 2 + 2 + 1;
+constexpr size_t kSmemBytes = 1024 + STAGES * STAGE_BYTES + kNumBars * 8 + 16;
+static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+
+__device__ __forceinline__ uint64_t desc_k(uint32_t base, int kk) {
+  return smem_desc_sw128(base + 32u * kk, 16u, 1024u);
+}
+__device__ __forceinline__ uint64_t desc_mn(uint32_t base, int kk) {
+  return smem_desc_sw128(base + 2048u * kk, MN_BOX_BYTES, 1024u);
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) ns_tc2_kernel(const NsLaunch L) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t ring = smem_u32(smem);
+  uint64_t* bar_mem = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_mem + kNumBars);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const uint32_t bar0 = smem_u32(bar_mem);
+  auto full = [&](int s) { return bar0 + 8u * s; };
+  auto empty = [&](int s) { return bar0 + 8u * (STAGES + s); };
+  auto tfull = [&](int a) { return bar0 + 8u * (2 * STAGES + a); };
+  auto tempty = [&](int a) { return bar0 + 8u * (2 * STAGES + 2 + a); };
+  const uint32_t drain = bar0 + 8u * (2 * STAGES + 4);
+
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const int pair = blockIdx.x >> 1;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full(s), 1);
+      mbar_init(empty(s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull(a), 1);
+      mbar_init(tempty(a), 8);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    fence_proxy_async_smem();
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  cluster_sync_all();  // both CTAs' barriers exist before any cross-CTA signal
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int t_begin = L.cta_begin[pair];
+  const int t_end = L.cta_begin[pair + 1];
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int fills[STAGES] = {0, 0, 0, 0, 0, 0};
+      bool ok = true;
+      for (int t = t_begin; t < t_end && ok; ++t) {
+        const uint2 tile = L.tiles[t];
+        const NsProblem& P = L.probs[tile.x];
+        const int m0 = static_cast<int>(tile.y >> 16) * TILE + 128 * static_cast<int>(rank);
+        const int n0 = static_cast<int>(tile.y & 0xFFFFu) * TILE + 128 * static_cast<int>(rank);
+        const CUtensorMap* ma = L.maps + P.map_a;
+        const CUtensorMap* mb = L.maps + P.map_b;
+        const bool a_mn = (P.majors & 1) != 0;
+        const bool b_mn = (P.majors & 2) != 0;
+        const int z = P.z;
+        const int nk = (P.K + BK - 1) / BK;
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!mbar_wait_bounded_cluster(empty(stage), phase ^ 1u, abort_flag, L.err, kErrTimeoutProducer)) {
+            ok = false;
+            break;
+          }
+          const uint32_t leader_full = mapa_shared(full(stage), 0);
+          if (leader) mbar_expect_tx(full(stage), 2 * STAGE_BYTES);
+          ++fills[stage];
+          const uint32_t sa = ring + stage * STAGE_BYTES;
+          const uint32_t sb = sa + HALF_BYTES;
+          const int k0 = kb * BK;
+          if (!a_mn) {
+            tma_load_3d_pair(sa, ma, leader_full, k0, m0, z);
+          } else {
+            tma_load_3d_pair(sa, ma, leader_full, m0, k0, z);
+            tma_load_3d_pair(sa + MN_BOX_BYTES, ma, leader_full, m0 + 64, k0, z);
+          }
+          if (!b_mn) {
+            tma_load_3d_pair(sb, mb, leader_full, k0, n0, z);
+          } else {
+            tma_load_3d_pair(sb, mb, leader_full, n0, k0, z);
+            tma_load_3d_pair(sb + MN_BOX_BYTES, mb, leader_full, n0 + 64, k0, z);
+          }
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok && leader) {
+        // The leader's barrier counts both CTAs' bytes: let every armed phase
+        // land before the pair tears down.
+        for (int s = 0; s < STAGES; ++s) {
+          if (fills[s] > 0) {
+            volatile int no_abort = 0;
+            mbar_wait_bounded_cluster(full(s), static_cast<uint32_t>(fills[s] - 1) & 1u, &no_abort, nullptr, 0,
+                                      100000000ull);
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------- MMA issuer (leader only)
+    if (leader && lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      int local = 0;
+      for (int t = t_begin; t < t_end && ok; ++t, ++local) {
+        const uint2 tile = L.tiles[t];
+        const NsProblem& P = L.probs[tile.x];
+        const bool a_mn = (P.majors & 1) != 0;
+        const bool b_mn = (P.majors & 2) != 0;
+        const uint32_t idesc = idesc_bf16_f32(TILE, TILE, a_mn, b_mn);
+        const int nk = (P.K + BK - 1) / BK;
+        const int acc = local & 1;
+        const uint32_t acc_phase = static_cast<uint32_t>(local >> 1) & 1u;
+        if (!mbar_wait_bounded_cluster(tempty(acc), acc_phase ^ 1u, abort_flag, L.err, kErrTimeoutMma)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * TILE);
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!mbar_wait_bounded_cluster(full(stage), phase, abort_flag, L.err, kErrTimeoutMma)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = ring + stage * STAGE_BYTES;
+          const uint32_t sb = sa + HALF_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            const uint64_t ad = a_mn ? desc_mn(sa, kk) : desc_k(sa, kk);
+            const uint64_t bd = b_mn ? desc_mn(sb, kk) : desc_k(sb, kk);
+            umma_bf16_pair(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+          }
+          umma_commit_pair_multicast(empty(stage), 0x3);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (ok) umma_commit_pair_multicast(tfull(acc), 0x3);
+      }
+      umma_commit_pair_multicast(drain, 0x1);
+      volatile int no_abort = 0;
+      mbar_wait_bounded_cluster(drain, 0, &no_abort, L.err, kErrTimeoutDrain);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int quarter = warp & 3;
+    const int row_in_tile = 128 * static_cast<int>(rank) + quarter * 32 + lane;
+    int local = 0;
+    for (int t = t_begin; t < t_end; ++t, ++local) {
+      const uint2 tile = L.tiles[t];
+      const NsProblem& P = L.probs[tile.x];
+      const int tm = static_cast<int>(tile.y >> 16), tn = static_cast<int>(tile.y & 0xFFFFu);
+      const int acc = local & 1;
+      const uint32_t acc_phase = static_cast<uint32_t>(local >> 1) & 1u;
+      if (!mbar_wait_bounded_cluster(tfull(acc), acc_phase, abort_flag, L.err, kErrTimeoutEpilogue)) break;
+      tc_fence_after();
+      const uint32_t t_lane =
+          tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * TILE);
+      ns_epilogue_tile(L, P, tm * TILE, tn * TILE, row_in_tile, t_lane, P.sym && tm < tn);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if (leader)
+          mbar_arrive(tempty(acc));
+        else
+          mbar_arrive_cluster(mapa_shared(tempty(acc), 0));
+      }
+    }
+  }
+
+  tc_fence_before();
+  cluster_sync_all();  // all MMAs drained, no more cross-CTA traffic
+  tc_fence_after();
+  if (warp == 1) {
+    __syncwarp();
+    tmem_dealloc_pair(tmem_base, kTmemCols);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_ns_tc2(const NsLaunch& L, int n_pairs, cudaStream_t st) {
+  if (n_pairs <= 0) return cudaSuccess;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(ns_tc2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kSmemBytes));
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  ns_tc2_kernel<<<2 * n_pairs, kThreads, kSmemBytes, st>>>(L);
+  return cudaGetLastError();
+}
+
+// Largest number of CTA pairs of this kernel that can be resident at once.
+int ns_tc2_max_pairs() {
+  static int cached = -1;
+  if (cached >= 0) return cached;
+  if (cudaFuncSetAttribute(ns_tc2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(kSmemBytes)) != cudaSuccess) {
+    cudaGetLastError();
+    return cached = 0;
+  }
+  cudaLaunchConfig_t cfg = {};  // cluster shape comes from __cluster_dims__
+  cfg.gridDim = dim3(2, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, ns_tc2_kernel, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    n = 0;
+  }
+  return cached = n;
+}
+
+}  // namespace dmuon

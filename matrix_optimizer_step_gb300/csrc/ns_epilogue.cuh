@@ -1,0 +1,129 @@
+// Fused epilogue of one Newton-Schulz output tile, shared by the one-CTA and
+// the CTA-pair tcgen05 kernels.  One epilogue warp drains its 32 TMEM lanes
+// (rows) of the accumulator, 32 columns at a time, applies the phase's
+// epilogue (see NsKind) and stores bf16 (plus the optional fp32 copy, plus the
+// transposed copy of a symmetric off-diagonal block).
+#pragma once
+
+#include <stdint.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace dmuon {
+
+// row_in_tile: this thread's row within the tile; tmem_lane_base: TMEM
+// address of this warp's lane quarter at column 0 of the accumulator.
+// Tiles are 256 columns wide; `mirror` tiles are strictly above the
+// diagonal of a symmetric output.
+__device__ __forceinline__ void ns_epilogue_tile(const NsLaunch& L, const NsProblem& P, int m0, int n0,
+                                                 int row_in_tile, uint32_t tmem_lane_base, bool mirror) {
+  constexpr int BN = 256;
+  const uint32_t t_lane = tmem_lane_base;
+  float g = 1.f;
+  if (L.gscale && L.gpow > 0) {
+    const float s = L.gscale[P.slice];
+    g = (L.gpow == 2) ? s * s : s;
+  }
+  float alpha, beta;
+  if (L.kind == kGram) {
+    alpha = g;
+    beta = 0.f;
+  } else if (L.kind == kPoly) {
+    alpha = L.c;
+    beta = L.b;
+  } else {
+    alpha = g;
+    beta = g * L.a;
+  }
+  const int row = m0 + row_in_tile;
+  const bool row_ok = row < P.M;
+  uint16_t* out_row = reinterpret_cast<uint16_t*>(P.out) + static_cast<int64_t>(row) * P.ld_out;
+  const uint16_t* aux_row =
+      reinterpret_cast<const uint16_t*>(P.aux) + static_cast<int64_t>(row) * P.ld_aux;
+  const float* auxf_row = reinterpret_cast<const float*>(P.aux) + static_cast<int64_t>(row) * P.ld_aux;
+  float* out2_row = P.out2 ? P.out2 + static_cast<int64_t>(row) * P.ld_out2 : nullptr;
+  const bool aux_f32 = L.aux_f32 != 0;
+#pragma unroll 1
+  for (int cc = 0; cc < BN / 32; ++cc) {
+    const int col0 = n0 + cc * 32;
+    if (col0 >= P.N) break;  // warp-uniform
+    __syncwarp();
+    uint32_t r[32];
+    tmem_ld_32x32b_x32(t_lane + static_cast<uint32_t>(cc * 32), r);
+    const bool full_chunk = (col0 + 32 <= P.N);
+    float auxf[32];
+    if (beta != 0.f && row_ok && full_chunk) {
+      if (aux_f32) {
+        const float4* src = reinterpret_cast<const float4*>(auxf_row + col0);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float4 q = __ldg(src + i);
+          auxf[4 * i] = q.x; auxf[4 * i + 1] = q.y; auxf[4 * i + 2] = q.z; auxf[4 * i + 3] = q.w;
+        }
+      } else {
+        const uint4* src = reinterpret_cast<const uint4*>(aux_row + col0);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const uint4 q = __ldg(src + i);
+          const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            auxf[8 * i + 2 * j] = __uint_as_float(w[j] << 16);
+            auxf[8 * i + 2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+          }
+        }
+      }
+    }
+    tmem_ld_wait();
+    if (!row_ok) {
+      // rows past M: nothing to store
+    } else if (full_chunk) {
+      float v[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        v[j] = alpha * __uint_as_float(r[j]);
+        if (beta != 0.f) v[j] = fmaf(beta, auxf[j], v[j]);
+      }
+      uint4* dst = reinterpret_cast<uint4*>(out_row + col0);
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        dst[i] = make_uint4(pack_bf16x2(v[8 * i], v[8 * i + 1]), pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
+                            pack_bf16x2(v[8 * i + 4], v[8 * i + 5]), pack_bf16x2(v[8 * i + 6], v[8 * i + 7]));
+      if (out2_row) {
+        float4* d2 = reinterpret_cast<float4*>(out2_row + col0);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) d2[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+      }
+      if (mirror) {
+        // Transposed copy: for each column j the warp's 32 lanes hold 32
+        // consecutive rows, so every store instruction writes one
+        // contiguous 64-byte (bf16) or 128-byte (fp32) run.
+        uint16_t* mo = reinterpret_cast<uint16_t*>(P.out) + row;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) mo[static_cast<int64_t>(col0 + j) * P.ld_out] = to_bf16_bits(v[j]);
+        if (P.out2) {
+          float* m2 = P.out2 + row;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) m2[static_cast<int64_t>(col0 + j) * P.ld_out2] = v[j];
+        }
+      }
+    } else {
+      for (int j = 0; j < 32 && col0 + j < P.N; ++j) {
+        float v = alpha * __uint_as_float(r[j]);
+        if (beta != 0.f)
+          v = fmaf(beta, aux_f32 ? auxf_row[col0 + j] : bf16_bits_to_f32(aux_row[col0 + j]), v);
+        const uint16_t vb = to_bf16_bits(v);
+        out_row[col0 + j] = vb;
+        if (out2_row) out2_row[col0 + j] = v;
+        if (mirror) {
+          const int64_t mi = static_cast<int64_t>(col0 + j);
+          reinterpret_cast<uint16_t*>(P.out)[mi * P.ld_out + row] = vb;
+          if (P.out2) P.out2[mi * P.ld_out2 + row] = v;
+        }
+      }
+    }
+  }
+}
+
+}  // namespace dmuon

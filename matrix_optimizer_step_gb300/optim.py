@@ -110,3 +110,11 @@ class OwnerStep:
             self.close()
         except Exception:
             pass
+
+
+def owner_partition(numels, n_owners):
+    """Owner rank of each Muon tensor: one global LPT pass over all tensors
+    ("架构设计" §3.1), element count as the cost.  Deterministic, so every
+    rank computes the same map on its own and each tensor has exactly one
+    owner.  Returns (owner per tensor, elements per owner)."""
+    return capi.dmuon_lpt_assign([int(n) for n in numels], int(n_owners))

@@ -250,6 +250,18 @@ def ns_flops(m, n, steps):
     return steps * (4 * p * p * q + 2 * p ** 3)
 
 
+def ns_flops_executed(m, n, steps):
+    """Flops the symmetric kernels execute: the Gram X X^T and the square
+    A A are symmetric, so only their upper triangle is formed (p(p+1)/2
+    dot products each), while B X is computed in full."""
+    p, q = min(m, n), max(m, n)
+    return steps * (p * (p + 1) * q + p * (p + 1) * p + 2 * p * p * q)
+
+
+def workload_ns_flops_executed(wl):
+    return sum(ns_flops_executed(*s.mn, wl.hyper["ns_steps"]) * s.n_slices for s in wl.matrices)
+
+
 def workload_ns_flops(wl):
     return sum(ns_flops(*s.mn, wl.hyper["ns_steps"]) * s.n_slices for s in wl.matrices)
 

@@ -155,10 +155,12 @@ def test_mn_major_descriptor_variant_report(cuda_lib, capsys):
     errs = {}
     for v in (0, 1):
         cuda_lib.dmuon_set_tuning(1, v)
+        cuda_lib.dmuon_set_tuning(2, 0)  # the descriptor switch lives in the one-CTA kernel
         try:
             res = run_muon(cuda_lib, shapes, seed=7)[0]
         finally:
             cuda_lib.dmuon_set_tuning(1, 0)
+            cuda_lib.dmuon_set_tuning(2, 1)
         errs[v] = [r["O"] for r in res]
     with capsys.disabled():
         print(f"\nMN-major descriptor variants: default {errs[0]}  exchanged {errs[1]}")
@@ -242,3 +244,52 @@ def test_validation_errors_leave_tensors_untouched(cuda_lib):
         assert torch.equal(w, w0)
     finally:
         cuda_lib.dmuon_context_destroy(ctx)
+
+
+# ------------------------------------------------ CTA-pair tensor-core kernel
+
+PAIR_SHAPES = [(256, 512), (384, 128), (512, 512), (200, 328), (328, 200), (3, 4), (16, 8),
+               (130, 1000), (1000, 130), (3, 64, 96), (64, 64), (520, 520), (1024, 256), (256, 1024)]
+
+
+@pytest.fixture
+def one_cta_kernel(cuda_lib):
+    cuda_lib.dmuon_set_tuning(2, 0)
+    yield cuda_lib
+    cuda_lib.dmuon_set_tuning(2, 1)
+
+
+def test_pair_kernel_grouped(cuda_lib):
+    res = run_muon(cuda_lib, PAIR_SHAPES, seed=21)[0]
+    for r in res:
+        assert r["buf"] <= 1e-6 and r["param_exact"], r
+        assert max(r["O_slices"]) <= bf16_tol(r["shape"]), r
+
+
+def test_pair_kernel_multi_step_and_ns_counts(cuda_lib):
+    for errs in run_muon(cuda_lib, [(512, 768), (768, 512)], seed=22, steps=2):
+        for r in errs:
+            assert r["O"] <= 2e-2, r
+    for k in (1, 2, 3):
+        for r in run_muon(cuda_lib, [(300, 260), (260, 300)], seed=23, ns_steps=k)[0]:
+            assert r["O"] <= 2e-2, r
+
+
+def test_one_cta_kernel_grouped(one_cta_kernel):
+    # The one-CTA tensor-core kernel (tuning key 2 = 0) on the same cases.
+    res = run_muon(one_cta_kernel, PAIR_SHAPES, seed=21)[0]
+    for r in res:
+        assert r["buf"] <= 1e-6 and r["param_exact"], r
+        assert max(r["O_slices"]) <= bf16_tol(r["shape"]), r
+
+
+def test_pair_kernel_agrees_with_one_cta_kernel(cuda_lib):
+    shapes = [(640, 384), (384, 640)]
+    a = run_muon(cuda_lib, shapes, seed=24)[0]
+    cuda_lib.dmuon_set_tuning(2, 0)
+    try:
+        b = run_muon(cuda_lib, shapes, seed=24)[0]
+    finally:
+        cuda_lib.dmuon_set_tuning(2, 1)
+    for x, y in zip(a, b):
+        assert abs(x["O"] - y["O"]) <= 5e-3, (x, y)
