@@ -38,6 +38,10 @@ void set_tc_mn_swap(int v);
 // Which tensor-core kernel runs the NS phases: 1 = CTA pairs on 256 x 256
 // tiles (default), 0 = one CTA per 128 x 256 tile.
 static int g_ns_pairs = 1;
+// Tile order inside one problem: 1 = longer tile dimension outer, 0 = rows outer.
+static int g_tile_order = 1;
+void set_tc2_variant(int stages, int prefetch);
+static int g_tc2_stages_sel = 4, g_tc2_prefetch_sel = 1;
 
 // ------------------------------------------------------------------ errors
 namespace {
@@ -360,6 +364,7 @@ int validate_matrix(const dmuon_matrix& M, int idx) {
 
 std::string plan_key(const dmuon_matrix* mats, int n, bool fp32) {
   std::string k = fp32 ? "f32|" : "bf16|";
+  k += "o" + std::to_string(g_tile_order) + "|";
   for (int i = 0; i < n; ++i) {
     k += std::to_string(mats[i].rank);
     for (int d = 0; d < mats[i].rank; ++d) k += ":" + std::to_string(mats[i].shape[d]);
@@ -399,8 +404,13 @@ int build_phase_tiles(const std::vector<NsProblem>& probs, int geometry, int slo
     const NsProblem& P = probs[p];
     const int tm = (P.M + bm - 1) / bm, tn = (P.N + bn - 1) / bn;
     const int64_t c = (P.K + kTcBK - 1) / kTcBK + 2;
-    for (int i = 0; i < tm; ++i)
-      for (int j = 0; j < tn; ++j) {
+    // Tiles of equal cost run in list order, so consecutive tiles run at the
+    // same time: walk the longer tile dimension in the outer loop, so a wave
+    // shares few panels of the larger operand (which then stay in L2).
+    const bool n_outer = g_tile_order && tn > tm;
+    for (int a = 0; a < (n_outer ? tn : tm); ++a)
+      for (int b = 0; b < (n_outer ? tm : tn); ++b) {
+        const int i = n_outer ? b : a, j = n_outer ? a : b;
         if (P.sym && (i * bm) / bn > j) continue;  // below the diagonal: mirrored
         tiles.push_back(make_uint2(static_cast<uint32_t>(p), (static_cast<uint32_t>(i) << 16) | static_cast<uint32_t>(j)));
         cost.push_back(c);
@@ -990,6 +1000,20 @@ int dmuon_set_tuning(int32_t key, int32_t value) {
   }
   if (key == 2) {
     g_ns_pairs = value ? 1 : 0;
+    return DMUON_OK;
+  }
+  if (key == 3) {
+    g_tc2_stages_sel = (value >= 4 && value <= 7) ? value : 4;
+    set_tc2_variant(g_tc2_stages_sel, g_tc2_prefetch_sel);
+    return DMUON_OK;
+  }
+  if (key == 4) {
+    g_tile_order = value ? 1 : 0;
+    return DMUON_OK;
+  }
+  if (key == 5) {
+    g_tc2_prefetch_sel = value ? 1 : 0;
+    set_tc2_variant(g_tc2_stages_sel, g_tc2_prefetch_sel);
     return DMUON_OK;
   }
   return set_error(DMUON_ERR_INVALID_ARG, "set_tuning: unknown key");

@@ -6,7 +6,7 @@
 //   * CTA r of the pair loads rows [128r, 128r+128) of the tile's A operand
 //     and columns [128r, 128r+128) of its B operand (K-contiguous: one
 //     64 x 128 TMA box; M/N-contiguous: two 64 x 64 boxes) into its own
-//     shared memory, and the completion of both CTAs' copies is counted on
+//     4-stage shared-memory ring, and the completion of both CTAs' copies is counted on
 //     the leader CTA's `full` barrier;
 //   * one thread of the leader (rank 0) issues tcgen05.mma.cta_group::2
 //     with M = 256, N = 256, K = 16: the tensor cores read A from both CTAs
@@ -37,15 +37,21 @@ namespace {
 
 constexpr int TILE = kTc2Tile;  // 256 x 256 per CTA pair
 constexpr int BK = 64;
-constexpr int STAGES = 6;
 constexpr uint32_t HALF_BYTES = 128 * BK * 2;         // 16 KiB: 128 rows x 64 k, bf16
 constexpr uint32_t STAGE_BYTES = 2 * HALF_BYTES;      // A half + B half per CTA
 constexpr uint32_t MN_BOX_BYTES = 64 * 64 * 2;        // 8 KiB
 constexpr int kThreads = 192;
 constexpr uint32_t kTmemCols = 512;
-constexpr int kNumBars = 2 * STAGES + 2 + 2 + 1;
-constexpr size_t kSmemBytes = 1024 + STAGES * STAGE_BYTES + kNumBars * 8 + 16;
-static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+template <int STAGES>
+constexpr size_t smem_bytes() {
+  return 1024 + STAGES * STAGE_BYTES + (2 * STAGES + 5) * 8 + 16;
+}
+static_assert(smem_bytes<7>() <= 227 * 1024, "shared memory budget");
+// Every CTA allocates all 512 TMEM columns, so two CTAs must never share an
+// SM: a second resident pair could hold one SM's TMEM while its partner waits
+// for the other's.  Asking for more than half of the SM's 228 KiB of shared
+// memory rules that out.
+static_assert(smem_bytes<4>() > 114 * 1024, "one CTA per SM");
 
 __device__ __forceinline__ uint64_t desc_k(uint32_t base, int kk) {
   return smem_desc_sw128(base + 32u * kk, 16u, 1024u);
@@ -54,7 +60,31 @@ __device__ __forceinline__ uint64_t desc_mn(uint32_t base, int kk) {
   return smem_desc_sw128(base + 2048u * kk, MN_BOX_BYTES, 1024u);
 }
 
+// What the producer and the MMA issuer need of one tile.  Loaded one tile
+// ahead, so the dependent global loads (tile list, then problem) overlap the
+// previous tile's main loop instead of stalling the pipeline between tiles.
+struct TileInfo {
+  int m0, n0;  // tile origin (rows, columns) of the pair
+  int map_a, map_b, z, majors, nk;
+};
+
+__device__ __forceinline__ TileInfo load_tile_info(const NsLaunch& L, int t) {
+  const uint2 tile = L.tiles[t];
+  const NsProblem& P = L.probs[tile.x];
+  TileInfo I;
+  I.m0 = static_cast<int>(tile.y >> 16) * TILE;
+  I.n0 = static_cast<int>(tile.y & 0xFFFFu) * TILE;
+  I.map_a = P.map_a;
+  I.map_b = P.map_b;
+  I.z = P.z;
+  I.majors = P.majors;
+  I.nk = (P.K + BK - 1) / BK;
+  return I;
+}
+
+template <int STAGES, bool PREFETCH>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) ns_tc2_kernel(const NsLaunch L) {
+  constexpr int kNumBars = 2 * STAGES + 2 + 2 + 1;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -107,19 +137,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) ns_tc2_
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
-      int fills[STAGES] = {0, 0, 0, 0, 0, 0};
+      int fills[STAGES] = {};
       bool ok = true;
+      TileInfo cur{}, nxt{};
+      if (t_begin < t_end) cur = load_tile_info(L, t_begin);
       for (int t = t_begin; t < t_end && ok; ++t) {
-        const uint2 tile = L.tiles[t];
-        const NsProblem& P = L.probs[tile.x];
-        const int m0 = static_cast<int>(tile.y >> 16) * TILE + 128 * static_cast<int>(rank);
-        const int n0 = static_cast<int>(tile.y & 0xFFFFu) * TILE + 128 * static_cast<int>(rank);
-        const CUtensorMap* ma = L.maps + P.map_a;
-        const CUtensorMap* mb = L.maps + P.map_b;
-        const bool a_mn = (P.majors & 1) != 0;
-        const bool b_mn = (P.majors & 2) != 0;
-        const int z = P.z;
-        const int nk = (P.K + BK - 1) / BK;
+        if (!PREFETCH) cur = load_tile_info(L, t);
+        if (PREFETCH && t + 1 < t_end) nxt = load_tile_info(L, t + 1);
+        const int m0 = cur.m0 + 128 * static_cast<int>(rank);
+        const int n0 = cur.n0 + 128 * static_cast<int>(rank);
+        const CUtensorMap* ma = L.maps + cur.map_a;
+        const CUtensorMap* mb = L.maps + cur.map_b;
+        const bool a_mn = (cur.majors & 1) != 0;
+        const bool b_mn = (cur.majors & 2) != 0;
+        const int z = cur.z;
+        const int nk = cur.nk;
+        if (PREFETCH) cur = nxt;
         for (int kb = 0; kb < nk; ++kb) {
           if (!mbar_wait_bounded_cluster(empty(stage), phase ^ 1u, abort_flag, L.err, kErrTimeoutProducer)) {
             ok = false;
@@ -168,13 +201,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) ns_tc2_
       uint32_t phase = 0;
       bool ok = true;
       int local = 0;
+      TileInfo cur{}, nxt{};
+      if (t_begin < t_end) cur = load_tile_info(L, t_begin);
       for (int t = t_begin; t < t_end && ok; ++t, ++local) {
-        const uint2 tile = L.tiles[t];
-        const NsProblem& P = L.probs[tile.x];
-        const bool a_mn = (P.majors & 1) != 0;
-        const bool b_mn = (P.majors & 2) != 0;
+        if (!PREFETCH) cur = load_tile_info(L, t);
+        if (PREFETCH && t + 1 < t_end) nxt = load_tile_info(L, t + 1);
+        const bool a_mn = (cur.majors & 1) != 0;
+        const bool b_mn = (cur.majors & 2) != 0;
         const uint32_t idesc = idesc_bf16_f32(TILE, TILE, a_mn, b_mn);
-        const int nk = (P.K + BK - 1) / BK;
+        const int nk = cur.nk;
+        if (PREFETCH) cur = nxt;
         const int acc = local & 1;
         const uint32_t acc_phase = static_cast<uint32_t>(local >> 1) & 1u;
         if (!mbar_wait_bounded_cluster(tempty(acc), acc_phase ^ 1u, abort_flag, L.err, kErrTimeoutMma)) {
@@ -247,34 +283,54 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) ns_tc2_
 
 }  // namespace
 
-cudaError_t launch_ns_tc2(const NsLaunch& L, int n_pairs, cudaStream_t st) {
-  if (n_pairs <= 0) return cudaSuccess;
+static int g_tc2_stages = 4;
+static int g_tc2_prefetch = 1;
+
+void set_tc2_variant(int stages, int prefetch) {
+  g_tc2_stages = (stages >= 4 && stages <= 7) ? stages : 6;
+  g_tc2_prefetch = prefetch ? 1 : 0;
+}
+
+template <int STAGES, bool PREFETCH>
+static cudaError_t launch_variant(const NsLaunch& L, int n_pairs, cudaStream_t st) {
   static bool attr_set = false;
+  constexpr size_t smem = smem_bytes<STAGES>();
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(ns_tc2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(kSmemBytes));
+    cudaError_t e = cudaFuncSetAttribute(ns_tc2_kernel<STAGES, PREFETCH>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  ns_tc2_kernel<<<2 * n_pairs, kThreads, kSmemBytes, st>>>(L);
+  ns_tc2_kernel<STAGES, PREFETCH><<<2 * n_pairs, kThreads, smem, st>>>(L);
   return cudaGetLastError();
+}
+
+cudaError_t launch_ns_tc2(const NsLaunch& L, int n_pairs, cudaStream_t st) {
+  if (n_pairs <= 0) return cudaSuccess;
+  switch (g_tc2_stages) {
+    case 4: return g_tc2_prefetch ? launch_variant<4, true>(L, n_pairs, st) : launch_variant<4, false>(L, n_pairs, st);
+    case 5: return g_tc2_prefetch ? launch_variant<5, true>(L, n_pairs, st) : launch_variant<5, false>(L, n_pairs, st);
+    case 7: return g_tc2_prefetch ? launch_variant<7, true>(L, n_pairs, st) : launch_variant<7, false>(L, n_pairs, st);
+    default: return g_tc2_prefetch ? launch_variant<6, true>(L, n_pairs, st) : launch_variant<6, false>(L, n_pairs, st);
+  }
 }
 
 // Largest number of CTA pairs of this kernel that can be resident at once.
 int ns_tc2_max_pairs() {
   static int cached = -1;
   if (cached >= 0) return cached;
-  if (cudaFuncSetAttribute(ns_tc2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(kSmemBytes)) != cudaSuccess) {
+  constexpr size_t smem = smem_bytes<7>();
+  if (cudaFuncSetAttribute(ns_tc2_kernel<7, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem)) != cudaSuccess) {
     cudaGetLastError();
     return cached = 0;
   }
   cudaLaunchConfig_t cfg = {};  // cluster shape comes from __cluster_dims__
   cfg.gridDim = dim3(2, 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.dynamicSmemBytes = smem;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, ns_tc2_kernel, &cfg) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&n, ns_tc2_kernel<7, true>, &cfg) != cudaSuccess) {
     cudaGetLastError();
     n = 0;
   }

@@ -44,29 +44,50 @@ __device__ __forceinline__ void ns_epilogue_tile(const NsLaunch& L, const NsProb
   const float* auxf_row = reinterpret_cast<const float*>(P.aux) + static_cast<int64_t>(row) * P.ld_aux;
   float* out2_row = P.out2 ? P.out2 + static_cast<int64_t>(row) * P.ld_out2 : nullptr;
   const bool aux_f32 = L.aux_f32 != 0;
+  // The aux operand of chunk cc+1 is loaded while chunk cc is processed, so
+  // the global-load latency overlaps the TMEM read and the stores.
+  const bool need_aux = beta != 0.f && row_ok;
+  auto load_aux = [&](int cc, uint4 (&q)[8]) {
+    const int c0 = n0 + cc * 32;
+    if (!need_aux || c0 + 32 > P.N) return;
+    if (aux_f32) {
+      const uint4* src = reinterpret_cast<const uint4*>(auxf_row + c0);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) q[i] = __ldg(src + i);
+    } else {
+      const uint4* src = reinterpret_cast<const uint4*>(aux_row + c0);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) q[i] = __ldg(src + i);
+    }
+  };
+  uint4 aux_next[8];
+  load_aux(0, aux_next);
 #pragma unroll 1
   for (int cc = 0; cc < BN / 32; ++cc) {
     const int col0 = n0 + cc * 32;
     if (col0 >= P.N) break;  // warp-uniform
+    uint4 aux_cur[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) aux_cur[i] = aux_next[i];
+    if (cc + 1 < BN / 32) load_aux(cc + 1, aux_next);
     __syncwarp();
     uint32_t r[32];
     tmem_ld_32x32b_x32(t_lane + static_cast<uint32_t>(cc * 32), r);
     const bool full_chunk = (col0 + 32 <= P.N);
     float auxf[32];
-    if (beta != 0.f && row_ok && full_chunk) {
+    if (need_aux && full_chunk) {
       if (aux_f32) {
-        const float4* src = reinterpret_cast<const float4*>(auxf_row + col0);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          const float4 q = __ldg(src + i);
-          auxf[4 * i] = q.x; auxf[4 * i + 1] = q.y; auxf[4 * i + 2] = q.z; auxf[4 * i + 3] = q.w;
+          auxf[4 * i] = __uint_as_float(aux_cur[i].x);
+          auxf[4 * i + 1] = __uint_as_float(aux_cur[i].y);
+          auxf[4 * i + 2] = __uint_as_float(aux_cur[i].z);
+          auxf[4 * i + 3] = __uint_as_float(aux_cur[i].w);
         }
       } else {
-        const uint4* src = reinterpret_cast<const uint4*>(aux_row + col0);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          const uint4 q = __ldg(src + i);
-          const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+          const uint32_t w[4] = {aux_cur[i].x, aux_cur[i].y, aux_cur[i].z, aux_cur[i].w};
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             auxf[8 * i + 2 * j] = __uint_as_float(w[j] << 16);
