@@ -318,9 +318,17 @@ def run_ours(args, wl, rank, world, local_rank):
     # X X^T and A A), not the dense count, so the fraction is not inflated.
     ns_exec = W.workload_ns_flops_executed(wl) if not h["fp32_ns"] else ns_flops
     ns_exec_tflops = ns_exec / (ns_ms / 1e3) / 1e12 if ns_ms > 0 else None
-    ew_bytes = W.muon_elementwise_bytes(wl) + W.adamw_bytes(wl)
-    ew_ms = sum(prof[k][0] for k in ("momentum", "norm", "update", "adamw")) / args.steps
+    # Streaming kernels: bytes of the passes that actually ran as their own
+    # launches (the update runs inside the last NS product on the bf16 path).
+    ew_parts = {"momentum": W.momentum_bytes(wl), "adamw": W.adamw_bytes(wl)}
+    if prof["update"][1] > 0:
+        ew_parts["update"] = W.update_bytes(wl)
+    ew_bytes = sum(ew_parts.values())
+    ew_ms = sum(prof[k][0] for k in list(ew_parts) + ["norm"]) / args.steps
     ew_gbs = ew_bytes / (ew_ms / 1e3) / 1e9 if ew_ms > 0 else None
+    ew_detail = {k: {"ms": prof[k][0] / args.steps,
+                     "GB/s": (v / (prof[k][0] / args.steps / 1e3) / 1e9) if prof[k][0] > 0 else None}
+                 for k, v in ew_parts.items()}
     peak = peaks["bf16_sustained"]
     traffic = None
     tpath = os.path.join(ROOT, "profiles", "ns_tc_traffic.json")
@@ -355,7 +363,7 @@ def run_ours(args, wl, rank, world, local_rank):
                      "traffic": traffic, "launches_per_step": ns_launches / args.steps},
         "elementwise": {"bound": "hbm", "achieved": ew_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                         "frac": (ew_gbs / peaks["hbm_gbs"]) if ew_gbs else None,
-                        "bytes_per_step": ew_bytes},
+                        "bytes_per_step": ew_bytes, "kernels": ew_detail},
         "kernel_ms_per_step": {k: v[0] / args.steps for k, v in prof.items()},
         "gpu_launches": launches,
         "e2e": {"value": world * ns_flops / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s",

@@ -834,6 +834,13 @@ int dmuon_muon_step(dmuon_context* ctx, const dmuon_matrix* mats, int32_t n, flo
       L.b = b;
       L.c = c;
       L.err = static_cast<int*>(ctx->err.p);
+      if (!fp32 && kind == kCombine && it == ns_steps - 1) {
+        // The last Combine applies the update itself (no X store, no update pass).
+        L.fuse_update = 1;
+        L.slices = d_slices;
+        L.lr = lr;
+        L.wd = wd;
+      }
       const bool pairs = !fp32 && g_ns_pairs;
       const PhaseTiles& T = pairs ? P.phase2[kind] : P.phase[kind];
       L.tiles = static_cast<const uint2*>(T.tiles.p);
@@ -845,6 +852,7 @@ int dmuon_muon_step(dmuon_context* ctx, const dmuon_matrix* mats, int32_t n, flo
       if (st != DMUON_OK) return st;
     }
   }
+  if (!fp32 && ns_steps > 0) return DMUON_OK;  // fused into the last Combine
   return timed_launch(ctx, DMUON_KERNEL_UPDATE, s, [&] {
     return launch_update(d_slices, d_chunks, n_chunks, lr, wd, fp32 ? 1 : 0,
                          ns_steps == 0 ? inv_norm : nullptr, s);

@@ -112,6 +112,13 @@ struct NsLaunch {
   int32_t aux_f32;          // aux is fp32 (tcgen05 path; the fp32 path is always fp32)
   float a, b, c;
   int* err;
+  // Last Combine of the step on the tensor-core path: instead of storing X,
+  // apply W <- W*(1 - lr*wd) - lr*shape_scale*X and the bf16 copy in the
+  // epilogue (slices[P.slice] gives W, the parameter and the scale; X has the
+  // orientation of W, so output (row, col) is W[row][col]).
+  const SliceDesc* slices;
+  int32_t fuse_update;
+  float lr, wd;
 };
 
 // ---- launch wrappers (each returns the cudaError_t of its launch) ----

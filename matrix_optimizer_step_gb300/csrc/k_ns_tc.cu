@@ -90,6 +90,7 @@ __device__ __forceinline__ uint64_t desc_mnmajor(uint32_t base, int kk, int swap
               : smem_desc_sw128(base + 2048u * kk, MN_BOX_BYTES, 1024u);
 }
 
+template <bool FUSE>
 __global__ void __launch_bounds__(kThreads, 1) ns_tc_kernel(const NsLaunch L, int mn_swap) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -262,7 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_kernel(const NsLaunch L, in
 
       const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                               static_cast<uint32_t>(acc * BN);
-      ns_epilogue_tile(L, P, m0, n0, row_in_tile, t_lane, P.sym && ((m0 >> 8) < (n0 >> 8)));
+      ns_epilogue_tile<FUSE>(L, P, m0, n0, row_in_tile, t_lane, !FUSE && P.sym && ((m0 >> 8) < (n0 >> 8)));
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bars.te(acc));
@@ -284,17 +285,22 @@ static int g_mn_swap = 0;
 
 void set_tc_mn_swap(int v) { g_mn_swap = v; }
 
-cudaError_t launch_ns_tc(const NsLaunch& L, int n_ctas, cudaStream_t st) {
-  if (n_ctas <= 0) return cudaSuccess;
+template <bool FUSE>
+static cudaError_t launch_tc_variant(const NsLaunch& L, int n_ctas, cudaStream_t st) {
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(ns_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(ns_tc_kernel<FUSE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kSmemBytes));
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  ns_tc_kernel<<<n_ctas, kThreads, kSmemBytes, st>>>(L, g_mn_swap);
+  ns_tc_kernel<FUSE><<<n_ctas, kThreads, kSmemBytes, st>>>(L, g_mn_swap);
   return cudaGetLastError();
+}
+
+cudaError_t launch_ns_tc(const NsLaunch& L, int n_ctas, cudaStream_t st) {
+  if (n_ctas <= 0) return cudaSuccess;
+  return L.fuse_update ? launch_tc_variant<true>(L, n_ctas, st) : launch_tc_variant<false>(L, n_ctas, st);
 }
 
 }  // namespace dmuon

@@ -82,7 +82,7 @@ __device__ __forceinline__ TileInfo load_tile_info(const NsLaunch& L, int t) {
   return I;
 }
 
-template <int STAGES, bool PREFETCH>
+template <int STAGES, bool PREFETCH, bool FUSE>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) ns_tc2_kernel(const NsLaunch L) {
   constexpr int kNumBars = 2 * STAGES + 2 + 2 + 1;
   extern __shared__ uint8_t smem_raw[];
@@ -260,7 +260,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) ns_tc2_
       tc_fence_after();
       const uint32_t t_lane =
           tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * TILE);
-      ns_epilogue_tile(L, P, tm * TILE, tn * TILE, row_in_tile, t_lane, P.sym && tm < tn);
+      ns_epilogue_tile<FUSE>(L, P, tm * TILE, tn * TILE, row_in_tile, t_lane, !FUSE && P.sym && tm < tn);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
@@ -291,18 +291,24 @@ void set_tc2_variant(int stages, int prefetch) {
   g_tc2_prefetch = prefetch ? 1 : 0;
 }
 
-template <int STAGES, bool PREFETCH>
-static cudaError_t launch_variant(const NsLaunch& L, int n_pairs, cudaStream_t st) {
+template <int STAGES, bool PREFETCH, bool FUSE>
+static cudaError_t launch_variant3(const NsLaunch& L, int n_pairs, cudaStream_t st) {
   static bool attr_set = false;
   constexpr size_t smem = smem_bytes<STAGES>();
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(ns_tc2_kernel<STAGES, PREFETCH>,
+    cudaError_t e = cudaFuncSetAttribute(ns_tc2_kernel<STAGES, PREFETCH, FUSE>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  ns_tc2_kernel<STAGES, PREFETCH><<<2 * n_pairs, kThreads, smem, st>>>(L);
+  ns_tc2_kernel<STAGES, PREFETCH, FUSE><<<2 * n_pairs, kThreads, smem, st>>>(L);
   return cudaGetLastError();
+}
+
+template <int STAGES, bool PREFETCH>
+static cudaError_t launch_variant(const NsLaunch& L, int n_pairs, cudaStream_t st) {
+  return L.fuse_update ? launch_variant3<STAGES, PREFETCH, true>(L, n_pairs, st)
+                       : launch_variant3<STAGES, PREFETCH, false>(L, n_pairs, st);
 }
 
 cudaError_t launch_ns_tc2(const NsLaunch& L, int n_pairs, cudaStream_t st) {
@@ -320,7 +326,7 @@ int ns_tc2_max_pairs() {
   static int cached = -1;
   if (cached >= 0) return cached;
   constexpr size_t smem = smem_bytes<7>();
-  if (cudaFuncSetAttribute(ns_tc2_kernel<7, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(ns_tc2_kernel<7, true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem)) != cudaSuccess) {
     cudaGetLastError();
     return cached = 0;
@@ -330,7 +336,7 @@ int ns_tc2_max_pairs() {
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, ns_tc2_kernel<7, true>, &cfg) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&n, ns_tc2_kernel<7, true, false>, &cfg) != cudaSuccess) {
     cudaGetLastError();
     n = 0;
   }

@@ -2,7 +2,8 @@
 // the CTA-pair tcgen05 kernels.  One epilogue warp drains its 32 TMEM lanes
 // (rows) of the accumulator, 32 columns at a time, applies the phase's
 // epilogue (see NsKind) and stores bf16 (plus the optional fp32 copy, plus the
-// transposed copy of a symmetric off-diagonal block).
+// transposed copy of a symmetric off-diagonal block) -- or, in the last
+// Combine of a step, applies the parameter update to W in place of storing X.
 #pragma once
 
 #include <stdint.h>
@@ -16,6 +17,7 @@ namespace dmuon {
 // address of this warp's lane quarter at column 0 of the accumulator.
 // Tiles are 256 columns wide; `mirror` tiles are strictly above the
 // diagonal of a symmetric output.
+template <bool FUSE>
 __device__ __forceinline__ void ns_epilogue_tile(const NsLaunch& L, const NsProblem& P, int m0, int n0,
                                                  int row_in_tile, uint32_t tmem_lane_base, bool mirror) {
   constexpr int BN = 256;
@@ -44,6 +46,20 @@ __device__ __forceinline__ void ns_epilogue_tile(const NsLaunch& L, const NsProb
   const float* auxf_row = reinterpret_cast<const float*>(P.aux) + static_cast<int64_t>(row) * P.ld_aux;
   float* out2_row = P.out2 ? P.out2 + static_cast<int64_t>(row) * P.ld_out2 : nullptr;
   const bool aux_f32 = L.aux_f32 != 0;
+  // Fused update (last iteration): W <- W*decay - step*X, param <- bf16(W).
+  constexpr bool fuse = FUSE;
+  float* w_row = nullptr;
+  uint16_t* p_row = nullptr;
+  float decay = 1.f, step = 0.f;
+  bool w_vec = false;
+  if (fuse) {
+    const SliceDesc& S = L.slices[P.slice];
+    w_row = S.master + static_cast<int64_t>(row) * S.n;
+    p_row = S.param ? S.param + static_cast<int64_t>(row) * S.n : nullptr;
+    decay = 1.0f - L.lr * L.wd;
+    step = L.lr * S.shape_scale;
+    w_vec = S.vec_ok != 0;
+  }
   // The aux operand of chunk cc+1 is loaded while chunk cc is processed, so
   // the global-load latency overlaps the TMEM read and the stores.
   const bool need_aux = beta != 0.f && row_ok;
@@ -96,9 +112,50 @@ __device__ __forceinline__ void ns_epilogue_tile(const NsLaunch& L, const NsProb
         }
       }
     }
+    float4 wq[8];
+    if (fuse && row_ok && full_chunk && w_vec) {
+      const float4* src = reinterpret_cast<const float4*>(w_row + col0);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) wq[i] = src[i];
+    }
     tmem_ld_wait();
     if (!row_ok) {
       // rows past M: nothing to store
+    } else if (full_chunk && fuse) {
+      float w[32];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        if (w_vec) {
+          w[4 * i] = wq[i].x; w[4 * i + 1] = wq[i].y; w[4 * i + 2] = wq[i].z; w[4 * i + 3] = wq[i].w;
+        } else {
+#pragma unroll
+          for (int k = 0; k < 4; ++k) w[4 * i + k] = w_row[col0 + 4 * i + k];
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        float v = alpha * __uint_as_float(r[j]);
+        if (beta != 0.f) v = fmaf(beta, auxf[j], v);
+        w[j] = fmaf(-step, v, w[j] * decay);
+      }
+      if (w_vec) {
+        float4* wd4 = reinterpret_cast<float4*>(w_row + col0);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) wd4[i] = make_float4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+        if (p_row) {
+          uint4* pd = reinterpret_cast<uint4*>(p_row + col0);
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            pd[i] = make_uint4(pack_bf16x2(w[8 * i], w[8 * i + 1]), pack_bf16x2(w[8 * i + 2], w[8 * i + 3]),
+                               pack_bf16x2(w[8 * i + 4], w[8 * i + 5]), pack_bf16x2(w[8 * i + 6], w[8 * i + 7]));
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          w_row[col0 + j] = w[j];
+          if (p_row) p_row[col0 + j] = to_bf16_bits(w[j]);
+        }
+      }
     } else if (full_chunk) {
       float v[32];
 #pragma unroll
@@ -134,6 +191,12 @@ __device__ __forceinline__ void ns_epilogue_tile(const NsLaunch& L, const NsProb
         float v = alpha * __uint_as_float(r[j]);
         if (beta != 0.f)
           v = fmaf(beta, aux_f32 ? auxf_row[col0 + j] : bf16_bits_to_f32(aux_row[col0 + j]), v);
+        if (fuse) {
+          const float w = fmaf(-step, v, w_row[col0 + j] * decay);
+          w_row[col0 + j] = w;
+          if (p_row) p_row[col0 + j] = to_bf16_bits(w);
+          continue;
+        }
         const uint16_t vb = to_bf16_bits(v);
         out_row[col0 + j] = vb;
         if (out2_row) out2_row[col0 + j] = v;

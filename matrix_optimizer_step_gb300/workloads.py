@@ -266,18 +266,26 @@ def workload_ns_flops(wl):
     return sum(ns_flops(*s.mn, wl.hyper["ns_steps"]) * s.n_slices for s in wl.matrices)
 
 
-def muon_elementwise_bytes(wl):
-    """Minimal HBM bytes of the two streaming passes of the Muon step.
+def momentum_bytes(wl):
+    """HBM bytes of the momentum pass: grad read, momentum read+write, X0
+    write (bf16 operand plus its fp32 copy on the bf16 path; fp32 only in
+    the fp32 mode)."""
+    xb = 4 if wl.hyper["fp32_ns"] else 2 + 4
+    return sum(s.numel * ((2 if s.grad_dtype == torch.bfloat16 else 4) + 8 + xb) for s in wl.matrices)
 
-    Momentum pass: grad read, momentum read+write, bf16 X0 write.
-    Update pass: X read (bf16), master read+write, bf16 param write.
-    """
-    total = 0
-    for s in wl.matrices:
-        gb = 2 if s.grad_dtype == torch.bfloat16 else 4
-        xb = 4 if wl.hyper["fp32_ns"] else 2
-        total += s.numel * (gb + 8 + xb) + s.numel * (xb + 8 + 2)
-    return total
+
+def update_bytes(wl):
+    """HBM bytes of a separate update pass: X read, master read+write, bf16
+    param write (on the bf16 path the update is fused into the last NS
+    product instead)."""
+    xb = 4 if wl.hyper["fp32_ns"] else 2
+    return wl.muon_numel * (xb + 8 + 2)
+
+
+def muon_elementwise_bytes(wl):
+    """Minimal HBM bytes of the streaming work of the Muon step (momentum
+    pass plus the update, wherever it runs)."""
+    return momentum_bytes(wl) + update_bytes(wl)
 
 
 def adamw_bytes(wl):
