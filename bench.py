@@ -245,13 +245,21 @@ def run_ours(args, wl, rank, world, local_rank):
     stream = torch.cuda.current_stream()
     t_counter = [0]
 
+    muon_kw = dict(lr=h["lr"], momentum=h["momentum"], wd=h["wd"], ns_steps=h["ns_steps"], a=h["a"],
+                   b=h["b"], c=h["c"], nesterov=h["nesterov"], fp32_ns=h["fp32_ns"])
+
     def one_step():
-        step.muon_step(h["lr"], h["momentum"], h["wd"], h["ns_steps"], h["a"], h["b"], h["c"],
-                       nesterov=h["nesterov"], fp32_ns=h["fp32_ns"], stream=stream)
+        adam_kw = None
         if wl.vectors:
             t_counter[0] += 1
-            step.adamw_step(h["adam_lr"], h["beta1"], h["beta2"], h["adam_eps"], h["adam_wd"],
-                            t_counter[0], stream=stream)
+            adam_kw = dict(lr=h["adam_lr"], beta1=h["beta1"], beta2=h["beta2"], eps=h["adam_eps"],
+                           wd=h["adam_wd"], step=t_counter[0])
+        if args.overlap_adamw:
+            step.step(muon_kw, adam_kw, stream=stream)
+        else:
+            step.muon_step(stream=stream, **muon_kw)
+            if adam_kw is not None:
+                step.adamw_step(stream=stream, **adam_kw)
 
     def barrier():
         if dist is not None:
@@ -389,6 +397,8 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default="llama3_8b")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--overlap-adamw", action="store_true",
+                    help="run the AdamW step on a side stream beside the Muon step (OwnerStep.step)")
     ap.add_argument("--tuning", action="append", default=[],
                     help="KEY=VALUE passed to dmuon_set_tuning before the run")
     args = ap.parse_args()

@@ -168,8 +168,9 @@ DMUON_API int dmuon_context_destroy(dmuon_context* ctx);
  * DMUON_ERR_NOMEM (workspace), DMUON_ERR_CUDA, DMUON_ERR_UNSUPPORTED.
  * Device-side waits inside the kernels are bounded; if one runs out the
  * kernel records it and returns, and the next dmuon_sync() reports
- * DMUON_ERR_TIMEOUT.  Calls on one context must not run concurrently on
- * different streams (they share the context's workspace).
+ * DMUON_ERR_TIMEOUT.  Muon steps on one context must not overlap on the
+ * GPU (they share the context's workspace); an AdamW step of the same
+ * context may run concurrently on another stream.
  */
 DMUON_API int dmuon_muon_step(dmuon_context* ctx, const dmuon_matrix* mats, int32_t n,
                     float lr, float momentum, float wd, int32_t ns_steps,

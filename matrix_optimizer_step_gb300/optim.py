@@ -87,6 +87,29 @@ class OwnerStep:
             self.ctx, self._vecs, self._n_vecs, float(lr), float(beta1), float(beta2), float(eps),
             float(wd), int(step), capi._stream_handle(stream)))
 
+    # ------------------------------------------------------ both routes
+    def step(self, muon, adamw, stream=None):
+        """One optimizer step of every registered tensor: the Muon step on
+        ``stream`` and, concurrently, the AdamW step on a side stream (the two
+        share no workspace; AdamW is HBM-bound while the Newton-Schulz
+        products are tensor-bound).  ``muon`` / ``adamw`` are keyword dicts for
+        muon_step / adamw_step (adamw may be None).  On return ``stream`` is
+        ordered after both."""
+        main = stream if stream is not None else torch.cuda.current_stream(self.device)
+        if adamw is None or self._vecs is None:
+            self.muon_step(stream=main, **muon)
+            return
+        if getattr(self, "_side", None) is None:
+            self._side = torch.cuda.Stream(device=self.device)
+            self._ev_fork = torch.cuda.Event()
+            self._ev_join = torch.cuda.Event()
+        self._ev_fork.record(main)
+        self._side.wait_event(self._ev_fork)
+        self.adamw_step(stream=self._side, **adamw)
+        self.muon_step(stream=main, **muon)
+        self._ev_join.record(self._side)
+        main.wait_event(self._ev_join)
+
     # ------------------------------------------------------------ misc
     def sync(self, stream=None):
         capi.dmuon_sync(self.ctx, stream)
