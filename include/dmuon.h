@@ -93,6 +93,27 @@ DMUON_API int dmuon_lpt_assign(const int64_t* sizes, int32_t n_items, int32_t n_
                      int32_t* out_slot, int64_t* out_load);
 
 /*
+ * dmuon_lpt_assign_layered -- LPT with the two constraints of "架构设计" §3.1
+ * ("算法内置的关键约束"): (1) same-layer concurrency: the items of one layer
+ * go to different slots, so each owner's broadcast of that layer can run at
+ * the same time; (2) small-parameter merging: within a layer, the items
+ * below `small_threshold` elements (the page's SMALL_PARAM_THRESHOLD, 5e6 by
+ * default) form one unit with one owner.  Units are placed in descending
+ * size (ties: lowest first item), each on the least-loaded slot that does
+ * not yet hold its layer (ties: lowest index), or on the least-loaded slot
+ * overall once every slot holds it.  layers[i] < 0: item i belongs to no
+ * layer (never merged, never constrained); with all layers < 0 the result
+ * equals dmuon_lpt_assign.
+ *
+ *   sizes, layers  host, n_items each (read only)
+ *   out_slot       host, n_items (written); out_load host, n_slots or NULL
+ * Pure host code.  Errors: DMUON_ERR_INVALID_ARG as dmuon_lpt_assign.
+ */
+DMUON_API int dmuon_lpt_assign_layered(const int64_t* sizes, const int32_t* layers, int32_t n_items,
+                                       int32_t n_slots, int64_t small_threshold, int32_t* out_slot,
+                                       int64_t* out_load);
+
+/*
  * One Muon-route tensor.  shape[0..rank-1] is row-major and contiguous; the
  * Newton-Schulz iteration acts on the last two dimensions (m rows, n cols)
  * and every leading index is a separate matrix.  All pointers are device

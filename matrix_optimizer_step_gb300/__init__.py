@@ -23,6 +23,7 @@ from .capi import (  # noqa: F401
     dmuon_context_destroy,
     dmuon_kernel_launches,
     dmuon_lpt_assign,
+    dmuon_lpt_assign_layered,
     dmuon_muon_step,
     dmuon_muon_step_noalloc,
     dmuon_profile,

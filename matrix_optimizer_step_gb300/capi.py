@@ -37,7 +37,7 @@ EXPORTED = (
     "dmuon_status_string", "dmuon_last_error", "dmuon_lpt_assign", "dmuon_context_create",
     "dmuon_context_destroy", "dmuon_muon_step", "dmuon_adamw_step", "dmuon_sync",
     "dmuon_selftest_wait_timeout", "dmuon_set_tuning", "dmuon_kernel_launches", "dmuon_profile",
-    "dmuon_profile_read", "dmuon_muon_step_noalloc",
+    "dmuon_profile_read", "dmuon_muon_step_noalloc", "dmuon_lpt_assign_layered",
 )
 
 KERNEL_KINDS = ("momentum", "norm", "ns_gram", "ns_poly", "ns_combine", "update", "adamw")
@@ -92,6 +92,8 @@ def load_library(path=LIB_PATH):
         "dmuon_last_error": (ctypes.c_char_p, []),
         "dmuon_lpt_assign": (ctypes.c_int, [ctypes.POINTER(i64), i32, i32, ctypes.POINTER(i32),
                                             ctypes.POINTER(i64)]),
+        "dmuon_lpt_assign_layered": (ctypes.c_int, [ctypes.POINTER(i64), ctypes.POINTER(i32), i32, i32, i64,
+                                                    ctypes.POINTER(i32), ctypes.POINTER(i64)]),
         "dmuon_context_create": (ctypes.c_int, [ctypes.POINTER(vp), i32]),
         "dmuon_context_destroy": (ctypes.c_int, [vp]),
         "dmuon_muon_step": (ctypes.c_int, [vp, ctypes.POINTER(DmuonMatrix), i32, f32, f32, f32, i32,
@@ -155,6 +157,21 @@ def dmuon_lpt_assign(sizes, n_slots):
     out = (ctypes.c_int32 * max(n, 1))()
     loads = (ctypes.c_int64 * max(int(n_slots), 1))()
     _check(lib.dmuon_lpt_assign(arr, n, int(n_slots), out, loads))
+    return [out[i] for i in range(n)], [loads[i] for i in range(int(n_slots))]
+
+
+def dmuon_lpt_assign_layered(sizes, layers, n_slots, small_threshold=5_000_000):
+    """Layer-aware LPT (same-layer distinct slots, small items of a layer
+    merged): (slots, loads)."""
+    lib = load_library()
+    n = len(sizes)
+    if len(layers) != n:
+        raise ValueError("one layer id per item")
+    arr = (ctypes.c_int64 * max(n, 1))(*[int(s) for s in sizes])
+    lay = (ctypes.c_int32 * max(n, 1))(*[int(x) for x in layers])
+    out = (ctypes.c_int32 * max(n, 1))()
+    loads = (ctypes.c_int64 * max(int(n_slots), 1))()
+    _check(lib.dmuon_lpt_assign_layered(arr, lay, n, int(n_slots), int(small_threshold), out, loads))
     return [out[i] for i in range(n)], [loads[i] for i in range(int(n_slots))]
 
 

@@ -135,9 +135,14 @@ class OwnerStep:
             pass
 
 
-def owner_partition(numels, n_owners):
+def owner_partition(numels, n_owners, layers=None, small_threshold=5_000_000):
     """Owner rank of each Muon tensor: one global LPT pass over all tensors
-    ("架构设计" §3.1), element count as the cost.  Deterministic, so every
-    rank computes the same map on its own and each tensor has exactly one
-    owner.  Returns (owner per tensor, elements per owner)."""
-    return capi.dmuon_lpt_assign([int(n) for n in numels], int(n_owners))
+    ("架构设计" §3.1), element count as the cost; with ``layers`` (a layer id
+    per tensor) the layer-aware pass (same-layer tensors on distinct owners,
+    a layer's tensors below ``small_threshold`` merged).  Deterministic, so
+    every rank computes the same map on its own and each tensor has exactly
+    one owner.  Returns (owner per tensor, elements per owner)."""
+    numels = [int(n) for n in numels]
+    if layers is None:
+        return capi.dmuon_lpt_assign(numels, int(n_owners))
+    return capi.dmuon_lpt_assign_layered(numels, layers, int(n_owners), small_threshold)

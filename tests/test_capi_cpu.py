@@ -157,3 +157,31 @@ def test_golden_last_two_dims_accepted_ranks(mos):
                 assert status == capi.DMUON_ERR_RANK_LT2, case
     finally:
         mos.dmuon_context_destroy(ctx)
+
+
+
+def test_layered_lpt_bit_exact_vs_oracle(mos):
+    r = np.random.default_rng(2)
+    for trial in range(150):
+        n = int(r.integers(0, 200))
+        R = int(r.integers(1, 40))
+        n_layers = int(r.integers(1, 30))
+        sizes = [int(x) for x in (10 ** r.uniform(3, 8, n)).astype(np.int64)]
+        layers = [int(x) for x in r.integers(-1, n_layers, n)]
+        thr = int(r.choice([0, 5_000_000, 10 ** 7]))
+        got = mos.dmuon_lpt_assign_layered(sizes, layers, R, thr)
+        want = olpt.lpt_assign_layered(sizes, layers, R, thr)
+        assert got[0] == want[0] and got[1] == want[1], trial
+
+
+def test_layered_lpt_llama_owner_partition(mos):
+    from matrix_optimizer_step_gb300 import workloads
+
+    wl = workloads.workload("llama3_8b")
+    numels = [s.numel for s in wl.matrices]
+    layers = [int(s.name.split(".")[1]) for s in wl.matrices]
+    got = mos.owner_partition(numels, 8, layers=layers)
+    want = olpt.lpt_assign_layered(numels, layers, 8)
+    assert list(got[0]) == want[0] and list(got[1]) == want[1]
+    with pytest.raises(mos.DmuonError):
+        mos.dmuon_lpt_assign_layered([1, -2], [0, 0], 2)

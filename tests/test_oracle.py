@@ -340,3 +340,69 @@ def test_lpt_rejects_bad_input():
     with pytest.raises(ValueError):
         olpt.lpt_assign([1, -2], 2)
     assert olpt.lpt_assign([], 3) == ([], [0, 0, 0])
+
+
+
+# ------------------------------------------------------- layer-aware LPT
+
+def test_layered_lpt_reduces_to_plain_lpt_without_layers():
+    r = _rng(16)
+    for _ in range(40):
+        n = int(r.integers(0, 60))
+        R = int(r.integers(1, 12))
+        sizes = [int(x) for x in r.integers(0, 10 ** 7, n)]
+        assert olpt.lpt_assign_layered(sizes, [-1] * n, R) == olpt.lpt_assign(sizes, R)
+        assert olpt.lpt_assign_layered(sizes, list(range(n)), R, small_threshold=0) == \
+            olpt.lpt_assign(sizes, R)
+
+
+def test_layered_lpt_constraints_hold():
+    r = _rng(17)
+    for _ in range(60):
+        n_layers = int(r.integers(1, 6))
+        per = int(r.integers(1, 9))
+        R = int(r.integers(1, 10))
+        sizes, layers = [], []
+        for l in range(n_layers):
+            for _ in range(per):
+                sizes.append(int(10 ** r.uniform(5, 8)))
+                layers.append(l)
+        slots, loads = olpt.lpt_assign_layered(sizes, layers, R)
+        assert sum(loads) == sum(sizes)
+        for l in range(n_layers):
+            small = {slots[i] for i in range(len(sizes)) if layers[i] == l and sizes[i] < 5_000_000}
+            assert len(small) <= 1  # merged unit: one owner
+            units = [i for i in range(len(sizes)) if layers[i] == l and sizes[i] >= 5_000_000]
+            n_units = len(units) + (1 if small else 0)
+            used = [slots[i] for i in units] + list(small)
+            if n_units <= R:
+                assert len(set(used)) == n_units  # distinct owners within a layer
+
+
+def test_layered_lpt_pages_example_uses_every_slot():
+    # "架构设计" §3.1: R = 8, 7 projection matrices per layer.  A per-layer
+    # assignment leaves one slot idle (golden fixture); the global layered
+    # pass keeps each layer's matrices on distinct slots and still balances
+    # all 8 slots.
+    with open(os.path.join(GOLDEN, "lpt_per_layer_idle.json")) as f:
+        gold = json.load(f)
+    R, k = gold["n_slots"], gold["items_per_layer"]
+    sizes = [16_777_216] * (k * 32)
+    layers = [i // k for i in range(k * 32)]
+    slots, loads = olpt.lpt_assign_layered(sizes, layers, R)
+    assert min(loads) == max(loads)
+    for l in range(32):
+        assert len({slots[i] for i in range(len(sizes)) if layers[i] == l}) == k
+
+
+def test_layered_lpt_llama_small_kv_merged():
+    # Llama-3-8B: k and v (1024 x 4096 = 4.19e6 < 5e6) merge into one unit.
+    shapes = [(4096, 4096), (1024, 4096), (1024, 4096), (4096, 4096), (14336, 4096), (14336, 4096),
+              (4096, 14336)]
+    sizes = [m * n for _ in range(32) for m, n in shapes]
+    layers = [l for l in range(32) for _ in shapes]
+    slots, loads = olpt.lpt_assign_layered(sizes, layers, 8)
+    for l in range(32):
+        ks, vs = slots[7 * l + 1], slots[7 * l + 2]
+        assert ks == vs
+        assert len({slots[7 * l + j] for j in (0, 1, 3, 4, 5, 6)}) == 6
