@@ -40,6 +40,9 @@ void set_tc_mn_swap(int v);
 static int g_ns_pairs = 1;
 // Tile order inside one problem: 1 = longer tile dimension outer, 0 = rows outer.
 static int g_tile_order = 1;
+// CTA-pair kernel: 1 = symmetric outputs stored as upper blocks only and read
+// through transposed loads, 0 = mirrored stores.
+static int g_tri = 1;
 void set_tc2_variant(int stages, int prefetch);
 static int g_tc2_stages_sel = 4, g_tc2_prefetch_sel = 1;
 
@@ -176,7 +179,7 @@ struct ShapeClass {
   int64_t ld, ldp;      // workspace row pitch (elements) for X and for A/B
   size_t off_x[2], off_a, off_b;  // byte offsets in the workspace
   size_t off_xf, off_af;          // fp32 side copies of X and A (bf16 path only)
-  int32_t map_xk[2], map_xmn[2], map_a, map_b;
+  int32_t map_xk[2], map_xmn[2], map_a, map_b, map_a_mn, map_b_mn;
 };
 
 struct PhaseTiles {
@@ -553,6 +556,17 @@ int build_muon_plan(dmuon_context* ctx, const dmuon_matrix* mats, int n, bool fp
       maps.push_back(ma);
       C.map_b = static_cast<int32_t>(maps.size());
       maps.push_back(mb);
+      // M/N-contiguous views of A and B (64 x 64 boxes): the transposed reads
+      // of the CTA-pair kernel's upper-block-only symmetric operands.
+      CUtensorMap mat, mbt;
+      st = make_map(enc, &mat, ws + C.off_a, p, p, C.count, C.ldp, 64, 64);
+      if (st != DMUON_OK) return st;
+      st = make_map(enc, &mbt, ws + C.off_b, p, p, C.count, C.ldp, 64, 64);
+      if (st != DMUON_OK) return st;
+      C.map_a_mn = static_cast<int32_t>(maps.size());
+      maps.push_back(mat);
+      C.map_b_mn = static_cast<int32_t>(maps.size());
+      maps.push_back(mbt);
     }
     st = upload(P.maps, maps);
     if (st != DMUON_OK) return st;
@@ -603,6 +617,8 @@ int build_muon_plan(dmuon_context* ctx, const dmuon_matrix* mats, int n, bool fp
       y.a_si = C.ldp; y.a_sk = 1; y.b_sk = C.ldp; y.b_sj = 1;
       y.map_a = y.map_b = C.map_a;
       y.majors = 0;
+      y.tri = 3;
+      y.map_a_t = y.map_b_t = C.map_a_mn;
       y.out = B;
       y.ld_out = C.ldp;
       y.aux = A;
@@ -620,6 +636,8 @@ int build_muon_plan(dmuon_context* ctx, const dmuon_matrix* mats, int n, bool fp
         c.map_a = C.map_b;
         c.map_b = C.map_xmn[par];
         c.majors = 2;
+        c.tri = 1;
+        c.map_a_t = C.map_b_mn;
       } else {        // M = q, N = p, K = p: A_op = X, B_op(k,j) = B[k,j] = B[j,k]
         c.M = q; c.N = p; c.K = p;
         c.a = X; c.a_si = C.ld; c.a_sk = 1;
@@ -627,6 +645,8 @@ int build_muon_plan(dmuon_context* ctx, const dmuon_matrix* mats, int n, bool fp
         c.map_a = C.map_xk[par];
         c.map_b = C.map_b;
         c.majors = 0;
+        c.tri = 2;
+        c.map_b_t = C.map_b_mn;
       }
       var[kGram][par].push_back(g);
       var[kPoly][par].push_back(y);
@@ -842,6 +862,7 @@ int dmuon_muon_step(dmuon_context* ctx, const dmuon_matrix* mats, int32_t n, flo
         L.wd = wd;
       }
       const bool pairs = !fp32 && g_ns_pairs;
+      L.tri = (pairs && g_tri) ? 1 : 0;
       const PhaseTiles& T = pairs ? P.phase2[kind] : P.phase[kind];
       L.tiles = static_cast<const uint2*>(T.tiles.p);
       L.cta_begin = static_cast<const int32_t*>(T.cta_begin.p);
@@ -1017,6 +1038,10 @@ int dmuon_set_tuning(int32_t key, int32_t value) {
   }
   if (key == 4) {
     g_tile_order = value ? 1 : 0;
+    return DMUON_OK;
+  }
+  if (key == 6) {
+    g_tri = value ? 1 : 0;
     return DMUON_OK;
   }
   if (key == 5) {

@@ -83,9 +83,16 @@ struct NsProblem {
   int32_t majors;
   // 1: the output is symmetric (Gram, Poly on the tcgen05 path).  Only tiles
   // whose 256-row block is on or above the diagonal 256-column block are
-  // scheduled; tiles strictly above the diagonal also write their transpose.
+  // scheduled.  The one-CTA kernel also writes the transpose of every tile
+  // strictly above the diagonal; the CTA-pair kernel (NsLaunch::tri) does
+  // not, and reads such outputs through `tri` instead.
   int32_t sym;
-  int32_t pad_;
+  // Bit 0 / bit 1: A_op / B_op is a symmetric p x p matrix of which only the
+  // 256-blocks on or above the diagonal are stored (CTA-pair kernel).  A
+  // k-block below the diagonal is loaded from the transposed stored block
+  // through the M/N-contiguous map map_a_t / map_b_t.
+  int32_t tri;
+  int32_t map_a_t, map_b_t;
 };
 
 // Phase kinds of one Newton-Schulz iteration.
@@ -119,6 +126,9 @@ struct NsLaunch {
   const SliceDesc* slices;
   int32_t fuse_update;
   float lr, wd;
+  // CTA-pair kernel: symmetric outputs keep only their upper blocks (no
+  // mirrored stores) and symmetric operands are read through NsProblem::tri.
+  int32_t tri;
 };
 
 // ---- launch wrappers (each returns the cudaError_t of its launch) ----

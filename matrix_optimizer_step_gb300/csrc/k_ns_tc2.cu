@@ -21,6 +21,12 @@
 // one-CTA kernel: two thirds of the shared-memory fill and L2 read traffic
 // per flop.
 //
+// Symmetric outputs (A = X X^T, B = b A + c A A) keep only their 256-blocks
+// on or above the diagonal: nothing is mirrored.  Where a later product reads
+// such a matrix as an operand, a k-block that falls below the diagonal is
+// loaded from the transposed stored block as an M/N-contiguous tile, and the
+// MMA descriptor for that k-block says so (NsProblem::tri).
+//
 // Every spin-wait is bounded; on a timeout the CTA records the error, stops
 // issuing, and both CTAs meet at the final cluster barrier before the pair
 // frees its TMEM.
@@ -40,7 +46,8 @@ constexpr int BK = 64;
 constexpr uint32_t HALF_BYTES = 128 * BK * 2;         // 16 KiB: 128 rows x 64 k, bf16
 constexpr uint32_t STAGE_BYTES = 2 * HALF_BYTES;      // A half + B half per CTA
 constexpr uint32_t MN_BOX_BYTES = 64 * 64 * 2;        // 8 KiB
-constexpr int kThreads = 192;
+constexpr int kThreads = 224;  // warps: 0 A producer, 1 MMA, 2-5 epilogue, 6 B producer
+constexpr int kProducerBWarp = 6;
 constexpr uint32_t kTmemCols = 512;
 template <int STAGES>
 constexpr size_t smem_bytes() {
@@ -66,6 +73,7 @@ __device__ __forceinline__ uint64_t desc_mn(uint32_t base, int kk) {
 struct TileInfo {
   int m0, n0;  // tile origin (rows, columns) of the pair
   int map_a, map_b, z, majors, nk;
+  int tri, map_a_t, map_b_t;
 };
 
 __device__ __forceinline__ TileInfo load_tile_info(const NsLaunch& L, int t) {
@@ -79,7 +87,17 @@ __device__ __forceinline__ TileInfo load_tile_info(const NsLaunch& L, int t) {
   I.z = P.z;
   I.majors = P.majors;
   I.nk = (P.K + BK - 1) / BK;
+  I.tri = L.tri ? P.tri : 0;
+  I.map_a_t = P.map_a_t;
+  I.map_b_t = P.map_b_t;
   return I;
+}
+
+// A k-block of a symmetric operand stored as upper 256-blocks only: below
+// the diagonal (k-block before the operand's row block) it is read from the
+// transposed stored block, M/N-contiguous.
+__device__ __forceinline__ bool tri_below(int tri_bit, int k0, int row0) {
+  return tri_bit && (k0 >> 8) < (row0 >> 8);
 }
 
 template <int STAGES, bool PREFETCH, bool FUSE>
@@ -108,7 +126,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) ns_tc2_
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(full(s), 1);
+      mbar_init(full(s), 2);  // one arrival per operand producer (leader)
       mbar_init(empty(s), 1);
     }
     for (int a = 0; a < 2; ++a) {
@@ -132,65 +150,67 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) ns_tc2_
   const int t_begin = L.cta_begin[pair];
   const int t_end = L.cta_begin[pair + 1];
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
-      int fills[STAGES] = {};
-      bool ok = true;
-      TileInfo cur{}, nxt{};
-      if (t_begin < t_end) cur = load_tile_info(L, t_begin);
-      for (int t = t_begin; t < t_end && ok; ++t) {
-        if (!PREFETCH) cur = load_tile_info(L, t);
-        if (PREFETCH && t + 1 < t_end) nxt = load_tile_info(L, t + 1);
-        const int m0 = cur.m0 + 128 * static_cast<int>(rank);
-        const int n0 = cur.n0 + 128 * static_cast<int>(rank);
-        const CUtensorMap* ma = L.maps + cur.map_a;
-        const CUtensorMap* mb = L.maps + cur.map_b;
-        const bool a_mn = (cur.majors & 1) != 0;
-        const bool b_mn = (cur.majors & 2) != 0;
-        const int z = cur.z;
-        const int nk = cur.nk;
-        if (PREFETCH) cur = nxt;
-        for (int kb = 0; kb < nk; ++kb) {
-          if (!mbar_wait_bounded_cluster(empty(stage), phase ^ 1u, abort_flag, L.err, kErrTimeoutProducer)) {
-            ok = false;
-            break;
-          }
-          const uint32_t leader_full = mapa_shared(full(stage), 0);
-          if (leader) mbar_expect_tx(full(stage), 2 * STAGE_BYTES);
-          ++fills[stage];
-          const uint32_t sa = ring + stage * STAGE_BYTES;
-          const uint32_t sb = sa + HALF_BYTES;
-          const int k0 = kb * BK;
-          if (!a_mn) {
-            tma_load_3d_pair(sa, ma, leader_full, k0, m0, z);
-          } else {
-            tma_load_3d_pair(sa, ma, leader_full, m0, k0, z);
-            tma_load_3d_pair(sa + MN_BOX_BYTES, ma, leader_full, m0 + 64, k0, z);
-          }
-          if (!b_mn) {
-            tma_load_3d_pair(sb, mb, leader_full, k0, n0, z);
-          } else {
-            tma_load_3d_pair(sb, mb, leader_full, n0, k0, z);
-            tma_load_3d_pair(sb + MN_BOX_BYTES, mb, leader_full, n0 + 64, k0, z);
-          }
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
+  if ((warp == 0 || warp == kProducerBWarp) && lane == 0) {
+    // ------------------------------------------- producers (A: warp 0, B: warp 6)
+    // Each operand has its own issuing thread, so the TMA issue work of a
+    // k-block is split over two warps.  Both follow the same ring and wait on
+    // the same `empty` barriers; in the leader each arms `full` with the bytes
+    // of its operand for both CTAs (the barrier takes two arrivals).
+    const int which = (warp == 0) ? 0 : 1;
+    const uint32_t dst_off = which ? HALF_BYTES : 0u;
+    int stage = 0;
+    uint32_t phase = 0;
+    int fills[STAGES] = {};
+    bool ok = true;
+    TileInfo cur{}, nxt{};
+    if (t_begin < t_end) cur = load_tile_info(L, t_begin);
+    for (int t = t_begin; t < t_end && ok; ++t) {
+      if (!PREFETCH) cur = load_tile_info(L, t);
+      if (PREFETCH && t + 1 < t_end) nxt = load_tile_info(L, t + 1);
+      const int tile_row0 = which ? cur.n0 : cur.m0;
+      const int row0 = tile_row0 + 128 * static_cast<int>(rank);
+      const CUtensorMap* map = L.maps + (which ? cur.map_b : cur.map_a);
+      const CUtensorMap* map_t = L.maps + (which ? cur.map_b_t : cur.map_a_t);
+      const bool mn = ((cur.majors >> which) & 1) != 0;
+      const bool tri = ((cur.tri >> which) & 1) != 0;
+      const int z = cur.z;
+      const int nk = cur.nk;
+      // k-blocks before the operand's diagonal block come transposed.
+      const int n_below = tri ? min(nk, (tile_row0 >> 8) * (256 / BK)) : 0;
+      if (PREFETCH) cur = nxt;
+      for (int kb = 0; kb < nk; ++kb) {
+        if (!mbar_wait_bounded_cluster(empty(stage), phase ^ 1u, abort_flag, L.err, kErrTimeoutProducer)) {
+          ok = false;
+          break;
+        }
+        const uint32_t leader_full = mapa_shared(full(stage), 0);
+        if (leader) mbar_expect_tx(full(stage), 2 * HALF_BYTES);
+        ++fills[stage];
+        const uint32_t dst = ring + stage * STAGE_BYTES + dst_off;
+        const int k0 = kb * BK;
+        if (kb < n_below) {
+          tma_load_3d_pair(dst, map_t, leader_full, row0, k0, z);
+          tma_load_3d_pair(dst + MN_BOX_BYTES, map_t, leader_full, row0 + 64, k0, z);
+        } else if (!mn) {
+          tma_load_3d_pair(dst, map, leader_full, k0, row0, z);
+        } else {
+          tma_load_3d_pair(dst, map, leader_full, row0, k0, z);
+          tma_load_3d_pair(dst + MN_BOX_BYTES, map, leader_full, row0 + 64, k0, z);
+        }
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
         }
       }
-      if (!ok && leader) {
-        // The leader's barrier counts both CTAs' bytes: let every armed phase
-        // land before the pair tears down.
-        for (int s = 0; s < STAGES; ++s) {
-          if (fills[s] > 0) {
-            volatile int no_abort = 0;
-            mbar_wait_bounded_cluster(full(s), static_cast<uint32_t>(fills[s] - 1) & 1u, &no_abort, nullptr, 0,
-                                      100000000ull);
-          }
+    }
+    if (!ok && leader) {
+      // The leader's barrier counts both CTAs' bytes: let every armed phase
+      // land before the pair tears down.
+      for (int s = 0; s < STAGES; ++s) {
+        if (fills[s] > 0) {
+          volatile int no_abort = 0;
+          mbar_wait_bounded_cluster(full(s), static_cast<uint32_t>(fills[s] - 1) & 1u, &no_abort, nullptr, 0,
+                                    100000000ull);
         }
       }
     }
@@ -208,7 +228,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) ns_tc2_
         if (PREFETCH && t + 1 < t_end) nxt = load_tile_info(L, t + 1);
         const bool a_mn = (cur.majors & 1) != 0;
         const bool b_mn = (cur.majors & 2) != 0;
-        const uint32_t idesc = idesc_bf16_f32(TILE, TILE, a_mn, b_mn);
+        const int tri = cur.tri;
+        const int tile_m0 = cur.m0, tile_n0 = cur.n0;
         const int nk = cur.nk;
         if (PREFETCH) cur = nxt;
         const int acc = local & 1;
@@ -227,10 +248,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) ns_tc2_
           tc_fence_after();
           const uint32_t sa = ring + stage * STAGE_BYTES;
           const uint32_t sb = sa + HALF_BYTES;
+          const bool a_is_mn = a_mn || tri_below(tri & 1, kb * BK, tile_m0);
+          const bool b_is_mn = b_mn || tri_below(tri & 2, kb * BK, tile_n0);
+          const uint32_t idesc = idesc_bf16_f32(TILE, TILE, a_is_mn, b_is_mn);
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
-            const uint64_t ad = a_mn ? desc_mn(sa, kk) : desc_k(sa, kk);
-            const uint64_t bd = b_mn ? desc_mn(sb, kk) : desc_k(sb, kk);
+            const uint64_t ad = a_is_mn ? desc_mn(sa, kk) : desc_k(sa, kk);
+            const uint64_t bd = b_is_mn ? desc_mn(sb, kk) : desc_k(sb, kk);
             umma_bf16_pair(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
           }
           umma_commit_pair_multicast(empty(stage), 0x3);
@@ -245,7 +269,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) ns_tc2_
       volatile int no_abort = 0;
       mbar_wait_bounded_cluster(drain, 0, &no_abort, L.err, kErrTimeoutDrain);
     }
-  } else {
+  } else if (warp >= 2 && warp <= 5) {
     // ------------------------------------------------------------ epilogue
     const int quarter = warp & 3;
     const int row_in_tile = 128 * static_cast<int>(rank) + quarter * 32 + lane;
@@ -260,7 +284,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) ns_tc2_
       tc_fence_after();
       const uint32_t t_lane =
           tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * TILE);
-      ns_epilogue_tile<FUSE>(L, P, tm * TILE, tn * TILE, row_in_tile, t_lane, !FUSE && P.sym && tm < tn);
+      ns_epilogue_tile<FUSE>(L, P, tm * TILE, tn * TILE, row_in_tile, t_lane,
+                             !FUSE && !L.tri && P.sym && tm < tn);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
