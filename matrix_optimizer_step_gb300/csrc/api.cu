@@ -180,6 +180,7 @@ struct ShapeClass {
   size_t off_x[2], off_a, off_b;  // byte offsets in the workspace
   size_t off_xf, off_af;          // fp32 side copies of X and A (bf16 path only)
   int32_t map_xk[2], map_xmn[2], map_a, map_b, map_a_mn, map_b_mn;
+  int32_t map_x_st[2], map_a_st, map_b_st;  // 64 x 32 boxes for TMA stores
 };
 
 struct PhaseTiles {
@@ -567,6 +568,22 @@ int build_muon_plan(dmuon_context* ctx, const dmuon_matrix* mats, int n, bool fp
       maps.push_back(mat);
       C.map_b_mn = static_cast<int32_t>(maps.size());
       maps.push_back(mbt);
+      // 64 x 32 store boxes: one epilogue warp's 32 rows x 64 columns.
+      CUtensorMap st_map;
+      for (int t = 0; t < 2; ++t) {
+        st = make_map(enc, &st_map, ws + C.off_x[t], C.n, C.m, C.count, C.ld, 64, 32);
+        if (st != DMUON_OK) return st;
+        C.map_x_st[t] = static_cast<int32_t>(maps.size());
+        maps.push_back(st_map);
+      }
+      st = make_map(enc, &st_map, ws + C.off_a, p, p, C.count, C.ldp, 64, 32);
+      if (st != DMUON_OK) return st;
+      C.map_a_st = static_cast<int32_t>(maps.size());
+      maps.push_back(st_map);
+      st = make_map(enc, &st_map, ws + C.off_b, p, p, C.count, C.ldp, 64, 32);
+      if (st != DMUON_OK) return st;
+      C.map_b_st = static_cast<int32_t>(maps.size());
+      maps.push_back(st_map);
     }
     st = upload(P.maps, maps);
     if (st != DMUON_OK) return st;
@@ -602,6 +619,7 @@ int build_muon_plan(dmuon_context* ctx, const dmuon_matrix* mats, int n, bool fp
       g.a = g.b = X;
       g.out = A;
       g.ld_out = C.ldp;
+      g.map_out = C.map_a_st;
       if (!C.tall) {  // A = X X^T: A_op(i,k) = X[i,k], B_op(k,j) = X[j,k]
         g.a_si = C.ld; g.a_sk = 1; g.b_sk = 1; g.b_sj = C.ld;
         g.map_a = g.map_b = C.map_xk[par];
@@ -621,12 +639,14 @@ int build_muon_plan(dmuon_context* ctx, const dmuon_matrix* mats, int n, bool fp
       y.map_a_t = y.map_b_t = C.map_a_mn;
       y.out = B;
       y.ld_out = C.ldp;
+      y.map_out = C.map_b_st;
       y.aux = A;
       y.ld_aux = C.ldp;
       g.sym = y.sym = fp32 ? 0 : 1;
       // Combine: X' = a X + B X (wide) or a X + X B (tall).
       c.out = Xn;
       c.ld_out = C.ld;
+      c.map_out = C.map_x_st[par ^ 1];
       c.aux = X;
       c.ld_aux = C.ld;
       if (!C.tall) {  // M = p, N = q, K = p: A_op = B, B_op(k,j) = X[k,j]
@@ -1032,7 +1052,7 @@ int dmuon_set_tuning(int32_t key, int32_t value) {
     return DMUON_OK;
   }
   if (key == 3) {
-    g_tc2_stages_sel = (value >= 4 && value <= 7) ? value : 4;
+    g_tc2_stages_sel = (value == 5) ? 5 : 4;
     set_tc2_variant(g_tc2_stages_sel, g_tc2_prefetch_sel);
     return DMUON_OK;
   }

@@ -93,6 +93,9 @@ struct NsProblem {
   // through the M/N-contiguous map map_a_t / map_b_t.
   int32_t tri;
   int32_t map_a_t, map_b_t;
+  // Tensor map of `out` with 64 x 32 boxes, for the CTA-pair kernel's staged
+  // TMA stores of bf16 outputs.
+  int32_t map_out;
 };
 
 // Phase kinds of one Newton-Schulz iteration.

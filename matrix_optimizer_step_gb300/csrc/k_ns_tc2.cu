@@ -49,11 +49,12 @@ constexpr uint32_t MN_BOX_BYTES = 64 * 64 * 2;        // 8 KiB
 constexpr int kThreads = 224;  // warps: 0 A producer, 1 MMA, 2-5 epilogue, 6 B producer
 constexpr int kProducerBWarp = 6;
 constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t STAGING_BYTES = 4 * 2 * 4096;  // 4 epilogue warps x 2 boxes of 32 x 64 bf16
 template <int STAGES>
 constexpr size_t smem_bytes() {
-  return 1024 + STAGES * STAGE_BYTES + (2 * STAGES + 5) * 8 + 16;
+  return 1024 + STAGES * STAGE_BYTES + STAGING_BYTES + (2 * STAGES + 5) * 8 + 16;
 }
-static_assert(smem_bytes<7>() <= 227 * 1024, "shared memory budget");
+static_assert(smem_bytes<5>() <= 227 * 1024, "shared memory budget");
 // Every CTA allocates all 512 TMEM columns, so two CTAs must never share an
 // SM: a second resident pair could hold one SM's TMEM while its partner waits
 // for the other's.  Asking for more than half of the SM's 228 KiB of shared
@@ -107,7 +108,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) ns_tc2_
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   const uint32_t ring = smem_u32(smem);
-  uint64_t* bar_mem = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  const uint32_t staging = ring + STAGES * STAGE_BYTES;  // 1 KiB aligned (swizzled TMA source)
+  uint64_t* bar_mem = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES + STAGING_BYTES);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_mem + kNumBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -273,6 +275,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) ns_tc2_
     // ------------------------------------------------------------ epilogue
     const int quarter = warp & 3;
     const int row_in_tile = 128 * static_cast<int>(rank) + quarter * 32 + lane;
+    const uint32_t my_staging = staging + static_cast<uint32_t>(warp - 2) * 8192u;
+    uint32_t box_count = 0;
     int local = 0;
     for (int t = t_begin; t < t_end; ++t, ++local) {
       const uint2 tile = L.tiles[t];
@@ -284,8 +288,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) ns_tc2_
       tc_fence_after();
       const uint32_t t_lane =
           tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * TILE);
-      ns_epilogue_tile<FUSE>(L, P, tm * TILE, tn * TILE, row_in_tile, t_lane,
-                             !FUSE && !L.tri && P.sym && tm < tn);
+      if (FUSE)
+        ns_epilogue_tile<true>(L, P, tm * TILE, tn * TILE, row_in_tile, t_lane, false);
+      else
+        ns_epilogue_tile_staged(L, P, tm * TILE, tn * TILE, row_in_tile, t_lane, !L.tri && P.sym && tm < tn,
+                                my_staging, box_count);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
@@ -295,6 +302,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) ns_tc2_
           mbar_arrive_cluster(mapa_shared(tempty(acc), 0));
       }
     }
+    if (lane == 0) bulk_wait_group<0>();  // staged TMA stores complete
+    __syncwarp();
   }
 
   tc_fence_before();
@@ -312,7 +321,7 @@ static int g_tc2_stages = 4;
 static int g_tc2_prefetch = 1;
 
 void set_tc2_variant(int stages, int prefetch) {
-  g_tc2_stages = (stages >= 4 && stages <= 7) ? stages : 6;
+  g_tc2_stages = (stages == 5) ? 5 : 4;
   g_tc2_prefetch = prefetch ? 1 : 0;
 }
 
@@ -338,20 +347,17 @@ static cudaError_t launch_variant(const NsLaunch& L, int n_pairs, cudaStream_t s
 
 cudaError_t launch_ns_tc2(const NsLaunch& L, int n_pairs, cudaStream_t st) {
   if (n_pairs <= 0) return cudaSuccess;
-  switch (g_tc2_stages) {
-    case 4: return g_tc2_prefetch ? launch_variant<4, true>(L, n_pairs, st) : launch_variant<4, false>(L, n_pairs, st);
-    case 5: return g_tc2_prefetch ? launch_variant<5, true>(L, n_pairs, st) : launch_variant<5, false>(L, n_pairs, st);
-    case 7: return g_tc2_prefetch ? launch_variant<7, true>(L, n_pairs, st) : launch_variant<7, false>(L, n_pairs, st);
-    default: return g_tc2_prefetch ? launch_variant<6, true>(L, n_pairs, st) : launch_variant<6, false>(L, n_pairs, st);
-  }
+  if (g_tc2_stages == 5)
+    return g_tc2_prefetch ? launch_variant<5, true>(L, n_pairs, st) : launch_variant<5, false>(L, n_pairs, st);
+  return g_tc2_prefetch ? launch_variant<4, true>(L, n_pairs, st) : launch_variant<4, false>(L, n_pairs, st);
 }
 
 // Largest number of CTA pairs of this kernel that can be resident at once.
 int ns_tc2_max_pairs() {
   static int cached = -1;
   if (cached >= 0) return cached;
-  constexpr size_t smem = smem_bytes<7>();
-  if (cudaFuncSetAttribute(ns_tc2_kernel<7, true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  constexpr size_t smem = smem_bytes<5>();
+  if (cudaFuncSetAttribute(ns_tc2_kernel<5, true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem)) != cudaSuccess) {
     cudaGetLastError();
     return cached = 0;
@@ -361,7 +367,7 @@ int ns_tc2_max_pairs() {
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, ns_tc2_kernel<7, true, false>, &cfg) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&n, ns_tc2_kernel<5, true, false>, &cfg) != cudaSuccess) {
     cudaGetLastError();
     n = 0;
   }

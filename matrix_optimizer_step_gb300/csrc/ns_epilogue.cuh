@@ -211,3 +211,152 @@ __device__ __forceinline__ void ns_epilogue_tile(const NsLaunch& L, const NsProb
 }
 
 }  // namespace dmuon
+
+namespace dmuon {
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+// Epilogue of the CTA-pair kernel for a bf16 output: the warp stages each
+// 32-row x 64-column box of its result in shared memory (128-byte swizzle:
+// the 16-byte piece j of row r sits at r*128 + ((j ^ (r & 7)) * 16), so a
+// warp's stores hit distinct banks) and lane 0 writes the box with one TMA
+// tile store (asynchronous, edges clipped by the hardware).  Two 4 KiB
+// buffers per warp alternate; before refilling one, lane 0 waits until the
+// store issued two boxes earlier has finished reading it.  The optional fp32
+// copy (first iteration) and the mirrored copy (when symmetric outputs are
+// not kept as upper blocks) are still stored directly.
+__device__ __forceinline__ void ns_epilogue_tile_staged(const NsLaunch& L, const NsProblem& P, int m0, int n0,
+                                                        int row_in_tile, uint32_t t_lane, bool mirror,
+                                                        uint32_t stage_smem, uint32_t& box_count) {
+  constexpr int BN = 256;
+  const int lane = threadIdx.x & 31;
+  float g = 1.f;
+  if (L.gscale && L.gpow > 0) {
+    const float s = L.gscale[P.slice];
+    g = (L.gpow == 2) ? s * s : s;
+  }
+  float alpha, beta;
+  if (L.kind == kGram) {
+    alpha = g;
+    beta = 0.f;
+  } else if (L.kind == kPoly) {
+    alpha = L.c;
+    beta = L.b;
+  } else {
+    alpha = g;
+    beta = g * L.a;
+  }
+  const int row = m0 + row_in_tile;
+  const bool row_ok = row < P.M;
+  const int warp_row0 = row - lane;
+  const uint16_t* aux_row = reinterpret_cast<const uint16_t*>(P.aux) + static_cast<int64_t>(row) * P.ld_aux;
+  const float* auxf_row = reinterpret_cast<const float*>(P.aux) + static_cast<int64_t>(row) * P.ld_aux;
+  float* out2_row = P.out2 ? P.out2 + static_cast<int64_t>(row) * P.ld_out2 : nullptr;
+  const bool aux_f32 = L.aux_f32 != 0;
+  const CUtensorMap* map_out = L.maps + P.map_out;
+  const int n_boxes = (min(BN, P.N - n0) + 63) / 64;
+
+  const bool need_aux = beta != 0.f && row_ok;
+  auto load_aux = [&](int cc, uint4 (&q)[8]) {
+    const int c0 = n0 + cc * 32;
+    if (!need_aux || c0 + 32 > P.N) return;
+    if (aux_f32) {
+      const uint4* src = reinterpret_cast<const uint4*>(auxf_row + c0);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) q[i] = __ldg(src + i);
+    } else {
+      const uint4* src = reinterpret_cast<const uint4*>(aux_row + c0);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) q[i] = __ldg(src + i);
+    }
+  };
+  uint4 aux_next[8];
+  load_aux(0, aux_next);
+#pragma unroll 1
+  for (int cc = 0; cc < 2 * n_boxes; ++cc) {
+    const int col0 = n0 + cc * 32;
+    uint4 aux_cur[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) aux_cur[i] = aux_next[i];
+    if (cc + 1 < 2 * n_boxes) load_aux(cc + 1, aux_next);
+    __syncwarp();
+    uint32_t r[32];
+    tmem_ld_32x32b_x32(t_lane + static_cast<uint32_t>(cc * 32), r);
+    const bool full_chunk = (col0 + 32 <= P.N);
+    float auxf[32];
+    if (need_aux && full_chunk) {
+      if (aux_f32) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          auxf[4 * i] = __uint_as_float(aux_cur[i].x);
+          auxf[4 * i + 1] = __uint_as_float(aux_cur[i].y);
+          auxf[4 * i + 2] = __uint_as_float(aux_cur[i].z);
+          auxf[4 * i + 3] = __uint_as_float(aux_cur[i].w);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const uint32_t w[4] = {aux_cur[i].x, aux_cur[i].y, aux_cur[i].z, aux_cur[i].w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            auxf[8 * i + 2 * j] = __uint_as_float(w[j] << 16);
+            auxf[8 * i + 2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+          }
+        }
+      }
+    } else if (need_aux) {
+      for (int j = 0; j < 32; ++j) {
+        const int c = col0 + j;
+        auxf[j] = (c < P.N) ? (aux_f32 ? auxf_row[c] : bf16_bits_to_f32(aux_row[c])) : 0.f;
+      }
+    }
+    tmem_ld_wait();
+    float v[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      v[j] = alpha * __uint_as_float(r[j]);
+      if (need_aux) v[j] = fmaf(beta, auxf[j], v[j]);
+    }
+    const uint32_t buf = stage_smem + (box_count & 1u) * 4096u;
+    if ((cc & 1) == 0) {
+      if (lane == 0) bulk_wait_group_read<1>();
+      __syncwarp();
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t j = static_cast<uint32_t>(4 * (cc & 1) + i);
+      st_shared_v4(buf + static_cast<uint32_t>(lane) * 128u + ((j ^ static_cast<uint32_t>(lane & 7)) << 4),
+                   pack_bf16x2(v[8 * i], v[8 * i + 1]), pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
+                   pack_bf16x2(v[8 * i + 4], v[8 * i + 5]), pack_bf16x2(v[8 * i + 6], v[8 * i + 7]));
+    }
+    if (row_ok && out2_row) {
+      if (full_chunk) {
+        float4* d2 = reinterpret_cast<float4*>(out2_row + col0);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) d2[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+      } else {
+        for (int j = 0; j < 32 && col0 + j < P.N; ++j) out2_row[col0 + j] = v[j];
+      }
+    }
+    if (row_ok && mirror) {
+      uint16_t* mo = reinterpret_cast<uint16_t*>(P.out) + row;
+      for (int j = 0; j < 32 && col0 + j < P.N; ++j) {
+        mo[static_cast<int64_t>(col0 + j) * P.ld_out] = to_bf16_bits(v[j]);
+        if (P.out2) P.out2[static_cast<int64_t>(col0 + j) * P.ld_out2 + row] = v[j];
+      }
+    }
+    if (cc & 1) {
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_3d(map_out, buf, n0 + 64 * (cc >> 1), warp_row0, P.z);
+        bulk_commit_group();
+      }
+      ++box_count;
+    }
+  }
+}
+
+}  // namespace dmuon
