@@ -293,3 +293,24 @@ def test_pair_kernel_agrees_with_one_cta_kernel(cuda_lib):
         cuda_lib.dmuon_set_tuning(2, 1)
     for x, y in zip(a, b):
         assert abs(x["O"] - y["O"]) <= 5e-3, (x, y)
+
+
+# ----------------------------------------------- every selectable kernel path
+
+VARIANT_SHAPES = [(256, 512), (512, 256), (520, 520), (200, 328), (1000, 130), (3, 4), (2, 96, 160)]
+
+
+@pytest.mark.parametrize("key,value", [(3, 5), (4, 0), (5, 0), (6, 0)])
+def test_pair_kernel_tuning_variants(cuda_lib, key, value):
+    """5-stage ring, rows-outer tile order, no descriptor prefetch, mirrored
+    symmetric outputs: each selectable variant of the CTA-pair kernel against
+    the oracle."""
+    defaults = {3: 4, 4: 1, 5: 1, 6: 1}
+    cuda_lib.dmuon_set_tuning(key, value)
+    try:
+        res = run_muon(cuda_lib, VARIANT_SHAPES, seed=30 + key)[0]
+    finally:
+        cuda_lib.dmuon_set_tuning(key, defaults[key])
+    for r in res:
+        assert r["buf"] <= 1e-6 and r["param_exact"], r
+        assert max(r["O_slices"]) <= bf16_tol(r["shape"]), r
