@@ -154,6 +154,19 @@ cudaError_t launch_ns_tc2(const NsLaunch& L, int n_pairs, cudaStream_t st);
 int ns_tc2_max_pairs();
 cudaError_t launch_ns_simt(const NsLaunch& L, int n_tiles, cudaStream_t st);
 
+// Function attributes (e.g. the shared-memory opt-in) are per device: one
+// bit per device ordinal records that a kernel's attributes are set there.
+inline bool attr_needed_on_current_device(unsigned long long* mask) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev > 63) return true;
+  return (__atomic_load_n(mask, __ATOMIC_ACQUIRE) & (1ull << dev)) == 0;
+}
+inline void attr_note_current_device(unsigned long long* mask) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev <= 63)
+    __atomic_fetch_or(mask, 1ull << dev, __ATOMIC_ACQ_REL);
+}
+
 // Tile geometry of the two Newton-Schulz GEMM paths.
 constexpr int kTcBM = 128, kTcBN = 256, kTcBK = 64;
 constexpr int kTc2Tile = 256;

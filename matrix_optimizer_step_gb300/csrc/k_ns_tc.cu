@@ -287,12 +287,12 @@ void set_tc_mn_swap(int v) { g_mn_swap = v; }
 
 template <bool FUSE>
 static cudaError_t launch_tc_variant(const NsLaunch& L, int n_ctas, cudaStream_t st) {
-  static bool attr_set = false;
-  if (!attr_set) {
+  static unsigned long long attr_mask = 0;
+  if (attr_needed_on_current_device(&attr_mask)) {
     cudaError_t e = cudaFuncSetAttribute(ns_tc_kernel<FUSE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kSmemBytes));
     if (e != cudaSuccess) return e;
-    attr_set = true;
+    attr_note_current_device(&attr_mask);
   }
   ns_tc_kernel<FUSE><<<n_ctas, kThreads, kSmemBytes, st>>>(L, g_mn_swap);
   return cudaGetLastError();

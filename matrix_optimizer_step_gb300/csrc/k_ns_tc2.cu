@@ -327,13 +327,13 @@ void set_tc2_variant(int stages, int prefetch) {
 
 template <int STAGES, bool PREFETCH, bool FUSE>
 static cudaError_t launch_variant3(const NsLaunch& L, int n_pairs, cudaStream_t st) {
-  static bool attr_set = false;
+  static unsigned long long attr_mask = 0;
   constexpr size_t smem = smem_bytes<STAGES>();
-  if (!attr_set) {
+  if (attr_needed_on_current_device(&attr_mask)) {
     cudaError_t e = cudaFuncSetAttribute(ns_tc2_kernel<STAGES, PREFETCH, FUSE>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    attr_set = true;
+    attr_note_current_device(&attr_mask);
   }
   ns_tc2_kernel<STAGES, PREFETCH, FUSE><<<2 * n_pairs, kThreads, smem, st>>>(L);
   return cudaGetLastError();
