@@ -176,6 +176,7 @@ struct SliceRef {
 struct ShapeClass {
   int32_t m, n, count;
   bool tall;            // m > n: Gram is X^T X, last product X B
+  bool f32;             // Newton-Schulz in fp32 on CUDA cores (workspace fp32)
   int64_t ld, ldp;      // workspace row pitch (elements) for X and for A/B
   size_t off_x[2], off_a, off_b;  // byte offsets in the workspace
   size_t off_xf, off_af;          // fp32 side copies of X and A (bf16 path only)
@@ -198,19 +199,27 @@ struct MuonPlan {
   std::vector<int32_t> slice_chunk_begin, slice_chunk_end;
   size_t ws_bytes = 0;
   DevBuf chunks_dev, partials, inv_norm, maps;
+  std::vector<Chunk> chunks_f32;  // chunks of the fp32-class slices only
+  DevBuf chunks_f32_dev;
   // Problem tables per kind and variant: 0/1 = X in buffer 0/1 (later
-  // iterations), 2 = first iteration, 3 = second iteration.
-  DevBuf probs[3][4];
-  PhaseTiles phase[3];   // fp32 path or one-CTA tensor-core tiles
-  PhaseTiles phase2[3];  // CTA-pair tensor-core tiles (bf16 path only)
+  // iterations), 2 = first iteration, 3 = second iteration.  probs: the
+  // bf16 classes (tensor cores); probs_f32: the fp32 classes (CUDA cores,
+  // variants 0 and 1 only).
+  DevBuf probs[3][4], probs_f32[3][2];
+  PhaseTiles phase[3];      // one-CTA tensor-core tiles
+  PhaseTiles phase2[3];     // CTA-pair tensor-core tiles
+  PhaseTiles phase_f32[3];  // fp32 CUDA-core tiles
   void release() {
     chunks_dev.release();
+    chunks_f32_dev.release();
+    for (auto& k : probs_f32)
+      for (auto& p : k) p.release();
     partials.release();
     inv_norm.release();
     maps.release();
     for (auto& k : probs)
       for (auto& p : k) p.release();
-    for (auto* ph : {phase, phase2})
+    for (auto* ph : {phase, phase2, phase_f32})
       for (int k = 0; k < 3; ++k) {
         ph[k].tiles.release();
         ph[k].cta_begin.release();
@@ -219,6 +228,7 @@ struct MuonPlan {
     slices.clear();
     classes.clear();
     chunks.clear();
+    chunks_f32.clear();
     key.clear();
   }
 };
@@ -449,7 +459,6 @@ int build_muon_plan(dmuon_context* ctx, const dmuon_matrix* mats, int n, bool fp
   MuonPlan& P = ctx->plan;
   P.release();
   P.fp32 = fp32;
-  const int64_t es = fp32 ? 4 : 2;
 
   // Slices and shape classes.
   for (int i = 0; i < n; ++i) {
@@ -467,6 +476,7 @@ int build_muon_plan(dmuon_context* ctx, const dmuon_matrix* mats, int n, bool fp
       C.n = nn;
       C.count = 0;
       C.tall = m > nn;
+      C.f32 = fp32 || std::min(m, nn) < kFp32BelowP;
       P.classes.push_back(C);
       cls = static_cast<int>(P.classes.size()) - 1;
     }
@@ -490,13 +500,14 @@ int build_muon_plan(dmuon_context* ctx, const dmuon_matrix* mats, int n, bool fp
   };
   for (auto& C : P.classes) {
     const int64_t p = std::min(C.m, C.n);
+    const int64_t es = C.f32 ? 4 : 2;
     C.ld = round_up(C.n, 8);
     C.ldp = round_up(p, 8);
     for (int t = 0; t < 2; ++t) C.off_x[t] = take(static_cast<size_t>(C.count) * C.m * C.ld * es);
     C.off_a = take(static_cast<size_t>(C.count) * p * C.ldp * es);
     C.off_b = take(static_cast<size_t>(C.count) * p * C.ldp * es);
-    C.off_xf = fp32 ? 0 : take(static_cast<size_t>(C.count) * C.m * C.ld * 4);
-    C.off_af = fp32 ? 0 : take(static_cast<size_t>(C.count) * p * C.ldp * 4);
+    C.off_xf = C.f32 ? 0 : take(static_cast<size_t>(C.count) * C.m * C.ld * 4);
+    C.off_af = C.f32 ? 0 : take(static_cast<size_t>(C.count) * p * C.ldp * 4);
   }
   P.ws_bytes = std::max<size_t>(off, 1024);
   if (ctx->ws.bytes < P.ws_bytes) {
@@ -519,12 +530,17 @@ int build_muon_plan(dmuon_context* ctx, const dmuon_matrix* mats, int n, bool fp
       ch.start = st;
       ch.count = static_cast<int32_t>(std::min<int64_t>(kChunkElems, numel - st));
       P.chunks.push_back(ch);
+      if (C.f32) P.chunks_f32.push_back(ch);
     }
     P.slice_chunk_end[s] = static_cast<int32_t>(P.chunks.size());
   }
   if (P.chunks.size() > size_t(INT32_MAX)) return set_error(DMUON_ERR_SHAPE, "too many chunks");
   int st = upload(P.chunks_dev, P.chunks);
   if (st != DMUON_OK) return st;
+  if (!P.chunks_f32.empty()) {
+    st = upload(P.chunks_f32_dev, P.chunks_f32);
+    if (st != DMUON_OK) return st;
+  }
   st = dev_alloc(P.partials, std::max<size_t>(P.chunks.size(), 1) * sizeof(float));
   if (st != DMUON_OK) return st;
   st = dev_alloc(P.inv_norm, std::max<size_t>(P.slices.size(), 1) * sizeof(float));
@@ -532,10 +548,13 @@ int build_muon_plan(dmuon_context* ctx, const dmuon_matrix* mats, int n, bool fp
 
   // Tensor maps (tcgen05 path): per class X0/X1 K-major and MN-major, A, B.
   std::vector<CUtensorMap> maps;
-  if (!fp32) {
+  bool any_bf16 = false;
+  for (const auto& C : P.classes) any_bf16 = any_bf16 || !C.f32;
+  if (any_bf16) {
     EncodeTiledFn enc = get_encode_fn();
     if (!enc) return set_error(DMUON_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
     for (auto& C : P.classes) {
+      if (C.f32) continue;
       const int64_t p = std::min(C.m, C.n);
       for (int t = 0; t < 2; ++t) {
         CUtensorMap mk, mm;
@@ -589,24 +608,26 @@ int build_muon_plan(dmuon_context* ctx, const dmuon_matrix* mats, int n, bool fp
     if (st != DMUON_OK) return st;
   }
 
-  // Problems of the three phases.  Variant 0/1: X in buffer 0/1, everything
-  // bf16 (or everything fp32 in validation mode).  Variant 2 (first
-  // iteration, X in buffer 0) and 3 (second iteration, X in buffer 1) add the
-  // fp32 side copies on the bf16 path: the first Gram also writes A in fp32,
-  // the first Poly reads that fp32 A, the first Combine reads the fp32 X0 and
-  // writes X1 in fp32 over it (each element is read before it is written, by
-  // the same thread), and the second Combine reads that fp32 X1.
-  std::vector<NsProblem> var[3][4];
+  // Problems of the three phases.  bf16 classes, variant 0/1: X in buffer
+  // 0/1, everything bf16.  Variant 2 (first iteration, X in buffer 0) and 3
+  // (second iteration, X in buffer 1) add the fp32 side copies: the first
+  // Gram also writes A in fp32, the first Poly reads that fp32 A, the first
+  // Combine reads the fp32 X0 and writes X1 in fp32 over it (each element is
+  // read before it is written, by the same thread), and the second Combine
+  // reads that fp32 X1.  fp32 classes (all of them in validation mode) go to
+  // separate lists with variants 0/1 only.
+  std::vector<NsProblem> var[3][4], var_f32[3][2];
   for (size_t s_i = 0; s_i < P.slices.size(); ++s_i) {
     const SliceRef& R = P.slices[s_i];
     const ShapeClass& C = P.classes[static_cast<size_t>(R.cls)];
+    const int64_t es = C.f32 ? 4 : 2;
     const int32_t p = std::min(C.m, C.n), q = std::max(C.m, C.n);
     const size_t xoff = static_cast<size_t>(R.z) * C.m * C.ld;
     const size_t poff = static_cast<size_t>(R.z) * p * C.ldp;
     uint8_t* A = ws + C.off_a + poff * es;
     uint8_t* B = ws + C.off_b + poff * es;
-    float* Xf = fp32 ? nullptr : reinterpret_cast<float*>(ws + C.off_xf) + xoff;
-    float* Af = fp32 ? nullptr : reinterpret_cast<float*>(ws + C.off_af) + poff;
+    float* Xf = C.f32 ? nullptr : reinterpret_cast<float*>(ws + C.off_xf) + xoff;
+    float* Af = C.f32 ? nullptr : reinterpret_cast<float*>(ws + C.off_af) + poff;
     for (int par = 0; par < 2; ++par) {
       uint8_t* X = ws + C.off_x[par] + xoff * es;
       uint8_t* Xn = ws + C.off_x[par ^ 1] + xoff * es;
@@ -642,7 +663,7 @@ int build_muon_plan(dmuon_context* ctx, const dmuon_matrix* mats, int n, bool fp
       y.map_out = C.map_b_st;
       y.aux = A;
       y.ld_aux = C.ldp;
-      g.sym = y.sym = fp32 ? 0 : 1;
+      g.sym = y.sym = C.f32 ? 0 : 1;
       // Combine: X' = a X + B X (wide) or a X + X B (tall).
       c.out = Xn;
       c.ld_out = C.ld;
@@ -668,10 +689,16 @@ int build_muon_plan(dmuon_context* ctx, const dmuon_matrix* mats, int n, bool fp
         c.tri = 2;
         c.map_b_t = C.map_b_mn;
       }
+      if (C.f32) {
+        var_f32[kGram][par].push_back(g);
+        var_f32[kPoly][par].push_back(y);
+        var_f32[kCombine][par].push_back(c);
+        continue;
+      }
       var[kGram][par].push_back(g);
       var[kPoly][par].push_back(y);
       var[kCombine][par].push_back(c);
-      if (!fp32 && par == 0) {
+      if (par == 0) {
         g.out2 = Af;
         g.ld_out2 = C.ldp;
         y.aux = Af;
@@ -679,21 +706,30 @@ int build_muon_plan(dmuon_context* ctx, const dmuon_matrix* mats, int n, bool fp
         c.out2 = Xf;
         c.ld_out2 = C.ld;
       }
-      if (!fp32 && par == 1) c.aux = Xf;
+      if (par == 1) c.aux = Xf;
       var[kGram][2 + par].push_back(g);
       var[kPoly][2 + par].push_back(y);
       var[kCombine][2 + par].push_back(c);
     }
   }
-  for (int kind = 0; kind < 3; ++kind)
+  for (int kind = 0; kind < 3; ++kind) {
     for (int v = 0; v < 4; ++v) {
       st = upload(P.probs[kind][v], var[kind][v]);
       if (st != DMUON_OK) return st;
     }
+    for (int v = 0; v < 2; ++v) {
+      st = upload(P.probs_f32[kind][v], var_f32[kind][v]);
+      if (st != DMUON_OK) return st;
+    }
+  }
   for (int kind = 0; kind < 3; ++kind) {
-    st = build_phase_tiles(var[kind][0], fp32 ? 0 : 1, ctx->num_sms, P.phase[kind]);
-    if (st != DMUON_OK) return st;
-    if (!fp32) {
+    if (!var_f32[kind][0].empty()) {
+      st = build_phase_tiles(var_f32[kind][0], 0, ctx->num_sms, P.phase_f32[kind]);
+      if (st != DMUON_OK) return st;
+    }
+    if (!var[kind][0].empty()) {
+      st = build_phase_tiles(var[kind][0], 1, ctx->num_sms, P.phase[kind]);
+      if (st != DMUON_OK) return st;
       const int pairs = std::max(1, std::min(ctx->num_sms / 2, ns_tc2_max_pairs()));
       st = build_phase_tiles(var[kind][0], 2, pairs, P.phase2[kind]);
       if (st != DMUON_OK) return st;
@@ -812,7 +848,6 @@ int dmuon_muon_step(dmuon_context* ctx, const dmuon_matrix* mats, int32_t n, flo
       return st;
     }
   }
-  const int64_t es = fp32 ? 4 : 2;
   uint8_t* ws = static_cast<uint8_t*>(ctx->ws.p);
 
   // Per-call pointer table.
@@ -828,9 +863,10 @@ int dmuon_muon_step(dmuon_context* ctx, const dmuon_matrix* mats, int32_t n, flo
     D.grad_bf16 = M.grad_dtype == DMUON_DTYPE_BF16;
     D.grad = static_cast<const uint8_t*>(M.grad) + R.elem_offset * (D.grad_bf16 ? 2 : 4);
     D.param = M.param_bf16 ? M.param_bf16 + R.elem_offset : nullptr;
-    const size_t xoff = static_cast<size_t>(R.z) * C.m * C.ld * es;
+    const size_t xoff = static_cast<size_t>(R.z) * C.m * C.ld * (C.f32 ? 4 : 2);
     D.x0 = ws + C.off_x[0] + xoff;
-    D.x0f = fp32 ? nullptr : reinterpret_cast<float*>(ws + C.off_xf) + static_cast<size_t>(R.z) * C.m * C.ld;
+    D.x0f = C.f32 ? nullptr : reinterpret_cast<float*>(ws + C.off_xf) + static_cast<size_t>(R.z) * C.m * C.ld;
+    D.x_f32 = C.f32 ? 1 : 0;
     D.xk = ws + C.off_x[ns_steps & 1] + xoff;
     D.ld = C.ld;
     D.m = C.m;
@@ -851,7 +887,7 @@ int dmuon_muon_step(dmuon_context* ctx, const dmuon_matrix* mats, int32_t n, flo
 
   const int nesterov = (flags & DMUON_FLAG_NESTEROV) ? 1 : 0;
   st = timed_launch(ctx, DMUON_KERNEL_MOMENTUM, s, [&] {
-    return launch_momentum(d_slices, d_chunks, n_chunks, momentum, nesterov, fp32 ? 1 : 0, partials, s);
+    return launch_momentum(d_slices, d_chunks, n_chunks, momentum, nesterov, 0, partials, s);
   });
   if (st != DMUON_OK) return st;
   st = timed_launch(ctx, DMUON_KERNEL_NORM, s, [&] {
@@ -862,10 +898,6 @@ int dmuon_muon_step(dmuon_context* ctx, const dmuon_matrix* mats, int32_t n, flo
     const int variant = it < 2 ? 2 + it : (it & 1);
     for (int kind = kGram; kind <= kCombine; ++kind) {
       NsLaunch L{};
-      L.probs = static_cast<const NsProblem*>(P.probs[kind][variant].p);
-      L.aux_f32 = (!fp32 && ((it == 0 && kind != kGram) || (it == 1 && kind == kCombine))) ? 1 : 0;
-      L.tiles = static_cast<const uint2*>(P.phase[kind].tiles.p);
-      L.cta_begin = static_cast<const int32_t*>(P.phase[kind].cta_begin.p);
       L.maps = static_cast<const CUtensorMap*>(P.maps.p);
       L.gscale = (it == 0 && kind != kPoly) ? inv_norm : nullptr;
       L.gpow = (kind == kGram) ? 2 : 1;
@@ -874,29 +906,48 @@ int dmuon_muon_step(dmuon_context* ctx, const dmuon_matrix* mats, int32_t n, flo
       L.b = b;
       L.c = c;
       L.err = static_cast<int*>(ctx->err.p);
-      if (!fp32 && kind == kCombine && it == ns_steps - 1) {
-        // The last Combine applies the update itself (no X store, no update pass).
-        L.fuse_update = 1;
-        L.slices = d_slices;
-        L.lr = lr;
-        L.wd = wd;
+      // Tensor-core launch over the bf16 classes.
+      if (P.phase[kind].n_tiles > 0) {
+        NsLaunch T = L;
+        T.probs = static_cast<const NsProblem*>(P.probs[kind][variant].p);
+        T.aux_f32 = ((it == 0 && kind != kGram) || (it == 1 && kind == kCombine)) ? 1 : 0;
+        if (kind == kCombine && it == ns_steps - 1) {
+          // The last Combine applies the update itself (no X store, no update pass).
+          T.fuse_update = 1;
+          T.slices = d_slices;
+          T.lr = lr;
+          T.wd = wd;
+        }
+        const bool pairs = g_ns_pairs != 0;
+        T.tri = (pairs && g_tri) ? 1 : 0;
+        const PhaseTiles& PT = pairs ? P.phase2[kind] : P.phase[kind];
+        T.tiles = static_cast<const uint2*>(PT.tiles.p);
+        T.cta_begin = static_cast<const int32_t*>(PT.cta_begin.p);
+        st = timed_launch(ctx, DMUON_KERNEL_NS_GRAM + kind, s, [&] {
+          return pairs ? launch_ns_tc2(T, PT.n_ctas, s) : launch_ns_tc(T, PT.n_ctas, s);
+        });
+        if (st != DMUON_OK) return st;
       }
-      const bool pairs = !fp32 && g_ns_pairs;
-      L.tri = (pairs && g_tri) ? 1 : 0;
-      const PhaseTiles& T = pairs ? P.phase2[kind] : P.phase[kind];
-      L.tiles = static_cast<const uint2*>(T.tiles.p);
-      L.cta_begin = static_cast<const int32_t*>(T.cta_begin.p);
-      st = timed_launch(ctx, DMUON_KERNEL_NS_GRAM + kind, s, [&] {
-        if (fp32) return launch_ns_simt(L, T.n_tiles, s);
-        return pairs ? launch_ns_tc2(L, T.n_ctas, s) : launch_ns_tc(L, T.n_ctas, s);
-      });
-      if (st != DMUON_OK) return st;
+      // CUDA-core launch over the fp32 classes.
+      const PhaseTiles& PF = P.phase_f32[kind];
+      if (PF.n_tiles > 0) {
+        NsLaunch F = L;
+        F.probs = static_cast<const NsProblem*>(P.probs_f32[kind][it & 1].p);
+        F.tiles = static_cast<const uint2*>(PF.tiles.p);
+        F.cta_begin = static_cast<const int32_t*>(PF.cta_begin.p);
+        st = timed_launch(ctx, DMUON_KERNEL_NS_GRAM + kind, s, [&] { return launch_ns_simt(F, PF.n_tiles, s); });
+        if (st != DMUON_OK) return st;
+      }
     }
   }
-  if (!fp32 && ns_steps > 0) return DMUON_OK;  // fused into the last Combine
+  // The bf16 classes' update is fused into their last Combine; the update
+  // pass covers the fp32 classes (every slice when there are no iterations).
+  const bool all = ns_steps == 0;
+  const int n_upd = all ? n_chunks : static_cast<int>(P.chunks_f32.size());
+  if (n_upd == 0) return DMUON_OK;
+  const Chunk* d_upd = all ? d_chunks : static_cast<const Chunk*>(P.chunks_f32_dev.p);
   return timed_launch(ctx, DMUON_KERNEL_UPDATE, s, [&] {
-    return launch_update(d_slices, d_chunks, n_chunks, lr, wd, fp32 ? 1 : 0,
-                         ns_steps == 0 ? inv_norm : nullptr, s);
+    return launch_update(d_slices, d_upd, n_upd, lr, wd, 0, all ? inv_norm : nullptr, s);
   });
 }
 

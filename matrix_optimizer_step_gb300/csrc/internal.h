@@ -37,7 +37,7 @@ struct SliceDesc {
   float shape_scale;      // sqrt(max(1, m/n))
   int32_t chunk_begin;    // first chunk of this slice in the chunk table
   int32_t chunk_end;
-  int32_t pad_;
+  int32_t x_f32;          // 1: this slice's NS workspace is fp32 (fp32 CUDA-core path)
 };
 
 // A contiguous run of one slice's elements (row-major element index of the
@@ -171,6 +171,11 @@ inline void attr_note_current_device(unsigned long long* mask) {
 constexpr int kTcBM = 128, kTcBN = 256, kTcBK = 64;
 constexpr int kTc2Tile = 256;
 constexpr int kSimtBM = 64, kSimtBN = 64;
+// Slices with min(m, n) below this run Newton-Schulz on the fp32 CUDA-core
+// path even in bf16 mode: with so few singular values the bf16 rounding
+// error does not average out (the oracle's emulation of the bf16 path
+// reaches 2.3e-2 at 24 x 256), and such products are cheap in fp32.
+constexpr int kFp32BelowP = 64;
 constexpr int kChunkElems = 1 << 16;
 
 }  // namespace dmuon

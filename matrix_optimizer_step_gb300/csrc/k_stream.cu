@@ -98,6 +98,7 @@ __global__ void __launch_bounds__(kThreads) momentum_kernel(const SliceDesc* __r
   const Chunk ch = chunks[blockIdx.x];
   const SliceDesc S = slices[ch.slice];
   const int64_t end = ch.start + ch.count;
+  x_fp32 = x_fp32 || S.x_f32;
   float ss = 0.f;
   if (S.vec_ok) {
     const bool dense = (S.ld == S.n);
@@ -166,6 +167,7 @@ __global__ void __launch_bounds__(kThreads) update_kernel(const SliceDesc* __res
   const Chunk ch = chunks[blockIdx.x];
   const SliceDesc S = slices[ch.slice];
   const int64_t end = ch.start + ch.count;
+  x_fp32 = x_fp32 || S.x_f32;
   const float decay = 1.0f - lr * wd;
   float step = lr * S.shape_scale;
   if (xscale) step *= xscale[ch.slice];

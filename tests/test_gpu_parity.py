@@ -88,12 +88,12 @@ BF16_SHAPES = [(256, 512), (384, 128), (256, 256), (200, 328), (328, 200), (3, 4
 
 
 def bf16_tol(shape):
-    # 2e-2 is the bar for the bf16 tensor-core path.  A slice with fewer than
-    # 16 rows or columns holds too few entries for the bf16 rounding errors to
-    # average out (the oracle's own bf16 emulation already reaches 1.6e-2 to
-    # 2.9e-2 on 3x4), so those tiny slices are held to 4e-2 here; the fp32
-    # validation path holds them to 1e-4.
-    return 2e-2 if min(shape[-2:]) >= 16 else 4e-2
+    # 2e-2 is the bar for the bf16 tensor-core path.  Slices with fewer than
+    # 64 rows or columns run Newton-Schulz on the fp32 CUDA-core path even in
+    # a bf16 step (with so few singular values the bf16 rounding errors do not
+    # average out: the oracle's own bf16 emulation reaches 2.3e-2 at 24 x 256
+    # and 2.9e-2 at 3 x 4), so they are held to the fp32 bar.
+    return 2e-2 if min(shape[-2:]) >= 64 else 1e-4
 
 
 def test_bf16_tc_path_grouped(cuda_lib):
@@ -314,3 +314,36 @@ def test_pair_kernel_tuning_variants(cuda_lib, key, value):
     for r in res:
         assert r["buf"] <= 1e-6 and r["param_exact"], r
         assert max(r["O_slices"]) <= bf16_tol(r["shape"]), r
+
+
+# ------------------------------------------------------------- degenerate shapes
+
+EDGE_SHAPES = [(1, 4096), (4096, 1), (1, 1), (2, 3), (17, 1000), (1000, 17), (7, 7), (1, 2, 3), (300, 1),
+               (257, 257), (255, 513)]
+
+
+def test_degenerate_shapes_bf16(cuda_lib):
+    res = run_muon(cuda_lib, EDGE_SHAPES, seed=40)[0]
+    for r in res:
+        assert r["buf"] <= 1e-6 and r["param_exact"], r
+        # A single row or column: p = 1, X X^T is a scalar and NS is exact up
+        # to the bf16 rounding of the vector itself.
+        assert max(r["O_slices"]) <= bf16_tol(r["shape"]), r
+
+
+def test_degenerate_shapes_fp32(cuda_lib):
+    res = run_muon(cuda_lib, EDGE_SHAPES, grad_dtype=torch.float32, fp32_ns=True, seed=41)[0]
+    for r in res:
+        assert r["buf"] <= 1e-6 and r["O"] <= 1e-4 and r["param_exact"], r
+
+
+def test_many_tensors_one_call(cuda_lib):
+    # 300 tensors of 12 distinct shapes in one call: the grouped launches,
+    # tile lists and per-class workspaces at many classes.
+    r = np.random.default_rng(42)
+    sides = [8, 24, 64, 96, 130, 256]
+    shapes = [(int(r.choice(sides)), int(r.choice(sides))) for _ in range(300)]
+    res = run_muon(cuda_lib, shapes, seed=43)[0]
+    for x in res:
+        assert x["buf"] <= 1e-6 and x["param_exact"], x
+        assert max(x["O_slices"]) <= bf16_tol(x["shape"]), x
