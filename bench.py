@@ -292,21 +292,46 @@ def run_ours(args, wl, rank, world, local_rank):
     step.sync(stream)
     ms = reduce_max_over_ranks(e0.elapsed_time(e1) / args.steps, dist, dev)
 
-    # ---------------- end to end: host grads in, host bf16 params out
+    # ---------------- end to end: host grads in, host bf16 params out.
+    # Through dmuon_step_host: every step copies this step's gradients in
+    # from page-locked host memory and the bf16 parameters out, group by
+    # group, overlapped with the other groups' compute.  No overlap across
+    # steps (the next step's gradients would depend on these parameters).
     e2e_steps = max(1, min(args.steps, 3))
     g_flat, p_flat = mat.flats["grad"], mat.flats["param"]
     host_g = torch.empty(g_flat.shape, dtype=g_flat.dtype, pin_memory=True)
     host_p = torch.empty(p_flat.shape, dtype=p_flat.dtype, pin_memory=True)
     host_g.copy_(g_flat)
+
+    def host_views(flat_host, flat_dev, views):
+        base = flat_dev.data_ptr()
+        out = []
+        for v in views:
+            o = (v.data_ptr() - base) // v.element_size()
+            out.append(flat_host[o:o + v.numel()].view(v.shape))
+        return out
+
+    step.set_host_io(host_views(host_g, g_flat, mat.grads), host_views(host_p, p_flat, mat.params),
+                     host_views(host_g, g_flat, mat.v_grads) if wl.vectors else None,
+                     host_views(host_p, p_flat, mat.v_params) if wl.vectors else None)
+
+    def e2e_step():
+        adam_kw = None
+        if wl.vectors:
+            t_counter[0] += 1
+            adam_kw = dict(lr=h["adam_lr"], beta1=h["beta1"], beta2=h["beta2"], eps=h["adam_eps"],
+                           wd=h["adam_wd"], step=t_counter[0])
+        step.step_host(muon_kw, adam_kw, n_groups=args.e2e_groups, stream=stream)
+
+    e2e_step()
+    step.sync(stream)
     barrier()
     torch.cuda.synchronize()
     x0 = torch.cuda.Event(enable_timing=True)
     x1 = torch.cuda.Event(enable_timing=True)
     x0.record(stream)
     for _ in range(e2e_steps):
-        g_flat.copy_(host_g, non_blocking=True)
-        one_step()
-        host_p.copy_(p_flat, non_blocking=True)
+        e2e_step()
     x1.record(stream)
     torch.cuda.synchronize()
     barrier()
@@ -376,7 +401,7 @@ def run_ours(args, wl, rank, world, local_rank):
         "gpu_launches": launches,
         "e2e": {"value": world * ns_flops / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "steps": e2e_steps},
+                "steps": e2e_steps, "api": "dmuon_step_host", "n_groups": args.e2e_groups},
         "clocks": clk,
     }
     if not args.no_cpu_baseline:
@@ -397,6 +422,8 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default="llama3_8b")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-groups", type=int, default=16,
+                    help="groups of the host-buffer step (copies of one group overlap the others' compute)")
     ap.add_argument("--overlap-adamw", action="store_true",
                     help="run the AdamW step on a side stream beside the Muon step (OwnerStep.step)")
     ap.add_argument("--tuning", action="append", default=[],

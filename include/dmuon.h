@@ -116,13 +116,20 @@ DMUON_API int dmuon_lpt_assign_layered(const int64_t* sizes, const int32_t* laye
 /*
  * One Muon-route tensor.  shape[0..rank-1] is row-major and contiguous; the
  * Newton-Schulz iteration acts on the last two dimensions (m rows, n cols)
- * and every leading index is a separate matrix.  All pointers are device
- * pointers to rank-shaped contiguous arrays:
+ * and every leading index is a separate matrix.  All pointers point to
+ * rank-shaped contiguous arrays the context's device can dereference:
  *   master      fp32, read and written (the fp32 master weight W)
  *   momentum    fp32, read and written (the momentum buffer)
  *   grad        fp32 or bf16 per grad_dtype, read only
  *   param_bf16  bf16 (raw uint16 bits), written, may be NULL (no bf16 copy)
  * master, momentum and param_bf16 must not overlap one another or grad.
+ * Reachable means memory of the context's device, managed memory, or
+ * page-locked host memory mapped into the device's address space
+ * (cudaHostAlloc / cudaHostRegister with mapping): the kernels then read
+ * grad and write param_bf16 in host memory directly (over NVLink-C2C on a
+ * Grace host), with no staging copy.  The step checks every pointer the
+ * first time it sees a descriptor array and fails with DMUON_ERR_INVALID_ARG
+ * for pageable host memory or another device's memory.
  */
 typedef struct dmuon_matrix {
   int32_t rank;          /* 2..4 */
@@ -134,9 +141,10 @@ typedef struct dmuon_matrix {
   uint16_t* param_bf16;
 } dmuon_matrix;
 
-/* One AdamW-route tensor, flattened: numel contiguous elements, all device
- * pointers.  master/exp_avg/exp_avg_sq fp32 read+write, grad read only,
- * param_bf16 written (may be NULL). */
+/* One AdamW-route tensor, flattened: numel contiguous elements, every
+ * pointer reachable from the context's device in the sense given for
+ * dmuon_matrix (checked the same way).  master/exp_avg/exp_avg_sq fp32
+ * read+write, grad read only, param_bf16 written (may be NULL). */
 typedef struct dmuon_vector {
   int64_t numel;
   int32_t grad_dtype;    /* DMUON_DTYPE_F32 or DMUON_DTYPE_BF16 */
@@ -247,6 +255,69 @@ DMUON_API int dmuon_muon_step_noalloc(const dmuon_matrix* mat, float lr, float m
 DMUON_API int dmuon_adamw_step(dmuon_context* ctx, const dmuon_vector* ts, int32_t n,
                      float lr, float beta1, float beta2, float eps, float wd,
                      int64_t step, void* stream);
+
+/* Host side of one tensor in dmuon_step_host: page-locked host buffers
+ * (cudaHostAlloc, or cudaHostRegister'ed) with the tensor's shape.
+ *   grad_host   this step's gradient, dtype = the descriptor's grad_dtype;
+ *               read (copied into the descriptor's device grad buffer)
+ *   param_host  bf16 parameter; written (copied from the descriptor's device
+ *               param_bf16 buffer, which must then be non-NULL); NULL = the
+ *               parameter stays on the device only */
+typedef struct dmuon_host_io {
+  const void* grad_host;
+  uint16_t* param_host;
+} dmuon_host_io;
+
+/* Hyper-parameters of dmuon_step_host, as the scalar arguments of
+ * dmuon_muon_step and dmuon_adamw_step. */
+typedef struct dmuon_muon_hparams {
+  float lr, momentum, wd;
+  int32_t ns_steps;
+  float a, b, c;
+  uint32_t flags;
+} dmuon_muon_hparams;
+
+typedef struct dmuon_adamw_hparams {
+  float lr, beta1, beta2, eps, wd;
+  int32_t reserved;  /* 0 */
+  int64_t step;
+} dmuon_adamw_hparams;
+
+/*
+ * dmuon_step_host -- one owner step whose gradients arrive in host memory and
+ * whose bf16 parameters go back to host memory.
+ *
+ * The pages' step starts from gradients already on the owner's GPU; this
+ * entry adds the host side around the same computation.  For every tensor it
+ * copies io.grad_host into the descriptor's device grad buffer, runs exactly
+ * dmuon_muon_step (mats, *muon) and dmuon_adamw_step (vecs, *adamw), and
+ * copies the device param_bf16 buffer into io.param_host.  The Muon tensors
+ * are cut into n_groups consecutive groups of about equal Newton-Schulz work
+ * (1 <= n_groups <= 64, fewer if there are fewer tensors); each group's
+ * gradients travel while earlier groups compute and each group's parameters
+ * travel while later groups compute, on two copy streams the context owns,
+ * so the host link is busy only at the ends of the step.  The AdamW tensors
+ * travel and step right after the first Muon group.  Results are bit-identical
+ * to the device entry points on the same inputs.
+ *
+ *   mats, mat_io  n_mats Muon tensors and their host buffers
+ *   muon          Muon hyper-parameters (non-NULL if n_mats > 0)
+ *   vecs, vec_io  n_vecs AdamW tensors and their host buffers
+ *   adamw         AdamW hyper-parameters (non-NULL if n_vecs > 0)
+ *   stream        all work is ordered after the work already on `stream`,
+ *                 and work enqueued on `stream` later runs after the last
+ *                 parameter copy has landed in host memory
+ * Host buffers are checked once per descriptor array: pageable host memory
+ * is refused (DMUON_ERR_INVALID_ARG).  Other errors as dmuon_muon_step and
+ * dmuon_adamw_step.  Shares the context's workspace with dmuon_muon_step:
+ * the two must not overlap on the GPU.
+ */
+DMUON_API int dmuon_step_host(dmuon_context* ctx,
+                              const dmuon_matrix* mats, const dmuon_host_io* mat_io, int32_t n_mats,
+                              const dmuon_muon_hparams* muon,
+                              const dmuon_vector* vecs, const dmuon_host_io* vec_io, int32_t n_vecs,
+                              const dmuon_adamw_hparams* adamw,
+                              int32_t n_groups, void* stream);
 
 /*
  * dmuon_sync -- wait for the stream and report device-side errors.

@@ -31,6 +31,7 @@ from .capi import (  # noqa: F401
     dmuon_selftest_wait_timeout,
     dmuon_set_tuning,
     dmuon_status_string,
+    dmuon_step_host,
     dmuon_sync,
     load_library,
 )

@@ -37,7 +37,7 @@ EXPORTED = (
     "dmuon_status_string", "dmuon_last_error", "dmuon_lpt_assign", "dmuon_context_create",
     "dmuon_context_destroy", "dmuon_muon_step", "dmuon_adamw_step", "dmuon_sync",
     "dmuon_selftest_wait_timeout", "dmuon_set_tuning", "dmuon_kernel_launches", "dmuon_profile",
-    "dmuon_profile_read", "dmuon_muon_step_noalloc", "dmuon_lpt_assign_layered",
+    "dmuon_profile_read", "dmuon_muon_step_noalloc", "dmuon_lpt_assign_layered", "dmuon_step_host",
 )
 
 KERNEL_KINDS = ("momentum", "norm", "ns_gram", "ns_poly", "ns_combine", "update", "adamw")
@@ -71,6 +71,25 @@ class DmuonVector(ctypes.Structure):
         ("exp_avg_sq", ctypes.c_void_p),
         ("grad", ctypes.c_void_p),
         ("param_bf16", ctypes.c_void_p),
+    ]
+
+
+class DmuonHostIO(ctypes.Structure):
+    _fields_ = [("grad_host", ctypes.c_void_p), ("param_host", ctypes.c_void_p)]
+
+
+class DmuonMuonHparams(ctypes.Structure):
+    _fields_ = [
+        ("lr", ctypes.c_float), ("momentum", ctypes.c_float), ("wd", ctypes.c_float),
+        ("ns_steps", ctypes.c_int32), ("a", ctypes.c_float), ("b", ctypes.c_float), ("c", ctypes.c_float),
+        ("flags", ctypes.c_uint32),
+    ]
+
+
+class DmuonAdamwHparams(ctypes.Structure):
+    _fields_ = [
+        ("lr", ctypes.c_float), ("beta1", ctypes.c_float), ("beta2", ctypes.c_float), ("eps", ctypes.c_float),
+        ("wd", ctypes.c_float), ("reserved", ctypes.c_int32), ("step", ctypes.c_int64),
     ]
 
 
@@ -108,6 +127,10 @@ def load_library(path=LIB_PATH):
         "dmuon_profile_read": (ctypes.c_int, [vp, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(i64)]),
         "dmuon_muon_step_noalloc": (ctypes.c_int, [ctypes.POINTER(DmuonMatrix), f32, f32, f32, i32, f32, f32,
                                                    f32, ctypes.c_uint32, vp]),
+        "dmuon_step_host": (ctypes.c_int, [vp, ctypes.POINTER(DmuonMatrix), ctypes.POINTER(DmuonHostIO), i32,
+                                           ctypes.POINTER(DmuonMuonHparams), ctypes.POINTER(DmuonVector),
+                                           ctypes.POINTER(DmuonHostIO), i32, ctypes.POINTER(DmuonAdamwHparams),
+                                           i32, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -280,3 +303,36 @@ def dmuon_muon_step_noalloc(mat, lr, momentum, wd, ns_steps, a, b, c, flags=DMUO
     _check(load_library().dmuon_muon_step_noalloc(
         ctypes.byref(mat), float(lr), float(momentum), float(wd), int(ns_steps), float(a), float(b),
         float(c), int(flags), _stream_handle(stream)))
+
+
+def muon_hparams(lr, momentum, wd, ns_steps=5, a=3.4445, b=-4.7750, c=2.0315, nesterov=True, fp32_ns=False):
+    flags = (DMUON_FLAG_NESTEROV if nesterov else 0) | (DMUON_FLAG_FP32_NS if fp32_ns else 0)
+    return DmuonMuonHparams(float(lr), float(momentum), float(wd), int(ns_steps), float(a), float(b), float(c),
+                            flags)
+
+
+def adamw_hparams(lr, beta1, beta2, eps, wd, step):
+    return DmuonAdamwHparams(float(lr), float(beta1), float(beta2), float(eps), float(wd), 0, int(step))
+
+
+def dmuon_step_host(ctx, mats, mat_io, muon, vecs=None, vec_io=None, adamw=None, n_groups=8, stream=None):
+    """``mats``/``vecs``: ctypes arrays (or lists) of DmuonMatrix/DmuonVector;
+    ``mat_io``/``vec_io``: matching arrays of DmuonHostIO; ``muon``/``adamw``:
+    DmuonMuonHparams/DmuonAdamwHparams (or None when the list is empty)."""
+    lib = load_library()
+    vecs = [] if vecs is None else vecs
+    vec_io = [] if vec_io is None else vec_io
+    n_m, n_v = len(mats), len(vecs)
+    if len(mat_io) != n_m or len(vec_io) != n_v:
+        raise ValueError("one host io entry per tensor")
+    if isinstance(mats, (list, tuple)):
+        mats = descriptor_array(mats, DmuonMatrix)
+    if isinstance(mat_io, (list, tuple)):
+        mat_io = descriptor_array(mat_io, DmuonHostIO)
+    if isinstance(vecs, (list, tuple)):
+        vecs = descriptor_array(vecs, DmuonVector)
+    if isinstance(vec_io, (list, tuple)):
+        vec_io = descriptor_array(vec_io, DmuonHostIO)
+    _check(lib.dmuon_step_host(ctx, mats, mat_io, n_m, ctypes.byref(muon) if muon is not None else None,
+                               vecs, vec_io, n_v, ctypes.byref(adamw) if adamw is not None else None,
+                               int(n_groups), _stream_handle(stream)))

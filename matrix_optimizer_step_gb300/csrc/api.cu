@@ -23,6 +23,7 @@
 
 #include <algorithm>
 #include <cmath>
+#include <memory>
 #include <new>
 #include <string>
 #include <vector>
@@ -83,6 +84,21 @@ static EncodeTiledFn get_encode_fn() {
                                          &q) == cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
       fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+using PointerAttrFn = CUresult (*)(void*, CUpointer_attribute, CUdeviceptr);
+
+static PointerAttrFn get_pointer_attr_fn() {
+  static PointerAttrFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuPointerGetAttribute", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PointerAttrFn>(p);
   }
   return fn;
 }
@@ -192,6 +208,7 @@ struct PhaseTiles {
 
 struct MuonPlan {
   std::string key;
+  uint64_t ws_epoch = 0;  // workspace allocation the tables point into
   bool fp32 = false;
   std::vector<SliceRef> slices;
   std::vector<ShapeClass> classes;
@@ -244,6 +261,40 @@ struct AdamPlan {
   }
 };
 
+// One Muon tensor list's cached state: its plan, its per-call pointer table
+// and the descriptor bytes that last passed the reachability check.  Slot 0
+// serves dmuon_muon_step; the host pipeline gives each of its groups its own
+// slot, so consecutive groups never wait on one another's table uploads.
+// All slots share the context's workspace (their steps run one after another
+// on one stream); a slot whose plan predates the workspace's current
+// allocation is rebuilt.
+// Copies of one host-buffer step (dmuon_step_host), cached for the
+// descriptor arrays they were built from.
+struct CopyRun {
+  void* dst;
+  const void* src;
+  size_t bytes;
+  uint64_t dst_id, src_id;  // CUDA allocation ids (0 = unknown)
+};
+
+struct HostPlan {
+  std::vector<uint8_t> key;
+  std::vector<std::pair<int, int>> groups;       // [begin, end) of each Muon group
+  std::vector<std::vector<CopyRun>> in, out;     // per group
+  std::vector<CopyRun> a_in, a_out;              // AdamW tensors
+};
+
+struct MuonSlot {
+  MuonPlan plan;
+  StagedTable table;
+  std::vector<uint8_t> checked;
+  void release() {
+    plan.release();
+    table.release();
+    checked.clear();
+  }
+};
+
 // Per-kernel device timing: events recorded around each launch on the
 // launching stream, resolved and summed on read.
 struct Profiler {
@@ -289,10 +340,17 @@ struct dmuon_context {
   int64_t launches = 0;
   dmuon::DevBuf err;
   dmuon::DevBuf ws;
-  dmuon::MuonPlan plan;
+  uint64_t ws_epoch = 0;  // bumped whenever ws is reallocated
+  std::vector<std::unique_ptr<dmuon::MuonSlot>> slots;
   dmuon::AdamPlan adam;
-  dmuon::StagedTable slice_table, vec_table;
+  dmuon::StagedTable vec_table;
   dmuon::Profiler prof;
+  // AdamW descriptor array whose pointers last passed the reachability check.
+  std::vector<uint8_t> checked_vecs;
+  // Host pipeline: copy streams, events, cached groups and copy lists.
+  cudaStream_t h2d = nullptr, d2h = nullptr;
+  std::vector<cudaEvent_t> events;
+  dmuon::HostPlan host;
 };
 
 namespace dmuon {
@@ -335,6 +393,72 @@ int ensure_device(dmuon_context* ctx) {
   if (st != DMUON_OK) return st;
   DM_CUDA(cudaMemset(ctx->err.p, 0, 16));
   ctx->dev_ready = true;
+  return DMUON_OK;
+}
+
+// Every pointer a kernel dereferences must be reachable from the context's
+// device: its own memory, managed memory, or page-locked host memory mapped
+// into the device's address space (on a Grace host the kernels then read and
+// write it over NVLink-C2C, with no staging copy).  Pageable host memory and
+// another device's memory are refused here, before any launch.
+int check_reachable(const dmuon_context* ctx, const void* p, const char* what, int idx) {
+  if (!p) return DMUON_OK;
+  cudaPointerAttributes at;
+  memset(&at, 0, sizeof at);
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();
+    at.type = cudaMemoryTypeUnregistered;
+  }
+  bool ok = false;
+  if (at.type == cudaMemoryTypeDevice) ok = at.device == ctx->device;
+  else if (at.type == cudaMemoryTypeManaged) ok = true;
+  else if (at.type == cudaMemoryTypeHost) ok = at.devicePointer == p;
+  if (ok) return DMUON_OK;
+  char buf[200];
+  snprintf(buf, sizeof buf,
+           "tensor %d: %s pointer is not reachable from device %d (pageable host memory or another "
+           "device's memory)", idx, what, ctx->device);
+  return set_error(DMUON_ERR_INVALID_ARG, buf);
+}
+
+template <class T>
+bool same_bytes(const std::vector<uint8_t>& v, const T* a, int n) {
+  return v.size() == sizeof(T) * static_cast<size_t>(n) && memcmp(v.data(), a, v.size()) == 0;
+}
+
+template <class T>
+void keep_bytes(std::vector<uint8_t>& v, const T* a, int n) {
+  v.assign(reinterpret_cast<const uint8_t*>(a), reinterpret_cast<const uint8_t*>(a) + sizeof(T) * static_cast<size_t>(n));
+}
+
+int check_matrices_reachable(dmuon_context* ctx, std::vector<uint8_t>& checked, const dmuon_matrix* mats,
+                             int n) {
+  if (same_bytes(checked, mats, n)) return DMUON_OK;
+  checked.clear();
+  for (int i = 0; i < n; ++i) {
+    int st;
+    if ((st = check_reachable(ctx, mats[i].master, "master", i)) != DMUON_OK) return st;
+    if ((st = check_reachable(ctx, mats[i].momentum, "momentum", i)) != DMUON_OK) return st;
+    if ((st = check_reachable(ctx, mats[i].grad, "grad", i)) != DMUON_OK) return st;
+    if ((st = check_reachable(ctx, mats[i].param_bf16, "param", i)) != DMUON_OK) return st;
+  }
+  keep_bytes(checked, mats, n);
+  return DMUON_OK;
+}
+
+int check_vectors_reachable(dmuon_context* ctx, const dmuon_vector* ts, int n) {
+  if (same_bytes(ctx->checked_vecs, ts, n)) return DMUON_OK;
+  ctx->checked_vecs.clear();
+  for (int i = 0; i < n; ++i) {
+    if (ts[i].numel == 0) continue;
+    int st;
+    if ((st = check_reachable(ctx, ts[i].master, "master", i)) != DMUON_OK) return st;
+    if ((st = check_reachable(ctx, ts[i].exp_avg, "exp_avg", i)) != DMUON_OK) return st;
+    if ((st = check_reachable(ctx, ts[i].exp_avg_sq, "exp_avg_sq", i)) != DMUON_OK) return st;
+    if ((st = check_reachable(ctx, ts[i].grad, "grad", i)) != DMUON_OK) return st;
+    if ((st = check_reachable(ctx, ts[i].param_bf16, "param", i)) != DMUON_OK) return st;
+  }
+  keep_bytes(ctx->checked_vecs, ts, n);
   return DMUON_OK;
 }
 
@@ -454,9 +578,8 @@ int build_phase_tiles(const std::vector<NsProblem>& probs, int geometry, int slo
   return upload(out.cta_begin, counts);
 }
 
-int build_muon_plan(dmuon_context* ctx, const dmuon_matrix* mats, int n, bool fp32,
+int build_muon_plan(dmuon_context* ctx, MuonPlan& P, const dmuon_matrix* mats, int n, bool fp32,
                     const std::string& key) {
-  MuonPlan& P = ctx->plan;
   P.release();
   P.fp32 = fp32;
 
@@ -512,6 +635,7 @@ int build_muon_plan(dmuon_context* ctx, const dmuon_matrix* mats, int n, bool fp
   P.ws_bytes = std::max<size_t>(off, 1024);
   if (ctx->ws.bytes < P.ws_bytes) {
     ctx->ws.release();
+    ctx->ws_epoch++;
     int st = dev_alloc(ctx->ws, P.ws_bytes);
     if (st != DMUON_OK) return st;
   }
@@ -736,6 +860,7 @@ int build_muon_plan(dmuon_context* ctx, const dmuon_matrix* mats, int n, bool fp
     }
   }
   P.key = key;
+  P.ws_epoch = ctx->ws_epoch;
   return DMUON_OK;
 }
 
@@ -763,65 +888,9 @@ int timed_launch(dmuon_context* ctx, int kind, cudaStream_t s, F&& launch) {
   return DMUON_OK;
 }
 
-}  // namespace
-}  // namespace dmuon
-
-using namespace dmuon;
-
-extern "C" {
-
-const char* dmuon_status_string(int status) {
-  switch (status) {
-    case DMUON_OK: return "ok";
-    case DMUON_ERR_INVALID_ARG: return "invalid argument";
-    case DMUON_ERR_RANK_LT2: return "Muon tensor of rank < 2";
-    case DMUON_ERR_SHAPE: return "unsupported shape";
-    case DMUON_ERR_DTYPE: return "unsupported dtype";
-    case DMUON_ERR_CUDA: return "CUDA error";
-    case DMUON_ERR_TIMEOUT: return "device-side wait timed out";
-    case DMUON_ERR_NOMEM: return "out of memory";
-    case DMUON_ERR_UNSUPPORTED: return "unsupported device";
-    default: return "unknown status";
-  }
-}
-
-const char* dmuon_last_error(void) { return g_last_error.c_str(); }
-
-int dmuon_context_create(dmuon_context** out, int32_t device) {
-  clear_error();
-  if (!out || device < 0) return set_error(DMUON_ERR_INVALID_ARG, "context_create: null out or negative device");
-  dmuon_context* c = new (std::nothrow) dmuon_context();
-  if (!c) return set_error(DMUON_ERR_NOMEM, "context_create: host allocation failed");
-  c->device = device;
-  *out = c;
-  return DMUON_OK;
-}
-
-int dmuon_context_destroy(dmuon_context* ctx) {
-  clear_error();
-  if (!ctx) return DMUON_OK;
-  if (ctx->dev_ready) {
-    DeviceGuard g(ctx->device);
-    cudaDeviceSynchronize();
-    ctx->plan.release();
-    ctx->adam.release();
-    ctx->slice_table.release();
-    ctx->vec_table.release();
-    ctx->prof.release();
-    ctx->ws.release();
-    ctx->err.release();
-  }
-  delete ctx;
-  return DMUON_OK;
-}
-
-int64_t dmuon_kernel_launches(const dmuon_context* ctx) { return ctx ? ctx->launches : -1; }
-
-int dmuon_muon_step(dmuon_context* ctx, const dmuon_matrix* mats, int32_t n, float lr,
-                    float momentum, float wd, int32_t ns_steps, float a, float b, float c,
-                    uint32_t flags, void* stream) {
-  clear_error();
-  if (!ctx) return set_error(DMUON_ERR_INVALID_ARG, "muon_step: null context");
+// Argument checks of a Muon step (host only, before any CUDA call).
+int validate_muon_call(const dmuon_matrix* mats, int32_t n, float lr, float momentum, float wd,
+                       int32_t ns_steps, float a, float b, float c, uint32_t flags) {
   if (n < 0 || (n > 0 && !mats)) return set_error(DMUON_ERR_INVALID_ARG, "muon_step: bad tensor list");
   if (!finite(lr) || !finite(momentum) || !finite(wd) || !finite(a) || !finite(b) || !finite(c))
     return set_error(DMUON_ERR_INVALID_ARG, "muon_step: non-finite hyper-parameter");
@@ -832,22 +901,65 @@ int dmuon_muon_step(dmuon_context* ctx, const dmuon_matrix* mats, int32_t n, flo
     int st = validate_matrix(mats[i], i);
     if (st != DMUON_OK) return st;
   }
-  if (n == 0) return DMUON_OK;
+  return DMUON_OK;
+}
 
-  DeviceGuard guard(ctx->device);
-  int st = ensure_device(ctx);
-  if (st != DMUON_OK) return st;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const bool fp32 = (flags & DMUON_FLAG_FP32_NS) != 0;
-  const std::string key = plan_key(mats, n, fp32);
-  MuonPlan& P = ctx->plan;
-  if (key != P.key) {
-    st = build_muon_plan(ctx, mats, n, fp32, key);
-    if (st != DMUON_OK) {
-      P.release();
-      return st;
+// Argument checks of an AdamW step (host only, before any CUDA call).
+int validate_adamw_call(const dmuon_vector* ts, int32_t n, float lr, float beta1, float beta2, float eps,
+                        float wd, int64_t step) {
+  if (n < 0 || (n > 0 && !ts)) return set_error(DMUON_ERR_INVALID_ARG, "adamw_step: bad tensor list");
+  if (!finite(lr) || !finite(wd) || !finite(eps) || eps < 0.f || !(beta1 >= 0.f && beta1 < 1.f) ||
+      !(beta2 >= 0.f && beta2 < 1.f))
+    return set_error(DMUON_ERR_INVALID_ARG, "adamw_step: bad hyper-parameter");
+  if (step < 1) return set_error(DMUON_ERR_INVALID_ARG, "adamw_step: step counter must be >= 1");
+  for (int i = 0; i < n; ++i) {
+    const dmuon_vector& V = ts[i];
+    char buf[120];
+    if (V.numel < 0 || V.numel > (int64_t(1) << 40)) {
+      snprintf(buf, sizeof buf, "adamw tensor %d: numel %lld", i, (long long)V.numel);
+      return set_error(DMUON_ERR_SHAPE, buf);
+    }
+    if (V.numel > 0 && (!V.master || !V.exp_avg || !V.exp_avg_sq || !V.grad)) {
+      snprintf(buf, sizeof buf, "adamw tensor %d: null pointer", i);
+      return set_error(DMUON_ERR_INVALID_ARG, buf);
+    }
+    if (V.grad_dtype != DMUON_DTYPE_F32 && V.grad_dtype != DMUON_DTYPE_BF16) {
+      snprintf(buf, sizeof buf, "adamw tensor %d: grad dtype %d", i, V.grad_dtype);
+      return set_error(DMUON_ERR_DTYPE, buf);
     }
   }
+  return DMUON_OK;
+}
+
+MuonSlot* get_slot(dmuon_context* ctx, size_t i) {
+  while (ctx->slots.size() <= i) {
+    MuonSlot* m = new (std::nothrow) MuonSlot();
+    if (!m) return nullptr;
+    ctx->slots.emplace_back(m);
+  }
+  return ctx->slots[i].get();
+}
+
+// The slot's plan for this tensor list, rebuilt when the shapes changed or
+// the workspace was reallocated since it was built.
+int prepare_slot(dmuon_context* ctx, MuonSlot& S, const dmuon_matrix* mats, int n, bool fp32) {
+  const std::string key = plan_key(mats, n, fp32);
+  if (key == S.plan.key && S.plan.ws_epoch == ctx->ws_epoch) return DMUON_OK;
+  int st = build_muon_plan(ctx, S.plan, mats, n, fp32, key);
+  if (st != DMUON_OK) S.plan.release();
+  return st;
+}
+
+// One Muon step of a validated, non-empty tensor list on the current device.
+int muon_step_impl(dmuon_context* ctx, MuonSlot& S, const dmuon_matrix* mats, int n, float lr,
+                   float momentum, float wd, int32_t ns_steps, float a, float b, float c,
+                   uint32_t flags, cudaStream_t s) {
+  int st = check_matrices_reachable(ctx, S.checked, mats, n);
+  if (st != DMUON_OK) return st;
+  const bool fp32 = (flags & DMUON_FLAG_FP32_NS) != 0;
+  st = prepare_slot(ctx, S, mats, n, fp32);
+  if (st != DMUON_OK) return st;
+  MuonPlan& P = S.plan;
   uint8_t* ws = static_cast<uint8_t*>(ctx->ws.p);
 
   // Per-call pointer table.
@@ -877,9 +989,9 @@ int dmuon_muon_step(dmuon_context* ctx, const dmuon_matrix* mats, int32_t n, flo
     D.chunk_begin = P.slice_chunk_begin[i];
     D.chunk_end = P.slice_chunk_end[i];
   }
-  st = ctx->slice_table.put(table.data(), table.size() * sizeof(SliceDesc), s);
+  st = S.table.put(table.data(), table.size() * sizeof(SliceDesc), s);
   if (st != DMUON_OK) return st;
-  const SliceDesc* d_slices = static_cast<const SliceDesc*>(ctx->slice_table.dev.p);
+  const SliceDesc* d_slices = static_cast<const SliceDesc*>(S.table.dev.p);
   const Chunk* d_chunks = static_cast<const Chunk*>(P.chunks_dev.p);
   float* partials = static_cast<float*>(P.partials.p);
   float* inv_norm = static_cast<float*>(P.inv_norm.p);
@@ -951,36 +1063,12 @@ int dmuon_muon_step(dmuon_context* ctx, const dmuon_matrix* mats, int32_t n, flo
   });
 }
 
-int dmuon_adamw_step(dmuon_context* ctx, const dmuon_vector* ts, int32_t n, float lr, float beta1,
-                     float beta2, float eps, float wd, int64_t step, void* stream) {
-  clear_error();
-  if (!ctx) return set_error(DMUON_ERR_INVALID_ARG, "adamw_step: null context");
-  if (n < 0 || (n > 0 && !ts)) return set_error(DMUON_ERR_INVALID_ARG, "adamw_step: bad tensor list");
-  if (!finite(lr) || !finite(wd) || !finite(eps) || eps < 0.f || !(beta1 >= 0.f && beta1 < 1.f) ||
-      !(beta2 >= 0.f && beta2 < 1.f))
-    return set_error(DMUON_ERR_INVALID_ARG, "adamw_step: bad hyper-parameter");
-  if (step < 1) return set_error(DMUON_ERR_INVALID_ARG, "adamw_step: step counter must be >= 1");
-  for (int i = 0; i < n; ++i) {
-    const dmuon_vector& V = ts[i];
-    char buf[120];
-    if (V.numel < 0 || V.numel > (int64_t(1) << 40)) {
-      snprintf(buf, sizeof buf, "adamw tensor %d: numel %lld", i, (long long)V.numel);
-      return set_error(DMUON_ERR_SHAPE, buf);
-    }
-    if (V.numel > 0 && (!V.master || !V.exp_avg || !V.exp_avg_sq || !V.grad)) {
-      snprintf(buf, sizeof buf, "adamw tensor %d: null pointer", i);
-      return set_error(DMUON_ERR_INVALID_ARG, buf);
-    }
-    if (V.grad_dtype != DMUON_DTYPE_F32 && V.grad_dtype != DMUON_DTYPE_BF16) {
-      snprintf(buf, sizeof buf, "adamw tensor %d: grad dtype %d", i, V.grad_dtype);
-      return set_error(DMUON_ERR_DTYPE, buf);
-    }
-  }
-  if (n == 0) return DMUON_OK;
-  DeviceGuard guard(ctx->device);
-  int st = ensure_device(ctx);
+
+// One AdamW step of a validated, non-empty tensor list on the current device.
+int adamw_step_impl(dmuon_context* ctx, const dmuon_vector* ts, int n, float lr, float beta1, float beta2,
+                    float eps, float wd, int64_t step, cudaStream_t s) {
+  int st = check_vectors_reachable(ctx, ts, n);
   if (st != DMUON_OK) return st;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
 
   std::string key;
   for (int i = 0; i < n; ++i) key += std::to_string(ts[i].numel) + ";";
@@ -1026,6 +1114,351 @@ int dmuon_adamw_step(dmuon_context* ctx, const dmuon_vector* ts, int32_t n, floa
                         lr, beta1, beta2, eps, wd, static_cast<float>(bc1),
                         static_cast<float>(std::sqrt(bc2)), s);
   });
+}
+
+
+// ------------------------------------------------------------ host pipeline
+// Id of the CUDA allocation holding `p` (0 when the driver does not know it).
+uint64_t buffer_id(const void* p) {
+  PointerAttrFn fn = get_pointer_attr_fn();
+  unsigned long long id = 0;
+  if (!fn || !p ||
+      fn(&id, CU_POINTER_ATTRIBUTE_BUFFER_ID, static_cast<CUdeviceptr>(reinterpret_cast<uintptr_t>(p))) != CUDA_SUCCESS)
+    return 0;
+  return id;
+}
+
+// Append a copy, merged into the previous one when its source and its
+// destination both continue the previous ones inside the same allocations
+// (one copy may not span two allocations, however adjacent).
+void add_run(std::vector<CopyRun>& runs, void* dst, const void* src, size_t bytes) {
+  if (bytes == 0) return;
+  const uint64_t did = buffer_id(dst), sid = buffer_id(src);
+  if (!runs.empty()) {
+    CopyRun& r = runs.back();
+    if (static_cast<uint8_t*>(r.dst) + r.bytes == dst && static_cast<const uint8_t*>(r.src) + r.bytes == src &&
+        did != 0 && sid != 0 && did == r.dst_id && sid == r.src_id) {
+      r.bytes += bytes;
+      return;
+    }
+  }
+  runs.push_back({dst, src, bytes, did, sid});
+}
+
+int enqueue_runs(const std::vector<CopyRun>& runs, cudaMemcpyKind kind, cudaStream_t st) {
+  for (const CopyRun& r : runs) DM_CUDA(cudaMemcpyAsync(r.dst, r.src, r.bytes, kind, st));
+  return DMUON_OK;
+}
+
+int check_page_locked(const void* p, const char* what, int idx) {
+  if (!p) return DMUON_OK;
+  cudaPointerAttributes at;
+  memset(&at, 0, sizeof at);
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();
+    at.type = cudaMemoryTypeUnregistered;
+  }
+  if (at.type == cudaMemoryTypeHost) return DMUON_OK;
+  char buf[160];
+  snprintf(buf, sizeof buf, "tensor %d: %s is not page-locked host memory", idx, what);
+  return set_error(DMUON_ERR_INVALID_ARG, buf);
+}
+
+int ensure_events(dmuon_context* ctx, size_t count) {
+  while (ctx->events.size() < count) {
+    cudaEvent_t e = nullptr;
+    DM_CUDA(cudaEventCreateWithFlags(&e, cudaEventDisableTiming));
+    ctx->events.push_back(e);
+  }
+  return DMUON_OK;
+}
+
+int64_t matrix_numel(const dmuon_matrix& M) {
+  int64_t k = 1;
+  for (int d = 0; d < M.rank; ++d) k *= M.shape[d];
+  return k;
+}
+
+// Consecutive groups of about equal Newton-Schulz work (element count when
+// there are no iterations), every group non-empty.
+std::vector<std::pair<int, int>> split_groups(const dmuon_matrix* mats, int n, int groups, int ns_steps) {
+  std::vector<double> cost(static_cast<size_t>(n));
+  double total = 0.0;
+  for (int i = 0; i < n; ++i) {
+    const dmuon_matrix& M = mats[i];
+    const double m = double(M.shape[M.rank - 2]), q0 = double(M.shape[M.rank - 1]);
+    const double p = std::min(m, q0), q = std::max(m, q0);
+    const double lead = double(matrix_numel(M)) / (m * q0);
+    cost[static_cast<size_t>(i)] = ns_steps > 0 ? lead * (4.0 * p * p * q + 2.0 * p * p * p) : lead * m * q0;
+    total += cost[static_cast<size_t>(i)];
+  }
+  std::vector<std::pair<int, int>> out;
+  int start = 0;
+  double acc = 0.0;
+  for (int i = 0; i < n; ++i) {
+    acc += cost[static_cast<size_t>(i)];
+    const int closed = static_cast<int>(out.size());
+    if (closed < groups - 1 && i + 1 < n && acc >= total * double(closed + 1) / double(groups)) {
+      out.push_back({start, i + 1});
+      start = i + 1;
+    }
+  }
+  if (start < n) out.push_back({start, n});
+  return out;
+}
+
+}  // namespace
+}  // namespace dmuon
+
+using namespace dmuon;
+
+extern "C" {
+
+const char* dmuon_status_string(int status) {
+  switch (status) {
+    case DMUON_OK: return "ok";
+    case DMUON_ERR_INVALID_ARG: return "invalid argument";
+    case DMUON_ERR_RANK_LT2: return "Muon tensor of rank < 2";
+    case DMUON_ERR_SHAPE: return "unsupported shape";
+    case DMUON_ERR_DTYPE: return "unsupported dtype";
+    case DMUON_ERR_CUDA: return "CUDA error";
+    case DMUON_ERR_TIMEOUT: return "device-side wait timed out";
+    case DMUON_ERR_NOMEM: return "out of memory";
+    case DMUON_ERR_UNSUPPORTED: return "unsupported device";
+    default: return "unknown status";
+  }
+}
+
+const char* dmuon_last_error(void) { return g_last_error.c_str(); }
+
+int dmuon_context_create(dmuon_context** out, int32_t device) {
+  clear_error();
+  if (!out || device < 0) return set_error(DMUON_ERR_INVALID_ARG, "context_create: null out or negative device");
+  dmuon_context* c = new (std::nothrow) dmuon_context();
+  if (!c) return set_error(DMUON_ERR_NOMEM, "context_create: host allocation failed");
+  c->device = device;
+  *out = c;
+  return DMUON_OK;
+}
+
+int dmuon_context_destroy(dmuon_context* ctx) {
+  clear_error();
+  if (!ctx) return DMUON_OK;
+  if (ctx->dev_ready) {
+    DeviceGuard g(ctx->device);
+    cudaDeviceSynchronize();
+    for (auto& sl : ctx->slots) sl->release();
+    ctx->slots.clear();
+    ctx->adam.release();
+    ctx->vec_table.release();
+    for (cudaEvent_t e : ctx->events) cudaEventDestroy(e);
+    ctx->events.clear();
+    if (ctx->h2d) cudaStreamDestroy(ctx->h2d);
+    if (ctx->d2h) cudaStreamDestroy(ctx->d2h);
+    ctx->h2d = ctx->d2h = nullptr;
+    ctx->prof.release();
+    ctx->ws.release();
+    ctx->err.release();
+  }
+  delete ctx;
+  return DMUON_OK;
+}
+
+int64_t dmuon_kernel_launches(const dmuon_context* ctx) { return ctx ? ctx->launches : -1; }
+
+int dmuon_muon_step(dmuon_context* ctx, const dmuon_matrix* mats, int32_t n, float lr,
+                    float momentum, float wd, int32_t ns_steps, float a, float b, float c,
+                    uint32_t flags, void* stream) {
+  clear_error();
+  if (!ctx) return set_error(DMUON_ERR_INVALID_ARG, "muon_step: null context");
+  int st = validate_muon_call(mats, n, lr, momentum, wd, ns_steps, a, b, c, flags);
+  if (st != DMUON_OK || n == 0) return st;
+  DeviceGuard guard(ctx->device);
+  st = ensure_device(ctx);
+  if (st != DMUON_OK) return st;
+  MuonSlot* S = get_slot(ctx, 0);
+  if (!S) return set_error(DMUON_ERR_NOMEM, "muon_step: host allocation failed");
+  return muon_step_impl(ctx, *S, mats, n, lr, momentum, wd, ns_steps, a, b, c, flags,
+                        static_cast<cudaStream_t>(stream));
+}
+
+int dmuon_adamw_step(dmuon_context* ctx, const dmuon_vector* ts, int32_t n, float lr, float beta1,
+                     float beta2, float eps, float wd, int64_t step, void* stream) {
+  clear_error();
+  if (!ctx) return set_error(DMUON_ERR_INVALID_ARG, "adamw_step: null context");
+  int st = validate_adamw_call(ts, n, lr, beta1, beta2, eps, wd, step);
+  if (st != DMUON_OK || n == 0) return st;
+  DeviceGuard guard(ctx->device);
+  st = ensure_device(ctx);
+  if (st != DMUON_OK) return st;
+  return adamw_step_impl(ctx, ts, n, lr, beta1, beta2, eps, wd, step, static_cast<cudaStream_t>(stream));
+}
+
+int dmuon_step_host(dmuon_context* ctx, const dmuon_matrix* mats, const dmuon_host_io* mat_io, int32_t n_mats,
+                    const dmuon_muon_hparams* muon, const dmuon_vector* vecs, const dmuon_host_io* vec_io,
+                    int32_t n_vecs, const dmuon_adamw_hparams* adamw, int32_t n_groups, void* stream) {
+  clear_error();
+  if (!ctx) return set_error(DMUON_ERR_INVALID_ARG, "step_host: null context");
+  if (n_mats < 0 || n_vecs < 0 || (n_mats > 0 && (!mats || !mat_io || !muon)) ||
+      (n_vecs > 0 && (!vecs || !vec_io || !adamw)))
+    return set_error(DMUON_ERR_INVALID_ARG, "step_host: bad tensor list or missing hyper-parameters");
+  if (n_groups < 1 || n_groups > 64) return set_error(DMUON_ERR_INVALID_ARG, "step_host: n_groups outside [1, 64]");
+  int st;
+  if (n_mats > 0) {
+    st = validate_muon_call(mats, n_mats, muon->lr, muon->momentum, muon->wd, muon->ns_steps, muon->a, muon->b,
+                            muon->c, muon->flags);
+    if (st != DMUON_OK) return st;
+  }
+  if (n_vecs > 0) {
+    st = validate_adamw_call(vecs, n_vecs, adamw->lr, adamw->beta1, adamw->beta2, adamw->eps, adamw->wd,
+                             adamw->step);
+    if (st != DMUON_OK) return st;
+  }
+  char buf[160];
+  for (int i = 0; i < n_mats; ++i) {
+    if (!mat_io[i].grad_host || (mat_io[i].param_host && !mats[i].param_bf16)) {
+      snprintf(buf, sizeof buf, "step_host: Muon tensor %d: null grad_host, or param_host without param_bf16", i);
+      return set_error(DMUON_ERR_INVALID_ARG, buf);
+    }
+  }
+  for (int i = 0; i < n_vecs; ++i) {
+    if (vecs[i].numel > 0 && (!vec_io[i].grad_host || (vec_io[i].param_host && !vecs[i].param_bf16))) {
+      snprintf(buf, sizeof buf, "step_host: AdamW tensor %d: null grad_host, or param_host without param_bf16", i);
+      return set_error(DMUON_ERR_INVALID_ARG, buf);
+    }
+  }
+  if (n_mats == 0 && n_vecs == 0) return DMUON_OK;
+
+  DeviceGuard guard(ctx->device);
+  st = ensure_device(ctx);
+  if (st != DMUON_OK) return st;
+  if (!ctx->h2d) DM_CUDA(cudaStreamCreateWithFlags(&ctx->h2d, cudaStreamNonBlocking));
+  if (!ctx->d2h) DM_CUDA(cudaStreamCreateWithFlags(&ctx->d2h, cudaStreamNonBlocking));
+  // Groups and copy lists, rebuilt (and the host buffers checked) only when
+  // the descriptor arrays change.
+  HostPlan& H = ctx->host;
+  {
+    std::vector<uint8_t> key, part;
+    auto append = [&](const std::vector<uint8_t>& b) { key.insert(key.end(), b.begin(), b.end()); };
+    keep_bytes(part, mats, n_mats);
+    append(part);
+    keep_bytes(part, mat_io, n_mats);
+    append(part);
+    keep_bytes(part, vecs, n_vecs);
+    append(part);
+    keep_bytes(part, vec_io, n_vecs);
+    append(part);
+    const int32_t extra[3] = {n_mats, n_groups, n_mats > 0 && muon->ns_steps > 0 ? 1 : 0};
+    keep_bytes(part, extra, 3);
+    append(part);
+    if (key != H.key) {
+      H = HostPlan();
+      for (int i = 0; i < n_mats; ++i) {
+        if ((st = check_page_locked(mat_io[i].grad_host, "grad_host", i)) != DMUON_OK) return st;
+        if ((st = check_page_locked(mat_io[i].param_host, "param_host", i)) != DMUON_OK) return st;
+      }
+      for (int i = 0; i < n_vecs; ++i) {
+        if (vecs[i].numel == 0) continue;
+        if ((st = check_page_locked(vec_io[i].grad_host, "grad_host", i)) != DMUON_OK) return st;
+        if ((st = check_page_locked(vec_io[i].param_host, "param_host", i)) != DMUON_OK) return st;
+      }
+      H.groups = split_groups(mats, n_mats, n_groups, n_mats > 0 ? muon->ns_steps : 0);
+      const size_t G = H.groups.size();
+      H.in.resize(G);
+      H.out.resize(G);
+      auto grad_bytes = [](int64_t numel, int32_t dtype) {
+        return static_cast<size_t>(numel) * (dtype == DMUON_DTYPE_BF16 ? 2 : 4);
+      };
+      for (size_t g = 0; g < G; ++g)
+        for (int i = H.groups[g].first; i < H.groups[g].second; ++i) {
+          const int64_t numel = matrix_numel(mats[i]);
+          add_run(H.in[g], const_cast<void*>(mats[i].grad), mat_io[i].grad_host, grad_bytes(numel, mats[i].grad_dtype));
+          if (mat_io[i].param_host)
+            add_run(H.out[g], mat_io[i].param_host, mats[i].param_bf16, static_cast<size_t>(numel) * 2);
+        }
+      for (int i = 0; i < n_vecs; ++i) {
+        if (vecs[i].numel == 0) continue;
+        add_run(H.a_in, const_cast<void*>(vecs[i].grad), vec_io[i].grad_host,
+                grad_bytes(vecs[i].numel, vecs[i].grad_dtype));
+        if (vec_io[i].param_host)
+          add_run(H.a_out, vec_io[i].param_host, vecs[i].param_bf16, static_cast<size_t>(vecs[i].numel) * 2);
+      }
+      H.key.swap(key);
+    }
+  }
+  const auto& groups = H.groups;
+  const int G = static_cast<int>(groups.size());
+  enum { kStart, kAdamIn, kAdamDone, kEndH2d, kEndD2h, kFixed };
+  st = ensure_events(ctx, kFixed + 2 * static_cast<size_t>(G));
+  if (st != DMUON_OK) return st;
+  auto ev = [&](int i) { return ctx->events[static_cast<size_t>(i)]; };
+  auto ev_in = [&](int g) { return ev(kFixed + g); };
+  auto ev_done = [&](int g) { return ev(kFixed + G + g); };
+
+  // Plans of every group before anything is enqueued: a plan that grows the
+  // workspace makes the earlier ones stale, so repeat until all are current.
+  const bool fp32 = n_mats > 0 && (muon->flags & DMUON_FLAG_FP32_NS) != 0;
+  std::vector<MuonSlot*> slot(static_cast<size_t>(G));
+  for (int pass = 0; pass < 3; ++pass) {
+    bool all_current = true;
+    for (int g = 0; g < G; ++g) {
+      slot[static_cast<size_t>(g)] = get_slot(ctx, static_cast<size_t>(g) + 1);
+      if (!slot[static_cast<size_t>(g)]) return set_error(DMUON_ERR_NOMEM, "step_host: host allocation failed");
+      st = prepare_slot(ctx, *slot[static_cast<size_t>(g)], mats + groups[static_cast<size_t>(g)].first,
+                        groups[static_cast<size_t>(g)].second - groups[static_cast<size_t>(g)].first, fp32);
+      if (st != DMUON_OK) return st;
+    }
+    for (int g = 0; g < G; ++g) all_current = all_current && slot[static_cast<size_t>(g)]->plan.ws_epoch == ctx->ws_epoch;
+    if (all_current) break;
+  }
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  DM_CUDA(cudaEventRecord(ev(kStart), s));
+  DM_CUDA(cudaStreamWaitEvent(ctx->h2d, ev(kStart), 0));
+  DM_CUDA(cudaStreamWaitEvent(ctx->d2h, ev(kStart), 0));
+  // Whatever happens below, `stream` ends up ordered after both copy streams.
+  auto join = [&](int status) {
+    if (cudaEventRecord(ev(kEndH2d), ctx->h2d) != cudaSuccess || cudaEventRecord(ev(kEndD2h), ctx->d2h) != cudaSuccess ||
+        cudaStreamWaitEvent(s, ev(kEndH2d), 0) != cudaSuccess || cudaStreamWaitEvent(s, ev(kEndD2h), 0) != cudaSuccess) {
+      if (status == DMUON_OK) return cuda_fail(cudaGetLastError(), "step_host: joining the copy streams");
+    }
+    return status;
+  };
+  // All gradient copies first, in the order the steps consume them.
+  for (int g = 0; g < G; ++g) {
+    if ((st = enqueue_runs(H.in[static_cast<size_t>(g)], cudaMemcpyHostToDevice, ctx->h2d)) != DMUON_OK) return join(st);
+    if (cudaEventRecord(ev_in(g), ctx->h2d) != cudaSuccess) return join(cuda_fail(cudaGetLastError(), "step_host"));
+    if (g == 0 && n_vecs > 0) {
+      if ((st = enqueue_runs(H.a_in, cudaMemcpyHostToDevice, ctx->h2d)) != DMUON_OK) return join(st);
+      if (cudaEventRecord(ev(kAdamIn), ctx->h2d) != cudaSuccess) return join(cuda_fail(cudaGetLastError(), "step_host"));
+    }
+  }
+  if (G == 0 && n_vecs > 0) {
+    if ((st = enqueue_runs(H.a_in, cudaMemcpyHostToDevice, ctx->h2d)) != DMUON_OK) return join(st);
+    if (cudaEventRecord(ev(kAdamIn), ctx->h2d) != cudaSuccess) return join(cuda_fail(cudaGetLastError(), "step_host"));
+  }
+  auto adam = [&]() {
+    if (cudaStreamWaitEvent(s, ev(kAdamIn), 0) != cudaSuccess) return cuda_fail(cudaGetLastError(), "step_host");
+    int r = adamw_step_impl(ctx, vecs, n_vecs, adamw->lr, adamw->beta1, adamw->beta2, adamw->eps, adamw->wd,
+                            adamw->step, s);
+    if (r != DMUON_OK) return r;
+    if (cudaEventRecord(ev(kAdamDone), s) != cudaSuccess || cudaStreamWaitEvent(ctx->d2h, ev(kAdamDone), 0) != cudaSuccess)
+      return cuda_fail(cudaGetLastError(), "step_host");
+    return enqueue_runs(H.a_out, cudaMemcpyDeviceToHost, ctx->d2h);
+  };
+  for (int g = 0; g < G; ++g) {
+    const int b = groups[static_cast<size_t>(g)].first, e = groups[static_cast<size_t>(g)].second;
+    if (cudaStreamWaitEvent(s, ev_in(g), 0) != cudaSuccess) return join(cuda_fail(cudaGetLastError(), "step_host"));
+    st = muon_step_impl(ctx, *slot[static_cast<size_t>(g)], mats + b, e - b, muon->lr, muon->momentum, muon->wd,
+                        muon->ns_steps, muon->a, muon->b, muon->c, muon->flags, s);
+    if (st != DMUON_OK) return join(st);
+    if (cudaEventRecord(ev_done(g), s) != cudaSuccess || cudaStreamWaitEvent(ctx->d2h, ev_done(g), 0) != cudaSuccess)
+      return join(cuda_fail(cudaGetLastError(), "step_host"));
+    if ((st = enqueue_runs(H.out[static_cast<size_t>(g)], cudaMemcpyDeviceToHost, ctx->d2h)) != DMUON_OK) return join(st);
+    if (g == 0 && n_vecs > 0 && (st = adam()) != DMUON_OK) return join(st);
+  }
+  if (G == 0 && n_vecs > 0 && (st = adam()) != DMUON_OK) return join(st);
+  return join(DMUON_OK);
 }
 
 int dmuon_sync(dmuon_context* ctx, void* stream) {

@@ -110,6 +110,59 @@ class OwnerStep:
         self._ev_join.record(self._side)
         main.wait_event(self._ev_join)
 
+    # ------------------------------------------------- host-side buffers
+    def set_host_io(self, grads_host, params_host=None, v_grads_host=None, v_params_host=None):
+        """Register page-locked CPU tensors for ``step_host``: per Muon tensor
+        a gradient (same shape and dtype as its device grad) and optionally a
+        bf16 parameter; the same per AdamW tensor."""
+        def check(t, name, like, dtype):
+            if not isinstance(t, torch.Tensor) or t.is_cuda or not t.is_pinned():
+                raise TypeError(f"{name} must be a page-locked CPU tensor")
+            if t.dtype != dtype or not t.is_contiguous() or t.numel() != like.numel():
+                raise ValueError(f"{name}: expected a contiguous {dtype} tensor of {like.numel()} elements")
+
+        def ios(host_g, host_p, grads, params, tag):
+            host_p = host_p if host_p is not None else [None] * len(host_g)
+            if len(host_g) != len(grads) or len(host_p) != len(grads):
+                raise ValueError(f"{tag}: one host buffer per registered tensor")
+            out = []
+            for i, (hg, hp) in enumerate(zip(host_g, host_p)):
+                check(hg, f"{tag} grad_host[{i}]", grads[i], grads[i].dtype)
+                if hp is not None:
+                    if params[i] is None:
+                        raise ValueError(f"{tag} param_host[{i}] given but no device param registered")
+                    check(hp, f"{tag} param_host[{i}]", grads[i], torch.bfloat16)
+                out.append(capi.DmuonHostIO(hg.data_ptr(), None if hp is None else hp.data_ptr()))
+            return capi.descriptor_array(out, capi.DmuonHostIO)
+
+        if self._mats is None:
+            raise RuntimeError("set_muon() first")
+        self._mat_io = ios(grads_host, params_host, self._keep[2], self._keep[3], "muon")
+        if v_grads_host is not None:
+            if self._vecs is None:
+                raise RuntimeError("set_adamw() first")
+            self._vec_io = ios(v_grads_host, v_params_host, self._keep_adam[3], self._keep_adam[4], "adamw")
+        else:
+            self._vec_io = None
+        self._keep_host = [grads_host, params_host, v_grads_host, v_params_host]
+
+    def step_host(self, muon, adamw=None, n_groups=8, stream=None):
+        """One step from host gradients to host bf16 parameters
+        (``dmuon_step_host``): the registered host gradients are copied in,
+        every tensor steps, the parameters are copied out, with the copies of
+        ``n_groups`` groups overlapping the compute of the others.  ``muon`` /
+        ``adamw``: keyword dicts as for muon_step / adamw_step."""
+        if getattr(self, "_mat_io", None) is None:
+            raise RuntimeError("set_host_io() first")
+        mh = capi.muon_hparams(**muon)
+        use_adam = adamw is not None and self._vecs is not None and self._vec_io is not None
+        ah = capi.adamw_hparams(**adamw) if use_adam else None
+        capi._check(capi.load_library().dmuon_step_host(
+            self.ctx, self._mats, self._mat_io, self._n_mats, capi.ctypes.byref(mh),
+            self._vecs if use_adam else None, self._vec_io if use_adam else None,
+            self._n_vecs if use_adam else 0, capi.ctypes.byref(ah) if use_adam else None,
+            int(n_groups), capi._stream_handle(stream)))
+
     # ------------------------------------------------------------ misc
     def sync(self, stream=None):
         capi.dmuon_sync(self.ctx, stream)

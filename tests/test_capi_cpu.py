@@ -185,3 +185,36 @@ def test_layered_lpt_llama_owner_partition(mos):
     assert list(got[0]) == want[0] and list(got[1]) == want[1]
     with pytest.raises(mos.DmuonError):
         mos.dmuon_lpt_assign_layered([1, -2], [0, 0], 2)
+
+
+def test_step_host_host_validation_without_gpu(mos):
+    capi = mos.capi
+    hp = capi.muon_hparams(0.02, 0.95, 0.01)
+    ctx = mos.dmuon_context_create(0)
+    try:
+        d = capi.DmuonMatrix()
+        d.rank = 2
+        d.shape[0], d.shape[1] = 8, 16
+        d.master = d.momentum = d.grad = 256
+        d.grad_dtype = capi.DMUON_DTYPE_BF16
+        io = capi.DmuonHostIO(512, None)
+        for groups in (0, 65):
+            with pytest.raises(mos.DmuonError) as e:
+                capi.dmuon_step_host(ctx, [d], [io], hp, n_groups=groups, stream=0)
+            assert e.value.status == capi.DMUON_ERR_INVALID_ARG
+        with pytest.raises(mos.DmuonError) as e:  # hyper-parameters missing
+            capi.dmuon_step_host(ctx, [d], [io], None, stream=0)
+        assert e.value.status == capi.DMUON_ERR_INVALID_ARG
+        with pytest.raises(mos.DmuonError) as e:  # no host gradient
+            capi.dmuon_step_host(ctx, [d], [capi.DmuonHostIO(None, None)], hp, stream=0)
+        assert e.value.status == capi.DMUON_ERR_INVALID_ARG
+        with pytest.raises(mos.DmuonError) as e:  # host parameter but no device parameter
+            capi.dmuon_step_host(ctx, [d], [capi.DmuonHostIO(512, 1024)], hp, stream=0)
+        assert e.value.status == capi.DMUON_ERR_INVALID_ARG
+        d.rank = 1
+        with pytest.raises(mos.DmuonError) as e:
+            capi.dmuon_step_host(ctx, [d], [io], hp, stream=0)
+        assert e.value.status == capi.DMUON_ERR_RANK_LT2
+        capi.dmuon_step_host(ctx, [], [], None, stream=0)  # nothing to do
+    finally:
+        mos.dmuon_context_destroy(ctx)
