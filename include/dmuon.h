@@ -353,6 +353,9 @@ DMUON_API int dmuon_selftest_wait_timeout(dmuon_context* ctx, int32_t timeout_us
  *   key 6: CTA-pair kernel keeps symmetric products as upper blocks only and
  *          reads them through transposed loads (1) or stores mirrored copies
  *          of off-diagonal blocks (0).
+ *   key 7: from the third Newton-Schulz iteration on, the a*X term is folded
+ *          into the polynomial matrix, X' = (a I + B) X, so the last product
+ *          reads no extra operand (1, default), or added in the epilogue (0).
  * Returns DMUON_ERR_INVALID_ARG for an unknown key.  Not thread-safe with
  * respect to concurrent steps.
  */

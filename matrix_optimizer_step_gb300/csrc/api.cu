@@ -46,6 +46,9 @@ static int g_tile_order = 1;
 static int g_tri = 1;
 void set_tc2_variant(int stages, int prefetch);
 static int g_tc2_stages_sel = 4, g_tc2_prefetch_sel = 1;
+// From the third iteration on (where X is read back in bf16 anyway), fold
+// the a*X term of the Combine into the Poly output: B + a I.  1 = on.
+static int g_fold_diag = 1;
 
 // ------------------------------------------------------------------ errors
 namespace {
@@ -1023,6 +1026,12 @@ int muon_step_impl(dmuon_context* ctx, MuonSlot& S, const dmuon_matrix* mats, in
         NsLaunch T = L;
         T.probs = static_cast<const NsProblem*>(P.probs[kind][variant].p);
         T.aux_f32 = ((it == 0 && kind != kGram) || (it == 1 && kind == kCombine)) ? 1 : 0;
+        if (g_fold_diag && it >= 2) {
+          // X' = a X + B X = (a I + B) X: the Poly adds a on B's diagonal and
+          // the Combine reads no aux.
+          if (kind == kPoly) T.diag = a;
+          if (kind == kCombine) T.a = 0.f;
+        }
         if (kind == kCombine && it == ns_steps - 1) {
           // The last Combine applies the update itself (no X store, no update pass).
           T.fuse_update = 1;
@@ -1538,6 +1547,10 @@ int dmuon_set_tuning(int32_t key, int32_t value) {
   if (key == 3) {
     g_tc2_stages_sel = (value == 5) ? 5 : 4;
     set_tc2_variant(g_tc2_stages_sel, g_tc2_prefetch_sel);
+    return DMUON_OK;
+  }
+  if (key == 7) {
+    g_fold_diag = value ? 1 : 0;
     return DMUON_OK;
   }
   if (key == 4) {

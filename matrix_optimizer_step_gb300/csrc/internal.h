@@ -132,6 +132,10 @@ struct NsLaunch {
   // CTA-pair kernel: symmetric outputs keep only their upper blocks (no
   // mirrored stores) and symmetric operands are read through NsProblem::tri.
   int32_t tri;
+  // Poly only: added to the diagonal of B, so that the Combine of the same
+  // iteration computes a X + B X as (a I + B) X without reading X as aux
+  // (that Combine then runs with a = 0).  0 = off.
+  float diag;
 };
 
 // ---- launch wrappers (each returns the cudaError_t of its launch) ----

@@ -38,6 +38,7 @@ __device__ __forceinline__ void ns_epilogue_tile(const NsLaunch& L, const NsProb
     alpha = g;
     beta = g * L.a;
   }
+  const float diag = (L.kind == kPoly) ? L.diag : 0.f;
   const int row = m0 + row_in_tile;
   const bool row_ok = row < P.M;
   uint16_t* out_row = reinterpret_cast<uint16_t*>(P.out) + static_cast<int64_t>(row) * P.ld_out;
@@ -162,6 +163,7 @@ __device__ __forceinline__ void ns_epilogue_tile(const NsLaunch& L, const NsProb
       for (int j = 0; j < 32; ++j) {
         v[j] = alpha * __uint_as_float(r[j]);
         if (beta != 0.f) v[j] = fmaf(beta, auxf[j], v[j]);
+        if (row == col0 + j) v[j] += diag;
       }
       uint4* dst = reinterpret_cast<uint4*>(out_row + col0);
 #pragma unroll
@@ -191,6 +193,7 @@ __device__ __forceinline__ void ns_epilogue_tile(const NsLaunch& L, const NsProb
         float v = alpha * __uint_as_float(r[j]);
         if (beta != 0.f)
           v = fmaf(beta, aux_f32 ? auxf_row[col0 + j] : bf16_bits_to_f32(aux_row[col0 + j]), v);
+        if (row == col0 + j) v += diag;
         if (fuse) {
           const float w = fmaf(-step, v, w_row[col0 + j] * decay);
           w_row[col0 + j] = w;
@@ -248,6 +251,7 @@ __device__ __forceinline__ void ns_epilogue_tile_staged(const NsLaunch& L, const
     alpha = g;
     beta = g * L.a;
   }
+  const float diag = (L.kind == kPoly) ? L.diag : 0.f;
   const int row = m0 + row_in_tile;
   const bool row_ok = row < P.M;
   const int warp_row0 = row - lane;
@@ -318,6 +322,7 @@ __device__ __forceinline__ void ns_epilogue_tile_staged(const NsLaunch& L, const
     for (int j = 0; j < 32; ++j) {
       v[j] = alpha * __uint_as_float(r[j]);
       if (need_aux) v[j] = fmaf(beta, auxf[j], v[j]);
+      if (row == col0 + j) v[j] += diag;
     }
     const uint32_t buf = stage_smem + (box_count & 1u) * 4096u;
     if ((cc & 1) == 0) {
