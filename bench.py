@@ -31,6 +31,7 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
+L2_BYTES = 129 * 1024 * 1024  # GB300 L2
 METRIC = "Muon step ms & NS TFLOP/s (% bf16 TC peak), Llama-3-8B-shaped matrix set"
 
 
@@ -254,7 +255,7 @@ def run_ours(args, wl, rank, world, local_rank):
             t_counter[0] += 1
             adam_kw = dict(lr=h["adam_lr"], beta1=h["beta1"], beta2=h["beta2"], eps=h["adam_eps"],
                            wd=h["adam_wd"], step=t_counter[0])
-        if args.overlap_adamw:
+        if not args.serial_adamw:
             step.step(muon_kw, adam_kw, stream=stream)
         else:
             step.muon_step(stream=stream, **muon_kw)
@@ -275,22 +276,41 @@ def run_ours(args, wl, rank, world, local_rank):
     step.profile(True)
     step.profile_read()
     launches0 = step.kernel_launches()
+    # State smaller than a few L2 sizes would stay cached from one step to
+    # the next: then every step is timed on its own and L2 is flushed (a
+    # write of twice its size) between steps, outside the timed spans.
+    state_bytes = sum(t.numel() * t.element_size() for t in mat.flats.values())
+    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev) if state_bytes < 4 * L2_BYTES else None
     barrier()
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
-        one_step()
-    e1.record(stream)
-    torch.cuda.synchronize()
+    if flush is None:
+        e0.record(stream)
+        for _ in range(args.steps):
+            one_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        total_ms = e0.elapsed_time(e1)
+    else:
+        total_ms = 0.0
+        for _ in range(args.steps):
+            flush.fill_(1)
+            e0.record(stream)
+            one_step()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            total_ms += e0.elapsed_time(e1)
     barrier()
     launches = step.kernel_launches() - launches0
     prof = step.profile_read()
     step.profile(False)
     clk = clocks.stop()
     step.sync(stream)
-    ms = reduce_max_over_ranks(e0.elapsed_time(e1) / args.steps, dist, dev)
+    ms = reduce_max_over_ranks(total_ms / args.steps, dist, dev)
+    l2_note = ("inputs larger than L2 (no flush needed)" if flush is None else
+               "L2 flushed between steps (each step timed on its own)")
+    del flush
 
     # ---------------- end to end: host grads in, host bf16 params out.
     # Through dmuon_step_host: every step copies this step's gradients in
@@ -338,6 +358,17 @@ def run_ours(args, wl, rank, world, local_rank):
     e2e_ms = reduce_max_over_ranks(x0.elapsed_time(x1) / e2e_steps, dist, dev)
     h2d = g_flat.numel() * g_flat.element_size()
     d2h = p_flat.numel() * p_flat.element_size()
+    # The host link's own rate in this run (one plain copy each way), which
+    # bounds e2e from below once the copies are the longer side.
+    link = {}
+    for name, fn, nbytes in (("h2d_gbs", lambda: g_flat.copy_(host_g, non_blocking=True), h2d),
+                             ("d2h_gbs", lambda: host_p.copy_(p_flat, non_blocking=True), d2h)):
+        torch.cuda.synchronize()
+        x0.record(stream)
+        fn()
+        x1.record(stream)
+        torch.cuda.synchronize()
+        link[name] = nbytes / (x0.elapsed_time(x1) / 1e3) / 1e9
     del host_g, host_p
 
     if rank != 0:
@@ -383,7 +414,8 @@ def run_ours(args, wl, rank, world, local_rank):
         "config": {"workload": _workload_desc(wl), "ns_steps": h["ns_steps"],
                    "ns_operands": "fp32 in NS mode" if h["fp32_ns"] else "bf16 operands, fp32 accumulate",
                    "state": "fp32 master/momentum/AdamW moments, bf16 grads and params",
-                   "l2": "inputs larger than L2 (no flush needed)", "parallelism": f"replicas x{world}"},
+                   "l2": l2_note, "parallelism": f"replicas x{world}",
+                   "adamw": "serial" if args.serial_adamw else "side stream beside the Muon step"},
         "ns_tflops_dense_count": ns_tflops,
         "ns_tflops_executed": ns_exec_tflops,
         "ns_tflop_per_step": {"dense_count": ns_flops / 1e12, "executed": ns_exec / 1e12},
@@ -401,7 +433,8 @@ def run_ours(args, wl, rank, world, local_rank):
         "gpu_launches": launches,
         "e2e": {"value": world * ns_flops / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "steps": e2e_steps, "api": "dmuon_step_host", "n_groups": args.e2e_groups},
+                "steps": e2e_steps, "api": "dmuon_step_host", "n_groups": args.e2e_groups,
+                "host_link": link},
         "clocks": clk,
     }
     if not args.no_cpu_baseline:
@@ -424,8 +457,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-groups", type=int, default=16,
                     help="groups of the host-buffer step (copies of one group overlap the others' compute)")
-    ap.add_argument("--overlap-adamw", action="store_true",
-                    help="run the AdamW step on a side stream beside the Muon step (OwnerStep.step)")
+    ap.add_argument("--serial-adamw", action="store_true",
+                    help="run the AdamW step after the Muon step on one stream instead of beside it on a "
+                         "side stream (OwnerStep.step, the default)")
     ap.add_argument("--tuning", action="append", default=[],
                     help="KEY=VALUE passed to dmuon_set_tuning before the run")
     args = ap.parse_args()
