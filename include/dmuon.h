@@ -356,6 +356,10 @@ DMUON_API int dmuon_selftest_wait_timeout(dmuon_context* ctx, int32_t timeout_us
  *   key 7: from the third Newton-Schulz iteration on, the a*X term is folded
  *          into the polynomial matrix, X' = (a I + B) X, so the last product
  *          reads no extra operand (1, default), or added in the epilogue (0).
+ *   key 8: CTA-pair kernel: a launch whose tiles average fewer than `value`
+ *          64-deep k-blocks drains its accumulators with 8 epilogue warps
+ *          instead of 4 (default 32; 0 = always 4, a large value = always 8
+ *          except for the fused update).
  * Returns DMUON_ERR_INVALID_ARG for an unknown key.  Not thread-safe with
  * respect to concurrent steps.
  */

@@ -49,6 +49,9 @@ static int g_tc2_stages_sel = 4, g_tc2_prefetch_sel = 1;
 // From the third iteration on (where X is read back in bf16 anyway), fold
 // the a*X term of the Combine into the Poly output: B + a I.  1 = on.
 static int g_fold_diag = 1;
+// CTA-pair kernel: launches whose tiles average fewer 64-deep k-blocks than
+// this drain their accumulators with 8 epilogue warps instead of 4.
+static int g_epi8_below = 32;
 
 // ------------------------------------------------------------------ errors
 namespace {
@@ -206,6 +209,7 @@ struct ShapeClass {
 struct PhaseTiles {
   int32_t n_tiles = 0;
   int32_t n_ctas = 0;
+  double mean_kblocks = 0.0;  // mean main-loop length of the tiles (64-deep k-blocks)
   DevBuf tiles, cta_begin;
 };
 
@@ -558,6 +562,9 @@ int build_phase_tiles(const std::vector<NsProblem>& probs, int geometry, int slo
       }
   }
   out.n_tiles = static_cast<int32_t>(tiles.size());
+  double kb = 0.0;
+  for (int64_t c : cost) kb += static_cast<double>(c - 2);
+  out.mean_kblocks = tiles.empty() ? 0.0 : kb / static_cast<double>(tiles.size());
   if (fp32) {
     out.n_ctas = out.n_tiles;
     int st = upload(out.tiles, tiles);
@@ -1042,6 +1049,7 @@ int muon_step_impl(dmuon_context* ctx, MuonSlot& S, const dmuon_matrix* mats, in
         const bool pairs = g_ns_pairs != 0;
         T.tri = (pairs && g_tri) ? 1 : 0;
         const PhaseTiles& PT = pairs ? P.phase2[kind] : P.phase[kind];
+        T.epi8 = (!T.fuse_update && PT.mean_kblocks < static_cast<double>(g_epi8_below)) ? 1 : 0;
         T.tiles = static_cast<const uint2*>(PT.tiles.p);
         T.cta_begin = static_cast<const int32_t*>(PT.cta_begin.p);
         st = timed_launch(ctx, DMUON_KERNEL_NS_GRAM + kind, s, [&] {
@@ -1551,6 +1559,11 @@ int dmuon_set_tuning(int32_t key, int32_t value) {
   }
   if (key == 7) {
     g_fold_diag = value ? 1 : 0;
+    return DMUON_OK;
+  }
+  if (key == 8) {
+    if (value < 0 || value > 1000000) return set_error(DMUON_ERR_INVALID_ARG, "set_tuning: key 8 value outside [0, 1e6]");
+    g_epi8_below = value;
     return DMUON_OK;
   }
   if (key == 4) {

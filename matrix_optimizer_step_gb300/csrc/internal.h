@@ -136,6 +136,8 @@ struct NsLaunch {
   // iteration computes a X + B X as (a I + B) X without reading X as aux
   // (that Combine then runs with a = 0).  0 = off.
   float diag;
+  // CTA-pair kernel: 8 epilogue warps instead of 4 (not with fuse_update).
+  int32_t epi8;
 };
 
 // ---- launch wrappers (each returns the cudaError_t of its launch) ----

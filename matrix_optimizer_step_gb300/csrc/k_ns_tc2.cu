@@ -46,20 +46,30 @@ constexpr int BK = 64;
 constexpr uint32_t HALF_BYTES = 128 * BK * 2;         // 16 KiB: 128 rows x 64 k, bf16
 constexpr uint32_t STAGE_BYTES = 2 * HALF_BYTES;      // A half + B half per CTA
 constexpr uint32_t MN_BOX_BYTES = 64 * 64 * 2;        // 8 KiB
-constexpr int kThreads = 224;  // warps: 0 A producer, 1 MMA, 2-5 epilogue, 6 B producer
-constexpr int kProducerBWarp = 6;
-constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t STAGING_BYTES = 4 * 2 * 4096;  // 4 epilogue warps x 2 boxes of 32 x 64 bf16
-template <int STAGES>
-constexpr size_t smem_bytes() {
-  return 1024 + STAGES * STAGE_BYTES + STAGING_BYTES + (2 * STAGES + 5) * 8 + 16;
+// Warps: 0 A producer, 1 MMA, 2 .. 2+EPI-1 epilogue, 2+EPI B producer.  The
+// epilogue has EPI = 4 warps (one per TMEM lane quarter) or 8 (two per lane
+// quarter, each on half of the tile's columns).  Eight drain a tile twice as
+// fast, which pays where the main loop is short (K of a few k-blocks: small
+// matrices), but their global loads then compete with the operand copies
+// for each SM's memory bandwidth, which slows long main loops; the host
+// picks per launch.  The fused update always runs with 4 (its register
+// needs leave no room for more threads).
+template <int EPI>
+constexpr int threads_of() {
+  return (3 + EPI) * 32;
 }
-static_assert(smem_bytes<5>() <= 227 * 1024, "shared memory budget");
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kStagingPerWarp = 2 * 4096;  // 2 boxes of 32 x 64 bf16
+template <int STAGES, int EPI>
+constexpr size_t smem_bytes() {
+  return 1024 + STAGES * STAGE_BYTES + EPI * kStagingPerWarp + (2 * STAGES + 5) * 8 + 16;
+}
+static_assert(smem_bytes<5, 8>() <= 227 * 1024, "shared memory budget");
 // Every CTA allocates all 512 TMEM columns, so two CTAs must never share an
 // SM: a second resident pair could hold one SM's TMEM while its partner waits
 // for the other's.  Asking for more than half of the SM's 228 KiB of shared
 // memory rules that out.
-static_assert(smem_bytes<4>() > 114 * 1024, "one CTA per SM");
+static_assert(smem_bytes<4, 4>() > 114 * 1024, "one CTA per SM");
 
 __device__ __forceinline__ uint64_t desc_k(uint32_t base, int kk) {
   return smem_desc_sw128(base + 32u * kk, 16u, 1024u);
@@ -101,15 +111,18 @@ __device__ __forceinline__ bool tri_below(int tri_bit, int k0, int row0) {
   return tri_bit && (k0 >> 8) < (row0 >> 8);
 }
 
-template <int STAGES, bool PREFETCH, bool FUSE>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) ns_tc2_kernel(const NsLaunch L) {
+template <int STAGES, bool PREFETCH, bool FUSE, int EPI>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_of<EPI>(), 1)
+    ns_tc2_kernel(const NsLaunch L) {
+  static_assert(EPI == 4 || (EPI == 8 && !FUSE), "epilogue warp count");
+  constexpr int kProducerBWarp = 2 + EPI;
   constexpr int kNumBars = 2 * STAGES + 2 + 2 + 1;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   const uint32_t ring = smem_u32(smem);
   const uint32_t staging = ring + STAGES * STAGE_BYTES;  // 1 KiB aligned (swizzled TMA source)
-  uint64_t* bar_mem = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES + STAGING_BYTES);
+  uint64_t* bar_mem = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES + EPI * kStagingPerWarp);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_mem + kNumBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -133,7 +146,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) ns_tc2_
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull(a), 1);
-      mbar_init(tempty(a), 8);
+      mbar_init(tempty(a), 2 * EPI);  // every epilogue warp of both CTAs
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -271,11 +284,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) ns_tc2_
       volatile int no_abort = 0;
       mbar_wait_bounded_cluster(drain, 0, &no_abort, L.err, kErrTimeoutDrain);
     }
-  } else if (warp >= 2 && warp <= 5) {
+  } else if (warp >= 2 && warp < 2 + EPI) {
     // ------------------------------------------------------------ epilogue
+    // A warp reaches the TMEM lanes of its warp index mod 4; with 8 warps
+    // the two warps of one lane quarter take one column half each.
     const int quarter = warp & 3;
+    const int half = (warp - 2) >> 2;
+    const int c_begin = (EPI == 8) ? 4 * half : 0;
+    const int c_end = (EPI == 8) ? c_begin + 4 : 8;
     const int row_in_tile = 128 * static_cast<int>(rank) + quarter * 32 + lane;
-    const uint32_t my_staging = staging + static_cast<uint32_t>(warp - 2) * 8192u;
+    const uint32_t my_staging = staging + static_cast<uint32_t>(warp - 2) * kStagingPerWarp;
     uint32_t box_count = 0;
     int local = 0;
     for (int t = t_begin; t < t_end; ++t, ++local) {
@@ -292,7 +310,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) ns_tc2_
         ns_epilogue_tile<true>(L, P, tm * TILE, tn * TILE, row_in_tile, t_lane, false);
       else
         ns_epilogue_tile_staged(L, P, tm * TILE, tn * TILE, row_in_tile, t_lane, !L.tri && P.sym && tm < tn,
-                                my_staging, box_count);
+                                my_staging, box_count, c_begin, c_end);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
@@ -325,24 +343,25 @@ void set_tc2_variant(int stages, int prefetch) {
   g_tc2_prefetch = prefetch ? 1 : 0;
 }
 
-template <int STAGES, bool PREFETCH, bool FUSE>
+template <int STAGES, bool PREFETCH, bool FUSE, int EPI>
 static cudaError_t launch_variant3(const NsLaunch& L, int n_pairs, cudaStream_t st) {
   static unsigned long long attr_mask = 0;
-  constexpr size_t smem = smem_bytes<STAGES>();
+  constexpr size_t smem = smem_bytes<STAGES, EPI>();
   if (attr_needed_on_current_device(&attr_mask)) {
-    cudaError_t e = cudaFuncSetAttribute(ns_tc2_kernel<STAGES, PREFETCH, FUSE>,
+    cudaError_t e = cudaFuncSetAttribute(ns_tc2_kernel<STAGES, PREFETCH, FUSE, EPI>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     attr_note_current_device(&attr_mask);
   }
-  ns_tc2_kernel<STAGES, PREFETCH, FUSE><<<2 * n_pairs, kThreads, smem, st>>>(L);
+  ns_tc2_kernel<STAGES, PREFETCH, FUSE, EPI><<<2 * n_pairs, threads_of<EPI>(), smem, st>>>(L);
   return cudaGetLastError();
 }
 
 template <int STAGES, bool PREFETCH>
 static cudaError_t launch_variant(const NsLaunch& L, int n_pairs, cudaStream_t st) {
-  return L.fuse_update ? launch_variant3<STAGES, PREFETCH, true>(L, n_pairs, st)
-                       : launch_variant3<STAGES, PREFETCH, false>(L, n_pairs, st);
+  if (L.fuse_update) return launch_variant3<STAGES, PREFETCH, true, 4>(L, n_pairs, st);
+  return L.epi8 ? launch_variant3<STAGES, PREFETCH, false, 8>(L, n_pairs, st)
+                : launch_variant3<STAGES, PREFETCH, false, 4>(L, n_pairs, st);
 }
 
 cudaError_t launch_ns_tc2(const NsLaunch& L, int n_pairs, cudaStream_t st) {
@@ -356,18 +375,18 @@ cudaError_t launch_ns_tc2(const NsLaunch& L, int n_pairs, cudaStream_t st) {
 int ns_tc2_max_pairs() {
   static int cached = -1;
   if (cached >= 0) return cached;
-  constexpr size_t smem = smem_bytes<5>();
-  if (cudaFuncSetAttribute(ns_tc2_kernel<5, true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  constexpr size_t smem = smem_bytes<5, 8>();
+  if (cudaFuncSetAttribute(ns_tc2_kernel<5, true, false, 8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem)) != cudaSuccess) {
     cudaGetLastError();
     return cached = 0;
   }
   cudaLaunchConfig_t cfg = {};  // cluster shape comes from __cluster_dims__
   cfg.gridDim = dim3(2, 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.blockDim = dim3(threads_of<8>(), 1, 1);
   cfg.dynamicSmemBytes = smem;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, ns_tc2_kernel<5, true, false>, &cfg) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&n, ns_tc2_kernel<5, true, false, 8>, &cfg) != cudaSuccess) {
     cudaGetLastError();
     n = 0;
   }

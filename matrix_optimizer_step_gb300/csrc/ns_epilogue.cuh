@@ -229,10 +229,12 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
 // buffers per warp alternate; before refilling one, lane 0 waits until the
 // store issued two boxes earlier has finished reading it.  The optional fp32
 // copy (first iteration) and the mirrored copy (when symmetric outputs are
-// not kept as upper blocks) are still stored directly.
+// not kept as upper blocks) are still stored directly.  The warp covers the
+// 32-column chunks [c_begin, c_end) of the tile (c_begin even: whole boxes).
 __device__ __forceinline__ void ns_epilogue_tile_staged(const NsLaunch& L, const NsProblem& P, int m0, int n0,
                                                         int row_in_tile, uint32_t t_lane, bool mirror,
-                                                        uint32_t stage_smem, uint32_t& box_count) {
+                                                        uint32_t stage_smem, uint32_t& box_count,
+                                                        int c_begin, int c_end) {
   constexpr int BN = 256;
   const int lane = threadIdx.x & 31;
   float g = 1.f;
@@ -261,6 +263,7 @@ __device__ __forceinline__ void ns_epilogue_tile_staged(const NsLaunch& L, const
   const bool aux_f32 = L.aux_f32 != 0;
   const CUtensorMap* map_out = L.maps + P.map_out;
   const int n_boxes = (min(BN, P.N - n0) + 63) / 64;
+  const int cc_end = min(c_end, 2 * n_boxes);
 
   const bool need_aux = beta != 0.f && row_ok;
   auto load_aux = [&](int cc, uint4 (&q)[8]) {
@@ -277,14 +280,14 @@ __device__ __forceinline__ void ns_epilogue_tile_staged(const NsLaunch& L, const
     }
   };
   uint4 aux_next[8];
-  load_aux(0, aux_next);
+  load_aux(c_begin, aux_next);
 #pragma unroll 1
-  for (int cc = 0; cc < 2 * n_boxes; ++cc) {
+  for (int cc = c_begin; cc < cc_end; ++cc) {
     const int col0 = n0 + cc * 32;
     uint4 aux_cur[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) aux_cur[i] = aux_next[i];
-    if (cc + 1 < 2 * n_boxes) load_aux(cc + 1, aux_next);
+    if (cc + 1 < cc_end) load_aux(cc + 1, aux_next);
     __syncwarp();
     uint32_t r[32];
     tmem_ld_32x32b_x32(t_lane + static_cast<uint32_t>(cc * 32), r);
