@@ -41,6 +41,9 @@ __device__ __forceinline__ void ns_epilogue_tile(const NsLaunch& L, const NsProb
   const float diag = (L.kind == kPoly) ? L.diag : 0.f;
   const int row = m0 + row_in_tile;
   const bool row_ok = row < P.M;
+  // A warp whose 32 rows all lie past the output's last row has nothing to
+  // read or write (the accumulator lanes are simply left for the next tile).
+  if (row - static_cast<int>(threadIdx.x & 31) >= P.M) return;
   uint16_t* out_row = reinterpret_cast<uint16_t*>(P.out) + static_cast<int64_t>(row) * P.ld_out;
   const uint16_t* aux_row =
       reinterpret_cast<const uint16_t*>(P.aux) + static_cast<int64_t>(row) * P.ld_aux;
@@ -257,6 +260,7 @@ __device__ __forceinline__ void ns_epilogue_tile_staged(const NsLaunch& L, const
   const int row = m0 + row_in_tile;
   const bool row_ok = row < P.M;
   const int warp_row0 = row - lane;
+  if (warp_row0 >= P.M) return;  // no row of this warp is in the output
   const uint16_t* aux_row = reinterpret_cast<const uint16_t*>(P.aux) + static_cast<int64_t>(row) * P.ld_aux;
   const float* auxf_row = reinterpret_cast<const float*>(P.aux) + static_cast<int64_t>(row) * P.ld_aux;
   float* out2_row = P.out2 ? P.out2 + static_cast<int64_t>(row) * P.ld_out2 : nullptr;

@@ -348,3 +348,44 @@ def test_many_tensors_one_call(cuda_lib):
     for x in res:
         assert x["buf"] <= 1e-6 and x["param_exact"], x
         assert max(x["O_slices"]) <= bf16_tol(x["shape"]), x
+
+
+# ------------------------------------------- momentum overlapped with NS
+
+def test_overlapped_momentum_groups_bit_identical(cuda_lib):
+    """A large step is cut into groups whose momentum runs on a side stream
+    beside the previous group's Newton-Schulz launches: every output must
+    equal the one-group step bit for bit, for several group counts, over two
+    steps (the smallest group size is lowered so that this 21 Mi-element
+    list forms up to 7 groups)."""
+    dev = torch.device("cuda")
+    shapes = [(1024, 4096), (4096, 1024), (2, 768, 3072), (1536, 1536), (3072, 768), (1024, 4096), (64, 4096),
+              (24, 2048)]
+    assert sum(int(np.prod(s)) for s in shapes) >= 16 << 20
+    g = torch.Generator(device=dev).manual_seed(77)
+    W0 = [torch.randn(s, generator=g, device=dev) * 0.02 for s in shapes]
+    grads = [[torch.randn(s, generator=g, device=dev).to(torch.bfloat16) for s in shapes] for _ in range(2)]
+    outs = {}
+    cuda_lib.dmuon_set_tuning(10, 1)
+    for groups in (1, 2, 4, 7):
+        cuda_lib.dmuon_set_tuning(9, groups)
+        try:
+            Wd = [w.clone() for w in W0]
+            Bd = [torch.zeros(s, device=dev) for s in shapes]
+            Gd = [torch.empty(s, device=dev, dtype=torch.bfloat16) for s in shapes]
+            Pd = [torch.empty(s, device=dev, dtype=torch.bfloat16) for s in shapes]
+            st = cuda_lib.OwnerStep(0)
+            st.set_muon(Wd, Bd, Gd, Pd)
+            for k in range(2):
+                for d, h in zip(Gd, grads[k]):
+                    d.copy_(h)
+                st.muon_step(0.02, 0.95, 0.01, 5, A, B, C)
+            st.sync()
+            outs[groups] = [t for t in Wd + Bd + Pd]
+            st.close()
+        finally:
+            cuda_lib.dmuon_set_tuning(9, 4)
+    cuda_lib.dmuon_set_tuning(10, 1024)
+    for groups in (2, 4, 7):
+        for i, (x, y) in enumerate(zip(outs[1], outs[groups])):
+            assert torch.equal(x, y), (groups, i)
