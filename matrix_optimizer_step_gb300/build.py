@@ -21,8 +21,8 @@ BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libdmuon.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
-SOURCES = ["api.cu", "lpt.cpp", "k_stream.cu", "k_ns_simt.cu", "k_ns_tc.cu", "k_ns_tc2.cu", "noalloc.cu"]
-HEADERS = ["internal.h", "ptx.cuh", "host_util.h", "ns_epilogue.cuh"]
+SOURCES = ["api.cu", "plan.cu", "step.cu", "host_io.cu", "lpt.cpp", "k_stream.cu", "k_ns_simt.cu", "k_ns_tc.cu", "k_ns_tc2.cu", "noalloc.cu"]
+HEADERS = ["internal.h", "runtime.h", "ptx.cuh", "host_util.h", "ns_epilogue.cuh"]
 
 
 def _nvcc():

@@ -218,3 +218,15 @@ def test_step_host_host_validation_without_gpu(mos):
         capi.dmuon_step_host(ctx, [], [], None, stream=0)  # nothing to do
     finally:
         mos.dmuon_context_destroy(ctx)
+
+
+def test_set_tuning_rejects_unknown_keys_and_bad_values(mos):
+    capi = mos.capi
+    for key, value in ((0, 1), (11, 1), (-3, 0), (8, -1), (9, 0), (9, 17), (10, 0), (10, 70000)):
+        with pytest.raises(mos.DmuonError) as e:
+            mos.dmuon_set_tuning(key, value)
+        assert e.value.status == capi.DMUON_ERR_INVALID_ARG, (key, value)
+    # Valid settings are accepted and put back to the defaults.
+    for key, value, default in ((8, 0, 32), (9, 1, 4), (10, 1, 1024), (7, 0, 1)):
+        mos.dmuon_set_tuning(key, value)
+        mos.dmuon_set_tuning(key, default)
