@@ -361,7 +361,7 @@ DMUON_API int dmuon_selftest_wait_timeout(dmuon_context* ctx, int32_t timeout_us
  *          instead of 4 (default 32; 0 = always 4, a large value = always 8
  *          except for the fused update).
  *   key 9: a Muon step is cut into up to `value` groups of consecutive
- *          tensors (1..16, default 4), each of at least key 10's size;
+ *          tensors (1..16, default 1), each of at least key 10's size;
  *          group g+1's momentum pass runs on a side stream of the context
  *          while group g's Newton-Schulz products run on the caller's
  *          stream.  1 = all on the caller's stream.  Results do not depend

@@ -29,12 +29,15 @@ int g_epi8_below = 32;
 // this many groups with disjoint workspace regions, and group g+1's
 // momentum pass (HBM-bound) runs on a side stream while group g's
 // Newton-Schulz products (tensor-core-bound) run on the caller's stream.
-// 1 = one group, everything on the caller's stream.  A group gets at least
-// g_group_min_elems elements (2^30 by default): smaller groups leave their
-// launches too few tiles to fill the GPU, which costs more than the hidden
-// momentum pass saves (measured: a GPT-2-sized list in 4 groups runs 40 %
-// slower, the Llama-3-8B set 1.5 % faster).
-int g_mom_groups = 4;
+// 1 (the default) = one group, everything on the caller's stream.  A group
+// gets at least g_group_min_elems elements (2^30 by default): smaller groups
+// leave their launches too few tiles to fill the GPU, which costs more than
+// the hidden momentum pass saves (measured: a GPT-2-sized list in 4 groups
+// runs 40 % slower, the Llama-3-8B set 1 % faster).  Off by default: the
+// gain is small, and kernels sharing the GPU make per-kernel timings
+// (and the rooflines computed from them) describe the contention rather
+// than the kernels.
+int g_mom_groups = 1;
 int64_t g_group_min_elems = int64_t(1) << 30;
 
 // ------------------------------------------------------------------ errors

@@ -227,6 +227,6 @@ def test_set_tuning_rejects_unknown_keys_and_bad_values(mos):
             mos.dmuon_set_tuning(key, value)
         assert e.value.status == capi.DMUON_ERR_INVALID_ARG, (key, value)
     # Valid settings are accepted and put back to the defaults.
-    for key, value, default in ((8, 0, 32), (9, 1, 4), (10, 1, 1024), (7, 0, 1)):
+    for key, value, default in ((8, 0, 32), (9, 4, 1), (10, 1, 1024), (7, 0, 1)):
         mos.dmuon_set_tuning(key, value)
         mos.dmuon_set_tuning(key, default)

@@ -384,7 +384,7 @@ def test_overlapped_momentum_groups_bit_identical(cuda_lib):
             outs[groups] = [t for t in Wd + Bd + Pd]
             st.close()
         finally:
-            cuda_lib.dmuon_set_tuning(9, 4)
+            cuda_lib.dmuon_set_tuning(9, 1)
     cuda_lib.dmuon_set_tuning(10, 1024)
     for groups in (2, 4, 7):
         for i, (x, y) in enumerate(zip(outs[1], outs[groups])):
