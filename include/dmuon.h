@@ -292,8 +292,9 @@ typedef struct dmuon_adamw_hparams {
  * copies io.grad_host into the descriptor's device grad buffer, runs exactly
  * dmuon_muon_step (mats, *muon) and dmuon_adamw_step (vecs, *adamw), and
  * copies the device param_bf16 buffer into io.param_host.  The Muon tensors
- * are cut into n_groups consecutive groups of about equal Newton-Schulz work
- * (1 <= n_groups <= 64, fewer if there are fewer tensors); each group's
+ * are cut into up to n_groups consecutive groups of about equal
+ * Newton-Schulz work (1 <= n_groups <= 64; fewer for short lists, since
+ * every group holds at least 2^25 elements, dmuon_set_tuning key 11); each group's
  * gradients travel while earlier groups compute and each group's parameters
  * travel while later groups compute, on two copy streams the context owns,
  * so the host link is busy only at the ends of the step.  The AdamW tensors
@@ -368,6 +369,8 @@ DMUON_API int dmuon_selftest_wait_timeout(dmuon_context* ctx, int32_t timeout_us
  *          on the setting.
  *   key 10: smallest group of key 9, in units of 2^20 elements (1..65536,
  *          default 1024).
+ *   key 11: smallest group of dmuon_step_host, in units of 2^10 elements
+ *          (1..2^20, default 32768).
  * Returns DMUON_ERR_INVALID_ARG for an unknown key.  Not thread-safe with
  * respect to concurrent steps.
  */

@@ -39,6 +39,8 @@ int g_epi8_below = 32;
 // than the kernels.
 int g_mom_groups = 1;
 int64_t g_group_min_elems = int64_t(1) << 30;
+// Host-buffer step: smallest group (elements).
+int64_t g_host_group_min_elems = int64_t(1) << 25;
 
 // ------------------------------------------------------------------ errors
 namespace {
@@ -447,6 +449,11 @@ int dmuon_set_tuning(int32_t key, int32_t value) {
   if (key == 10) {
     if (value < 1 || value > 65536) return set_error(DMUON_ERR_INVALID_ARG, "set_tuning: key 10 value outside [1, 65536]");
     g_group_min_elems = int64_t(value) << 20;
+    return DMUON_OK;
+  }
+  if (key == 11) {
+    if (value < 1 || value > (1 << 20)) return set_error(DMUON_ERR_INVALID_ARG, "set_tuning: key 11 value outside [1, 2^20]");
+    g_host_group_min_elems = int64_t(value) << 10;
     return DMUON_OK;
   }
   if (key == 4) {

@@ -45,8 +45,18 @@ def _host_grads(seed, st):
     return hg, hv
 
 
+@pytest.fixture
+def small_host_groups(cuda_lib):
+    # These lists are far below the default smallest group: allow groups of
+    # 1 Ki elements so that the requested group counts are formed.
+    cuda_lib.dmuon_set_tuning(11, 1)
+    yield cuda_lib
+    cuda_lib.dmuon_set_tuning(11, 32768)
+
+
 @pytest.mark.parametrize("n_groups", [1, 3, 8])
-def test_step_host_bit_identical_to_device_path(cuda_lib, n_groups):
+def test_step_host_bit_identical_to_device_path(small_host_groups, n_groups):
+    cuda_lib = small_host_groups
     dev = torch.device("cuda")
     a = _state(5, SHAPES, VEC_NUMELS, dev)
     b = _state(5, SHAPES, VEC_NUMELS, dev)
@@ -84,7 +94,8 @@ def test_step_host_bit_identical_to_device_path(cuda_lib, n_groups):
     sb.close()
 
 
-def test_step_host_against_oracle(cuda_lib):
+def test_step_host_against_oracle(small_host_groups):
+    cuda_lib = small_host_groups
     dev = torch.device("cuda")
     shape = (256, 768)
     g = torch.Generator().manual_seed(11)
