@@ -94,6 +94,13 @@ int muon_launch_ns(dmuon_context* ctx, MuonSlot& S, float lr, float wd, int32_t 
   float* inv_norm = static_cast<float*>(P.inv_norm.p);
   const int n_chunks = static_cast<int>(P.chunks.size());
   int st = DMUON_OK;
+  // The last Combine applies the update in its epilogue, except where its
+  // tiles' main loops are short: there the epilogue sets the pace, and a
+  // plain X store by 8 epilogue warps followed by the streaming update pass
+  // is faster (GPT-2 set: 380 us fused against 120 + ~160 us).
+  const bool pairs = g_ns_pairs != 0;
+  const PhaseTiles& last_combine = pairs ? P.phase2[kCombine] : P.phase[kCombine];
+  const bool fuse_last = last_combine.mean_kblocks >= static_cast<double>(g_epi8_below);
   for (int it = 0; it < ns_steps; ++it) {
     const int variant = it < 2 ? 2 + it : (it & 1);
     for (int kind = kGram; kind <= kCombine; ++kind) {
@@ -117,14 +124,13 @@ int muon_launch_ns(dmuon_context* ctx, MuonSlot& S, float lr, float wd, int32_t 
           if (kind == kPoly) T.diag = a;
           if (kind == kCombine) T.a = 0.f;
         }
-        if (kind == kCombine && it == ns_steps - 1) {
+        if (kind == kCombine && it == ns_steps - 1 && fuse_last) {
           // The last Combine applies the update itself (no X store, no update pass).
           T.fuse_update = 1;
           T.slices = d_slices;
           T.lr = lr;
           T.wd = wd;
         }
-        const bool pairs = g_ns_pairs != 0;
         T.tri = (pairs && g_tri) ? 1 : 0;
         const PhaseTiles& PT = pairs ? P.phase2[kind] : P.phase[kind];
         T.epi8 = (!T.fuse_update && PT.mean_kblocks < static_cast<double>(g_epi8_below)) ? 1 : 0;
@@ -147,14 +153,14 @@ int muon_launch_ns(dmuon_context* ctx, MuonSlot& S, float lr, float wd, int32_t 
       }
     }
   }
-  // The bf16 classes' update is fused into their last Combine; the update
-  // pass covers the fp32 classes (every slice when there are no iterations).
-  const bool all = ns_steps == 0;
-  const int n_upd = all ? n_chunks : static_cast<int>(P.chunks_f32.size());
+  // With a fused last Combine the update pass covers the fp32 classes only;
+  // otherwise (or with no iterations) every slice.
+  const bool every = ns_steps == 0 || !fuse_last;
+  const int n_upd = every ? n_chunks : static_cast<int>(P.chunks_f32.size());
   if (n_upd == 0) return DMUON_OK;
-  const Chunk* d_upd = all ? d_chunks : static_cast<const Chunk*>(P.chunks_f32_dev.p);
+  const Chunk* d_upd = every ? d_chunks : static_cast<const Chunk*>(P.chunks_f32_dev.p);
   return timed_launch(ctx, DMUON_KERNEL_UPDATE, s, [&] {
-    return launch_update(d_slices, d_upd, n_upd, lr, wd, 0, all ? inv_norm : nullptr, s);
+    return launch_update(d_slices, d_upd, n_upd, lr, wd, 0, ns_steps == 0 ? inv_norm : nullptr, s);
   });
 }
 

@@ -188,8 +188,12 @@ def vector_init(spec, index, device="cpu"):
 
 
 def _orthonormal(rows, k, g, device):
-    q, _ = torch.linalg.qr(torch.randn(rows, k, generator=g, device=device, dtype=torch.float32))
-    return q
+    # Drawn on `device` (seeded stream), factored on the host: a rows x k QR
+    # is tiny, and the host routine needs no optional GPU linear-algebra
+    # library at run time.
+    a = torch.randn(rows, k, generator=g, device=device, dtype=torch.float32)
+    q, _ = torch.linalg.qr(a.cpu())
+    return q.to(device)
 
 
 def muon_grad(wl, spec, index, step=0, device="cpu"):
