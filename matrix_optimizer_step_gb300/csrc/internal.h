@@ -28,7 +28,7 @@ struct SliceDesc {
   const void* grad;
   uint16_t* param;        // may be null
   void* x0;               // workspace: X before the first iteration (NS operand dtype)
-  float* x0f;             // workspace: fp32 copy of X0 for the first epilogues (bf16 path), or null
+  uint16_t* x0lo;         // workspace: low bf16 half of X0, X0 - bf16(X0) (bf16 path), or null
   const void* xk;         // workspace: X after the last iteration
   int64_t ld;             // workspace row pitch, elements
   int32_t m, n;
@@ -74,8 +74,12 @@ struct NsProblem {
   void* out;
   const void* aux;
   int64_t ld_out, ld_aux;
-  float* out2;            // optional fp32 copy of the output (tcgen05 path), or null
-  int64_t ld_out2;
+  // tcgen05 path, first iterations: low bf16 halves (v - bf16(v)) of the aux
+  // operand (read, aux + aux_lo carries 16 significant bits) and of the
+  // output (written), or null.  Same pitch as aux / out.
+  const uint16_t* aux_lo;
+  uint16_t* out_lo;
+  int32_t map_out_lo;     // tensor map of out_lo with 64 x 32 boxes (CTA-pair kernel)
   int32_t M, N, K;
   int32_t slice;          // global slice index (norm table)
   int32_t map_a, map_b;
@@ -104,11 +108,13 @@ struct NsProblem {
 //   kCombine: out = g^p * (acc + a * aux)      (X' = a X + B X, aux = X)
 // g = 1/(||u||+eps) of the slice when the fold-in of the normalisation is
 // active (first iteration), p = gpow; g^0 = 1.
-// On the bf16 path the MMA operands are always bf16, but the first
-// iteration keeps fp32 copies of X0, A and X1 for the epilogue terms b*A and
-// a*X (aux_f32 = 1 and out2 set): those terms carry the weak directions of a
+// On the bf16 path the MMA operands are always bf16, but the first two
+// iterations keep the low halves of X0, A and X1 (aux_lo / out_lo) for the
+// epilogue terms b*A and a*X: those terms carry the weak directions of a
 // gradient dominated by a few large singular values, and rounding them to
-// bf16 before the iteration amplifies them is what costs accuracy.
+// bf16 before the iteration amplifies them is what costs accuracy.  A bf16
+// value plus its bf16 remainder holds 16 significant bits, which is as good
+// as fp32 here and costs 2 bytes per element instead of 4.
 enum NsKind : int { kGram = 0, kPoly = 1, kCombine = 2 };
 
 struct NsLaunch {
@@ -119,7 +125,6 @@ struct NsLaunch {
   const float* gscale;      // per-slice 1/(||u||+eps), or null
   int32_t gpow;
   int32_t kind;
-  int32_t aux_f32;          // aux is fp32 (tcgen05 path; the fp32 path is always fp32)
   float a, b, c;
   int* err;
   // Last Combine of the step on the tensor-core path: instead of storing X,

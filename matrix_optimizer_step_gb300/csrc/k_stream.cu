@@ -126,7 +126,14 @@ __global__ void __launch_bounds__(kThreads) momentum_kernel(const SliceDesc* __r
         store8_f32(reinterpret_cast<float*>(S.x0) + xi, u);
       else
         store8_bf16(reinterpret_cast<uint16_t*>(S.x0) + xi, u);
-      if (S.x0f) store8_f32(S.x0f + xi, u);
+      if (S.x0lo) {
+        uint4 q;
+        q.x = pack_bf16x2_remainder(u[0], u[1]);
+        q.y = pack_bf16x2_remainder(u[2], u[3]);
+        q.z = pack_bf16x2_remainder(u[4], u[5]);
+        q.w = pack_bf16x2_remainder(u[6], u[7]);
+        *reinterpret_cast<uint4*>(S.x0lo + xi) = q;
+      }
     }
   } else {
     for (int64_t e = ch.start + threadIdx.x; e < end; e += kThreads) {
@@ -138,7 +145,7 @@ __global__ void __launch_bounds__(kThreads) momentum_kernel(const SliceDesc* __r
       const int64_t row = e / S.n;
       const int64_t xi = row * S.ld + (e - row * S.n);
       store1(S.x0, xi, u, !x_fp32);
-      if (S.x0f) S.x0f[xi] = u;
+      if (S.x0lo) S.x0lo[xi] = to_bf16_bits(bf16_remainder(u));
     }
   }
   const float tot = block_sum(ss, red);

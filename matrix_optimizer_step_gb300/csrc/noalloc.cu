@@ -109,8 +109,9 @@ extern "C" int dmuon_muon_step_noalloc(const dmuon_matrix* mat, float lr, float 
   const int64_t ld = up(n, 8), ldp = up(p, 8);
   const int64_t S = slices;
 
-  // Scratch layout: tensor maps, then X0/X1 bf16, fp32 X, A bf16, fp32 A,
-  // B bf16, chunk partials, per-slice norms, error word, tables.
+  // Scratch layout: tensor maps, then X0/X1 bf16, X low halves bf16, A bf16,
+  // A low halves bf16, B bf16, chunk partials, per-slice norms, error word,
+  // tables.
   const int64_t chunks_per_slice = (m * n + kChunkElems - 1) / kChunkElems;
   const int64_t n_chunks = chunks_per_slice * S;
   size_t off = 0;
@@ -123,9 +124,9 @@ extern "C" int dmuon_muon_step_noalloc(const dmuon_matrix* mat, float lr, float 
   size_t o_x[2];
   o_x[0] = take(size_t(S) * m * ld * 2);
   o_x[1] = take(size_t(S) * m * ld * 2);
-  const size_t o_xf = take(size_t(S) * m * ld * 4);
+  const size_t o_xl = take(size_t(S) * m * ld * 2);
   const size_t o_a = take(size_t(S) * p * ldp * 2);
-  const size_t o_af = take(size_t(S) * p * ldp * 4);
+  const size_t o_al = take(size_t(S) * p * ldp * 2);
   const size_t o_b = take(size_t(S) * p * ldp * 2);
   const size_t o_part = take(size_t(n_chunks) * 4);
   const size_t o_norm = take(size_t(S) * 4);
@@ -229,7 +230,7 @@ extern "C" int dmuon_muon_step_noalloc(const dmuon_matrix* mat, float lr, float 
     D.grad = static_cast<const uint8_t*>(M.grad) + eo * (gbf ? 2 : 4);
     D.param = M.param_bf16 ? M.param_bf16 + eo : nullptr;
     D.x0 = base + o_x[0] + size_t(s) * m * ld * 2;
-    D.x0f = reinterpret_cast<float*>(base + o_xf) + size_t(s) * m * ld;
+    D.x0lo = reinterpret_cast<uint16_t*>(base + o_xl) + size_t(s) * m * ld;
     D.xk = base + o_x[ns_steps & 1] + size_t(s) * m * ld * 2;
     D.ld = ld;
     D.m = static_cast<int32_t>(m);
@@ -256,8 +257,8 @@ extern "C" int dmuon_muon_step_noalloc(const dmuon_matrix* mat, float lr, float 
   for (int64_t s = 0; s < S; ++s) {
     uint8_t* A = base + o_a + size_t(s) * p * ldp * 2;
     uint8_t* Bm = base + o_b + size_t(s) * p * ldp * 2;
-    float* Af = reinterpret_cast<float*>(base + o_af) + size_t(s) * p * ldp;
-    float* Xf = reinterpret_cast<float*>(base + o_xf) + size_t(s) * m * ld;
+    uint16_t* Al = reinterpret_cast<uint16_t*>(base + o_al) + size_t(s) * p * ldp;
+    uint16_t* Xl = reinterpret_cast<uint16_t*>(base + o_xl) + size_t(s) * m * ld;
     for (int par = 0; par < 2; ++par) {
       uint8_t* X = base + o_x[par] + size_t(s) * m * ld * 2;
       uint8_t* Xn = base + o_x[par ^ 1] + size_t(s) * m * ld * 2;
@@ -299,14 +300,12 @@ extern "C" int dmuon_muon_step_noalloc(const dmuon_matrix* mat, float lr, float 
       NsProblem* v[3] = {&g, &y, &cc};
       for (int k = 0; k < 3; ++k) memcpy(&hp[(size_t(k) * 4 + par) * S + s], v[k], sizeof(NsProblem));
       if (par == 0) {
-        g.out2 = Af;
-        g.ld_out2 = ldp;
-        y.aux = Af;
-        cc.aux = Xf;
-        cc.out2 = Xf;
-        cc.ld_out2 = ld;
+        g.out_lo = Al;
+        y.aux_lo = Al;
+        cc.aux_lo = Xl;
+        cc.out_lo = Xl;
       } else {
-        cc.aux = Xf;
+        cc.aux_lo = Xl;
       }
       for (int k = 0; k < 3; ++k) memcpy(&hp[(size_t(k) * 4 + 2 + par) * S + s], v[k], sizeof(NsProblem));
     }
@@ -374,7 +373,6 @@ extern "C" int dmuon_muon_step_noalloc(const dmuon_matrix* mat, float lr, float 
       L.gscale = (it == 0 && kind != kPoly) ? inv_norm : nullptr;
       L.gpow = (kind == kGram) ? 2 : 1;
       L.kind = kind;
-      L.aux_f32 = ((it == 0 && kind != kGram) || (it == 1 && kind == kCombine)) ? 1 : 0;
       L.a = a;
       L.b = b;
       L.c = c;

@@ -13,6 +13,43 @@
 
 namespace dmuon {
 
+// One 32-column chunk of a thread's aux row: q[0..3] the bf16 values, and
+// q[4..7] their bf16 low halves when lo_row is given.
+__device__ __forceinline__ void load_aux_chunk(const uint16_t* hi_row, const uint16_t* lo_row, int c0,
+                                               uint4 (&q)[8]) {
+  const uint4* h = reinterpret_cast<const uint4*>(hi_row + c0);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) q[i] = __ldg(h + i);
+  if (lo_row) {
+    const uint4* l = reinterpret_cast<const uint4*>(lo_row + c0);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) q[4 + i] = __ldg(l + i);
+  }
+}
+
+__device__ __forceinline__ void unpack_aux_chunk(const uint4 (&q)[8], bool has_lo, float (&f)[32]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t w[4] = {q[i].x, q[i].y, q[i].z, q[i].w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      f[8 * i + 2 * j] = __uint_as_float(w[j] << 16);
+      f[8 * i + 2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+    }
+  }
+  if (has_lo) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t w[4] = {q[4 + i].x, q[4 + i].y, q[4 + i].z, q[4 + i].w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        f[8 * i + 2 * j] += __uint_as_float(w[j] << 16);
+        f[8 * i + 2 * j + 1] += __uint_as_float(w[j] & 0xFFFF0000u);
+      }
+    }
+  }
+}
+
 // row_in_tile: this thread's row within the tile; tmem_lane_base: TMEM
 // address of this warp's lane quarter at column 0 of the accumulator.
 // Tiles are 256 columns wide; `mirror` tiles are strictly above the
@@ -47,9 +84,8 @@ __device__ __forceinline__ void ns_epilogue_tile(const NsLaunch& L, const NsProb
   uint16_t* out_row = reinterpret_cast<uint16_t*>(P.out) + static_cast<int64_t>(row) * P.ld_out;
   const uint16_t* aux_row =
       reinterpret_cast<const uint16_t*>(P.aux) + static_cast<int64_t>(row) * P.ld_aux;
-  const float* auxf_row = reinterpret_cast<const float*>(P.aux) + static_cast<int64_t>(row) * P.ld_aux;
-  float* out2_row = P.out2 ? P.out2 + static_cast<int64_t>(row) * P.ld_out2 : nullptr;
-  const bool aux_f32 = L.aux_f32 != 0;
+  const uint16_t* auxlo_row = P.aux_lo ? P.aux_lo + static_cast<int64_t>(row) * P.ld_aux : nullptr;
+  uint16_t* outlo_row = P.out_lo ? P.out_lo + static_cast<int64_t>(row) * P.ld_out : nullptr;
   // Fused update (last iteration): W <- W*decay - step*X, param <- bf16(W).
   constexpr bool fuse = FUSE;
   float* w_row = nullptr;
@@ -70,15 +106,10 @@ __device__ __forceinline__ void ns_epilogue_tile(const NsLaunch& L, const NsProb
   auto load_aux = [&](int cc, uint4 (&q)[8]) {
     const int c0 = n0 + cc * 32;
     if (!need_aux || c0 + 32 > P.N) return;
-    if (aux_f32) {
-      const uint4* src = reinterpret_cast<const uint4*>(auxf_row + c0);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) q[i] = __ldg(src + i);
-    } else {
-      const uint4* src = reinterpret_cast<const uint4*>(aux_row + c0);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) q[i] = __ldg(src + i);
-    }
+    load_aux_chunk(aux_row, auxlo_row, c0, q);
+  };
+  auto aux_at = [&](int c) {
+    return bf16_bits_to_f32(aux_row[c]) + (auxlo_row ? bf16_bits_to_f32(auxlo_row[c]) : 0.f);
   };
   uint4 aux_next[8];
   load_aux(0, aux_next);
@@ -95,27 +126,7 @@ __device__ __forceinline__ void ns_epilogue_tile(const NsLaunch& L, const NsProb
     tmem_ld_32x32b_x32(t_lane + static_cast<uint32_t>(cc * 32), r);
     const bool full_chunk = (col0 + 32 <= P.N);
     float auxf[32];
-    if (need_aux && full_chunk) {
-      if (aux_f32) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          auxf[4 * i] = __uint_as_float(aux_cur[i].x);
-          auxf[4 * i + 1] = __uint_as_float(aux_cur[i].y);
-          auxf[4 * i + 2] = __uint_as_float(aux_cur[i].z);
-          auxf[4 * i + 3] = __uint_as_float(aux_cur[i].w);
-        }
-      } else {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const uint32_t w[4] = {aux_cur[i].x, aux_cur[i].y, aux_cur[i].z, aux_cur[i].w};
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            auxf[8 * i + 2 * j] = __uint_as_float(w[j] << 16);
-            auxf[8 * i + 2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
-          }
-        }
-      }
-    }
+    if (need_aux && full_chunk) unpack_aux_chunk(aux_cur, auxlo_row != nullptr, auxf);
     float4 wq[8];
     if (fuse && row_ok && full_chunk && w_vec) {
       const float4* src = reinterpret_cast<const float4*>(w_row + col0);
@@ -173,29 +184,32 @@ __device__ __forceinline__ void ns_epilogue_tile(const NsLaunch& L, const NsProb
       for (int i = 0; i < 4; ++i)
         dst[i] = make_uint4(pack_bf16x2(v[8 * i], v[8 * i + 1]), pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
                             pack_bf16x2(v[8 * i + 4], v[8 * i + 5]), pack_bf16x2(v[8 * i + 6], v[8 * i + 7]));
-      if (out2_row) {
-        float4* d2 = reinterpret_cast<float4*>(out2_row + col0);
+      if (outlo_row) {
+        uint4* dl = reinterpret_cast<uint4*>(outlo_row + col0);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) d2[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+        for (int i = 0; i < 4; ++i)
+          dl[i] = make_uint4(pack_bf16x2_remainder(v[8 * i], v[8 * i + 1]),
+                             pack_bf16x2_remainder(v[8 * i + 2], v[8 * i + 3]),
+                             pack_bf16x2_remainder(v[8 * i + 4], v[8 * i + 5]),
+                             pack_bf16x2_remainder(v[8 * i + 6], v[8 * i + 7]));
       }
       if (mirror) {
         // Transposed copy: for each column j the warp's 32 lanes hold 32
         // consecutive rows, so every store instruction writes one
-        // contiguous 64-byte (bf16) or 128-byte (fp32) run.
+        // contiguous 64-byte run.
         uint16_t* mo = reinterpret_cast<uint16_t*>(P.out) + row;
 #pragma unroll
         for (int j = 0; j < 32; ++j) mo[static_cast<int64_t>(col0 + j) * P.ld_out] = to_bf16_bits(v[j]);
-        if (P.out2) {
-          float* m2 = P.out2 + row;
+        if (P.out_lo) {
+          uint16_t* ml = P.out_lo + row;
 #pragma unroll
-          for (int j = 0; j < 32; ++j) m2[static_cast<int64_t>(col0 + j) * P.ld_out2] = v[j];
+          for (int j = 0; j < 32; ++j) ml[static_cast<int64_t>(col0 + j) * P.ld_out] = to_bf16_bits(bf16_remainder(v[j]));
         }
       }
     } else {
       for (int j = 0; j < 32 && col0 + j < P.N; ++j) {
         float v = alpha * __uint_as_float(r[j]);
-        if (beta != 0.f)
-          v = fmaf(beta, aux_f32 ? auxf_row[col0 + j] : bf16_bits_to_f32(aux_row[col0 + j]), v);
+        if (beta != 0.f) v = fmaf(beta, aux_at(col0 + j), v);
         if (row == col0 + j) v += diag;
         if (fuse) {
           const float w = fmaf(-step, v, w_row[col0 + j] * decay);
@@ -204,12 +218,13 @@ __device__ __forceinline__ void ns_epilogue_tile(const NsLaunch& L, const NsProb
           continue;
         }
         const uint16_t vb = to_bf16_bits(v);
+        const uint16_t vl = to_bf16_bits(bf16_remainder(v));
         out_row[col0 + j] = vb;
-        if (out2_row) out2_row[col0 + j] = v;
+        if (outlo_row) outlo_row[col0 + j] = vl;
         if (mirror) {
           const int64_t mi = static_cast<int64_t>(col0 + j);
           reinterpret_cast<uint16_t*>(P.out)[mi * P.ld_out + row] = vb;
-          if (P.out2) P.out2[mi * P.ld_out2 + row] = v;
+          if (P.out_lo) P.out_lo[mi * P.ld_out + row] = vl;
         }
       }
     }
@@ -262,10 +277,12 @@ __device__ __forceinline__ void ns_epilogue_tile_staged(const NsLaunch& L, const
   const int warp_row0 = row - lane;
   if (warp_row0 >= P.M) return;  // no row of this warp is in the output
   const uint16_t* aux_row = reinterpret_cast<const uint16_t*>(P.aux) + static_cast<int64_t>(row) * P.ld_aux;
-  const float* auxf_row = reinterpret_cast<const float*>(P.aux) + static_cast<int64_t>(row) * P.ld_aux;
-  float* out2_row = P.out2 ? P.out2 + static_cast<int64_t>(row) * P.ld_out2 : nullptr;
-  const bool aux_f32 = L.aux_f32 != 0;
+  const uint16_t* auxlo_row = P.aux_lo ? P.aux_lo + static_cast<int64_t>(row) * P.ld_aux : nullptr;
   const CUtensorMap* map_out = L.maps + P.map_out;
+  // With a low-half output both staging buffers of the warp hold one
+  // 64-column group (value and remainder), written by two TMA stores.
+  const bool has_lo = P.out_lo != nullptr;
+  const CUtensorMap* map_out_lo = has_lo ? L.maps + P.map_out_lo : nullptr;
   const int n_boxes = (min(BN, P.N - n0) + 63) / 64;
   const int cc_end = min(c_end, 2 * n_boxes);
 
@@ -273,15 +290,7 @@ __device__ __forceinline__ void ns_epilogue_tile_staged(const NsLaunch& L, const
   auto load_aux = [&](int cc, uint4 (&q)[8]) {
     const int c0 = n0 + cc * 32;
     if (!need_aux || c0 + 32 > P.N) return;
-    if (aux_f32) {
-      const uint4* src = reinterpret_cast<const uint4*>(auxf_row + c0);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) q[i] = __ldg(src + i);
-    } else {
-      const uint4* src = reinterpret_cast<const uint4*>(aux_row + c0);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) q[i] = __ldg(src + i);
-    }
+    load_aux_chunk(aux_row, auxlo_row, c0, q);
   };
   uint4 aux_next[8];
   load_aux(c_begin, aux_next);
@@ -298,29 +307,12 @@ __device__ __forceinline__ void ns_epilogue_tile_staged(const NsLaunch& L, const
     const bool full_chunk = (col0 + 32 <= P.N);
     float auxf[32];
     if (need_aux && full_chunk) {
-      if (aux_f32) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          auxf[4 * i] = __uint_as_float(aux_cur[i].x);
-          auxf[4 * i + 1] = __uint_as_float(aux_cur[i].y);
-          auxf[4 * i + 2] = __uint_as_float(aux_cur[i].z);
-          auxf[4 * i + 3] = __uint_as_float(aux_cur[i].w);
-        }
-      } else {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const uint32_t w[4] = {aux_cur[i].x, aux_cur[i].y, aux_cur[i].z, aux_cur[i].w};
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            auxf[8 * i + 2 * j] = __uint_as_float(w[j] << 16);
-            auxf[8 * i + 2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
-          }
-        }
-      }
+      unpack_aux_chunk(aux_cur, auxlo_row != nullptr, auxf);
     } else if (need_aux) {
       for (int j = 0; j < 32; ++j) {
         const int c = col0 + j;
-        auxf[j] = (c < P.N) ? (aux_f32 ? auxf_row[c] : bf16_bits_to_f32(aux_row[c])) : 0.f;
+        auxf[j] = (c < P.N) ? bf16_bits_to_f32(aux_row[c]) + (auxlo_row ? bf16_bits_to_f32(auxlo_row[c]) : 0.f)
+                            : 0.f;
       }
     }
     tmem_ld_wait();
@@ -331,32 +323,36 @@ __device__ __forceinline__ void ns_epilogue_tile_staged(const NsLaunch& L, const
       if (need_aux) v[j] = fmaf(beta, auxf[j], v[j]);
       if (row == col0 + j) v[j] += diag;
     }
-    const uint32_t buf = stage_smem + (box_count & 1u) * 4096u;
+    const uint32_t buf = has_lo ? stage_smem : stage_smem + (box_count & 1u) * 4096u;
     if ((cc & 1) == 0) {
-      if (lane == 0) bulk_wait_group_read<1>();
+      // Before refilling: the store that last read this buffer has read it
+      // (with a low half both buffers are refilled, so wait for all).
+      if (lane == 0) {
+        if (has_lo)
+          bulk_wait_group_read<0>();
+        else
+          bulk_wait_group_read<1>();
+      }
       __syncwarp();
     }
+    const uint32_t swz = static_cast<uint32_t>(lane) * 128u;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const uint32_t j = static_cast<uint32_t>(4 * (cc & 1) + i);
-      st_shared_v4(buf + static_cast<uint32_t>(lane) * 128u + ((j ^ static_cast<uint32_t>(lane & 7)) << 4),
-                   pack_bf16x2(v[8 * i], v[8 * i + 1]), pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
+      const uint32_t off = swz + ((j ^ static_cast<uint32_t>(lane & 7)) << 4);
+      st_shared_v4(buf + off, pack_bf16x2(v[8 * i], v[8 * i + 1]), pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
                    pack_bf16x2(v[8 * i + 4], v[8 * i + 5]), pack_bf16x2(v[8 * i + 6], v[8 * i + 7]));
-    }
-    if (row_ok && out2_row) {
-      if (full_chunk) {
-        float4* d2 = reinterpret_cast<float4*>(out2_row + col0);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) d2[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
-      } else {
-        for (int j = 0; j < 32 && col0 + j < P.N; ++j) out2_row[col0 + j] = v[j];
-      }
+      if (has_lo)
+        st_shared_v4(buf + 4096u + off, pack_bf16x2_remainder(v[8 * i], v[8 * i + 1]),
+                     pack_bf16x2_remainder(v[8 * i + 2], v[8 * i + 3]),
+                     pack_bf16x2_remainder(v[8 * i + 4], v[8 * i + 5]),
+                     pack_bf16x2_remainder(v[8 * i + 6], v[8 * i + 7]));
     }
     if (row_ok && mirror) {
       uint16_t* mo = reinterpret_cast<uint16_t*>(P.out) + row;
       for (int j = 0; j < 32 && col0 + j < P.N; ++j) {
         mo[static_cast<int64_t>(col0 + j) * P.ld_out] = to_bf16_bits(v[j]);
-        if (P.out2) P.out2[static_cast<int64_t>(col0 + j) * P.ld_out2 + row] = v[j];
+        if (has_lo) P.out_lo[static_cast<int64_t>(col0 + j) * P.ld_out + row] = to_bf16_bits(bf16_remainder(v[j]));
       }
     }
     if (cc & 1) {
@@ -364,10 +360,16 @@ __device__ __forceinline__ void ns_epilogue_tile_staged(const NsLaunch& L, const
       __syncwarp();
       if (lane == 0) {
         tma_store_3d(map_out, buf, n0 + 64 * (cc >> 1), warp_row0, P.z);
+        if (has_lo) tma_store_3d(map_out_lo, buf + 4096u, n0 + 64 * (cc >> 1), warp_row0, P.z);
         bulk_commit_group();
       }
       ++box_count;
     }
+  }
+  if (has_lo) {
+    // Leave both buffers free for the next tile, whichever kind it is.
+    if (lane == 0) bulk_wait_group_read<0>();
+    __syncwarp();
   }
 }
 

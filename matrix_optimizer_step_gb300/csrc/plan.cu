@@ -152,8 +152,8 @@ int layout_plan(MuonPlan& P, const dmuon_matrix* mats, int n, bool fp32, size_t 
     for (int t = 0; t < 2; ++t) C.off_x[t] = take(static_cast<size_t>(C.count) * C.m * C.ld * es);
     C.off_a = take(static_cast<size_t>(C.count) * p * C.ldp * es);
     C.off_b = take(static_cast<size_t>(C.count) * p * C.ldp * es);
-    C.off_xf = C.f32 ? 0 : take(static_cast<size_t>(C.count) * C.m * C.ld * 4);
-    C.off_af = C.f32 ? 0 : take(static_cast<size_t>(C.count) * p * C.ldp * 4);
+    C.off_xl = C.f32 ? 0 : take(static_cast<size_t>(C.count) * C.m * C.ld * 2);
+    C.off_al = C.f32 ? 0 : take(static_cast<size_t>(C.count) * p * C.ldp * 2);
   }
   P.ws_bytes = std::max<size_t>(off - ws_base, 1024);
   return DMUON_OK;
@@ -269,6 +269,14 @@ int build_muon_plan(dmuon_context* ctx, MuonPlan& P, const dmuon_matrix* mats, i
       if (st != DMUON_OK) return st;
       C.map_b_st = static_cast<int32_t>(maps.size());
       maps.push_back(st_map);
+      st = make_map(enc, &st_map, ws + C.off_xl, C.n, C.m, C.count, C.ld, 64, 32);
+      if (st != DMUON_OK) return st;
+      C.map_xl_st = static_cast<int32_t>(maps.size());
+      maps.push_back(st_map);
+      st = make_map(enc, &st_map, ws + C.off_al, p, p, C.count, C.ldp, 64, 32);
+      if (st != DMUON_OK) return st;
+      C.map_al_st = static_cast<int32_t>(maps.size());
+      maps.push_back(st_map);
     }
     st = upload(P.maps, maps);
     if (st != DMUON_OK) return st;
@@ -276,12 +284,13 @@ int build_muon_plan(dmuon_context* ctx, MuonPlan& P, const dmuon_matrix* mats, i
 
   // Problems of the three phases.  bf16 classes, variant 0/1: X in buffer
   // 0/1, everything bf16.  Variant 2 (first iteration, X in buffer 0) and 3
-  // (second iteration, X in buffer 1) add the fp32 side copies: the first
-  // Gram also writes A in fp32, the first Poly reads that fp32 A, the first
-  // Combine reads the fp32 X0 and writes X1 in fp32 over it (each element is
-  // read before it is written, by the same thread), and the second Combine
-  // reads that fp32 X1.  fp32 classes (all of them in validation mode) go to
-  // separate lists with variants 0/1 only.
+  // (second iteration, X in buffer 1) add the low bf16 halves: the first
+  // Gram also writes A's low half, the first Poly reads A with it, the first
+  // Combine reads X0 with its low half (written by the momentum pass) and
+  // writes X1's low half over it (each element is read before it is
+  // written, by the same thread), and the second Combine reads X1 with that
+  // low half.  fp32 classes (all of them in validation mode) go to separate
+  // lists with variants 0/1 only.
   std::vector<NsProblem> var[3][4], var_f32[3][2];
   for (size_t s_i = 0; s_i < P.slices.size(); ++s_i) {
     const SliceRef& R = P.slices[s_i];
@@ -292,8 +301,8 @@ int build_muon_plan(dmuon_context* ctx, MuonPlan& P, const dmuon_matrix* mats, i
     const size_t poff = static_cast<size_t>(R.z) * p * C.ldp;
     uint8_t* A = ws + C.off_a + poff * es;
     uint8_t* B = ws + C.off_b + poff * es;
-    float* Xf = C.f32 ? nullptr : reinterpret_cast<float*>(ws + C.off_xf) + xoff;
-    float* Af = C.f32 ? nullptr : reinterpret_cast<float*>(ws + C.off_af) + poff;
+    uint16_t* Xl = C.f32 ? nullptr : reinterpret_cast<uint16_t*>(ws + C.off_xl) + xoff;
+    uint16_t* Al = C.f32 ? nullptr : reinterpret_cast<uint16_t*>(ws + C.off_al) + poff;
     for (int par = 0; par < 2; ++par) {
       uint8_t* X = ws + C.off_x[par] + xoff * es;
       uint8_t* Xn = ws + C.off_x[par ^ 1] + xoff * es;
@@ -365,14 +374,14 @@ int build_muon_plan(dmuon_context* ctx, MuonPlan& P, const dmuon_matrix* mats, i
       var[kPoly][par].push_back(y);
       var[kCombine][par].push_back(c);
       if (par == 0) {
-        g.out2 = Af;
-        g.ld_out2 = C.ldp;
-        y.aux = Af;
-        c.aux = Xf;
-        c.out2 = Xf;
-        c.ld_out2 = C.ld;
+        g.out_lo = Al;
+        g.map_out_lo = C.map_al_st;
+        y.aux_lo = Al;
+        c.aux_lo = Xl;
+        c.out_lo = Xl;  // X1's low half over X0's: each element is read before it is written
+        c.map_out_lo = C.map_xl_st;
       }
-      if (par == 1) c.aux = Xf;
+      if (par == 1) c.aux_lo = Xl;
       var[kGram][2 + par].push_back(g);
       var[kPoly][2 + par].push_back(y);
       var[kCombine][2 + par].push_back(c);

@@ -188,6 +188,14 @@ __device__ __forceinline__ uint16_t to_bf16_bits(float x) {
 __device__ __forceinline__ float bf16_bits_to_f32(uint32_t bits16) {
   return __uint_as_float(bits16 << 16);
 }
+// Low half of a value split as bf16 + bf16: x - bf16(x), rounded to bf16.
+// The pair carries 16 significant bits.
+__device__ __forceinline__ float bf16_remainder(float x) {
+  return x - bf16_bits_to_f32(to_bf16_bits(x));
+}
+__device__ __forceinline__ uint32_t pack_bf16x2_remainder(float lo, float hi) {
+  return pack_bf16x2(bf16_remainder(lo), bf16_remainder(hi));
+}
 
 }  // namespace dmuon
 

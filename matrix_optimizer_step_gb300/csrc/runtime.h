@@ -132,9 +132,10 @@ struct ShapeClass {
   bool f32;             // Newton-Schulz in fp32 on CUDA cores (workspace fp32)
   int64_t ld, ldp;      // workspace row pitch (elements) for X and for A/B
   size_t off_x[2], off_a, off_b;  // byte offsets in the workspace
-  size_t off_xf, off_af;          // fp32 side copies of X and A (bf16 path only)
+  size_t off_xl, off_al;          // low bf16 halves of X and A (bf16 classes only)
   int32_t map_xk[2], map_xmn[2], map_a, map_b, map_a_mn, map_b_mn;
   int32_t map_x_st[2], map_a_st, map_b_st;  // 64 x 32 boxes for TMA stores
+  int32_t map_xl_st, map_al_st;              // the same for the low halves
 };
 
 struct PhaseTiles {

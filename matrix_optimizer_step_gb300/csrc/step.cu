@@ -51,7 +51,7 @@ int muon_stage_table(dmuon_context* ctx, MuonSlot& S, const dmuon_matrix* mats, 
     D.param = M.param_bf16 ? M.param_bf16 + R.elem_offset : nullptr;
     const size_t xoff = static_cast<size_t>(R.z) * C.m * C.ld * (C.f32 ? 4 : 2);
     D.x0 = ws + C.off_x[0] + xoff;
-    D.x0f = C.f32 ? nullptr : reinterpret_cast<float*>(ws + C.off_xf) + static_cast<size_t>(R.z) * C.m * C.ld;
+    D.x0lo = C.f32 ? nullptr : reinterpret_cast<uint16_t*>(ws + C.off_xl) + static_cast<size_t>(R.z) * C.m * C.ld;
     D.x_f32 = C.f32 ? 1 : 0;
     D.xk = ws + C.off_x[ns_steps & 1] + xoff;
     D.ld = C.ld;
@@ -117,7 +117,6 @@ int muon_launch_ns(dmuon_context* ctx, MuonSlot& S, float lr, float wd, int32_t 
       if (P.phase[kind].n_tiles > 0) {
         NsLaunch T = L;
         T.probs = static_cast<const NsProblem*>(P.probs[kind][variant].p);
-        T.aux_f32 = ((it == 0 && kind != kGram) || (it == 1 && kind == kCombine)) ? 1 : 0;
         if (g_fold_diag && it >= 2) {
           // X' = a X + B X = (a I + B) X: the Poly adds a on B's diagonal and
           // the Combine reads no aux.

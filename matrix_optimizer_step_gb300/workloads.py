@@ -272,9 +272,10 @@ def workload_ns_flops(wl):
 
 def momentum_bytes(wl):
     """HBM bytes of the momentum pass: grad read, momentum read+write, X0
-    write (bf16 operand plus its fp32 copy on the bf16 path; fp32 only in
-    the fp32 mode)."""
-    xb = 4 if wl.hyper["fp32_ns"] else 2 + 4
+    write (4 bytes per element either way: the bf16 operand plus its bf16
+    low half on the bf16 path, fp32 in the fp32 mode and for the small
+    classes that run in fp32)."""
+    xb = 4
     return sum(s.numel * ((2 if s.grad_dtype == torch.bfloat16 else 4) + 8 + xb) for s in wl.matrices)
 
 
