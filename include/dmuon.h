@@ -287,15 +287,17 @@ typedef struct dmuon_adamw_hparams {
  * dmuon_step_host -- one owner step whose gradients arrive in host memory and
  * whose bf16 parameters go back to host memory.
  *
- * The pages' step starts from gradients already on the owner's GPU; this
- * entry adds the host side around the same computation.  For every tensor it
- * copies io.grad_host into the descriptor's device grad buffer, runs exactly
- * dmuon_muon_step (mats, *muon) and dmuon_adamw_step (vecs, *adamw), and
- * copies the device param_bf16 buffer into io.param_host.  The Muon tensors
- * are cut into up to n_groups consecutive groups of about equal
+ * The pages have no counterpart: their owner step ("架构设计" §3.3 "Owner
+ * 步进") starts from gradients already in the owner's device memory.  This
+ * entry serves callers whose gradients and parameters live in host memory,
+ * and adds only the copies around the same computation.  For every tensor
+ * it copies io.grad_host into the descriptor's device grad buffer, runs
+ * exactly dmuon_muon_step (mats, *muon) and dmuon_adamw_step (vecs,
+ * *adamw), and copies the device param_bf16 buffer into io.param_host.  The
+ * Muon tensors are cut into up to n_groups consecutive groups of about equal
  * Newton-Schulz work (1 <= n_groups <= 64; fewer for short lists, since
- * every group holds at least 2^25 elements, dmuon_set_tuning key 11); each group's
- * gradients travel while earlier groups compute and each group's parameters
+ * every group holds at least 2^25 elements, dmuon_set_tuning key 11); each
+ * group's gradients travel while earlier groups compute and each group's parameters
  * travel while later groups compute, on two copy streams the context owns,
  * so the host link is busy only at the ends of the step.  The AdamW tensors
  * travel and step right after the first Muon group.  Results are bit-identical
