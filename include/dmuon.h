@@ -21,6 +21,10 @@
  *    frees in dmuon_context_destroy.
  *  - Device work is enqueued on the caller's stream (a cudaStream_t passed
  *    as void*, NULL = the legacy default stream) and returns without waiting.
+ *    Where an entry also uses streams the context owns (the host-buffer
+ *    step's copies, the optional momentum overlap), that work starts after
+ *    the work already on the caller's stream, and work enqueued there later
+ *    runs after it.
  *  - All arguments are validated on the host before anything is enqueued:
  *    a call that returns an error has changed no tensor.
  *  - Results are deterministic: the same inputs give bit-identical outputs
