@@ -35,4 +35,4 @@ from .capi import (  # noqa: F401
     dmuon_sync,
     load_library,
 )
-from .optim import OwnerStep, owner_partition  # noqa: F401
+from .optim import OwnerStep, adamw_shard_ranges, adamw_shard_views, owner_partition  # noqa: F401

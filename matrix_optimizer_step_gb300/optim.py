@@ -199,3 +199,40 @@ def owner_partition(numels, n_owners, layers=None, small_threshold=5_000_000):
     if layers is None:
         return capi.dmuon_lpt_assign(numels, int(n_owners))
     return capi.dmuon_lpt_assign_layered(numels, layers, int(n_owners), small_threshold)
+
+
+def adamw_shard_ranges(numels, n_ranks, align=8):
+    """The `sharded_adamw` route ("Pure DMuon 路由"): every AdamW-route element
+    is stepped by exactly one rank.  The tensors are laid end to end and the
+    concatenation is cut into n_ranks contiguous pieces of equal size
+    (boundaries rounded to multiples of `align` elements, so each piece keeps
+    16-byte alignment in fp32 and bf16).  Returns, per rank, a list of
+    (tensor index, start, count) runs in concatenation order; the pieces
+    partition every tensor exactly once.  Deterministic, so each rank computes
+    the same split on its own; gathering the pieces in rank order rebuilds
+    the concatenation."""
+    numels = [int(n) for n in numels]
+    n_ranks = int(n_ranks)
+    if n_ranks < 1 or align < 1 or any(n < 0 for n in numels):
+        raise ValueError("need n_ranks >= 1, align >= 1 and non-negative sizes")
+    total = sum(numels)
+    cuts = [min(total, (total * r // n_ranks + align - 1) // align * align) for r in range(n_ranks + 1)]
+    cuts[0], cuts[-1] = 0, total
+    out = []
+    for r in range(n_ranks):
+        lo, hi = cuts[r], max(cuts[r], cuts[r + 1])
+        runs, base = [], 0
+        for i, n in enumerate(numels):
+            a, b = max(lo, base), min(hi, base + n)
+            if a < b:
+                runs.append((i, a - base, b - a))
+            base += n
+        out.append(runs)
+    return out
+
+
+def adamw_shard_views(tensors, runs):
+    """Views of `tensors` (flattened) for one rank's runs, in order: the
+    arguments of OwnerStep.set_adamw for that rank's piece."""
+    return [tensors[i].reshape(-1)[start:start + count] for i, start, count in runs]
+
