@@ -467,7 +467,7 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default="llama3_8b")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--e2e-groups", type=int, default=16,
+    ap.add_argument("--e2e-groups", type=int, default=12,
                     help="groups of the host-buffer step (copies of one group overlap the others' compute)")
     ap.add_argument("--overlap-adamw", action="store_true",
                     help="run the AdamW step on a side stream beside the Muon step (OwnerStep.step); "

@@ -75,15 +75,25 @@ std::vector<std::pair<int, int>> split_groups(const dmuon_matrix* mats, int n, i
     cost[static_cast<size_t>(i)] = ns_steps > 0 ? lead * (4.0 * p * p * q + 2.0 * p * p * p) : lead * m * q0;
     total += cost[static_cast<size_t>(i)];
   }
+  // Shares grow from both ends, 2^min(g, G-1-g, 3): the first group's
+  // gradients (copied before any compute) and the last group's parameters
+  // (copied after all compute) are small, the middle groups large and few.
+  std::vector<double> share(static_cast<size_t>(groups));
+  double wsum = 0.0;
+  for (int g = 0; g < groups; ++g) {
+    share[static_cast<size_t>(g)] = double(1 << std::min(std::min(g, groups - 1 - g), 3));
+    wsum += share[static_cast<size_t>(g)];
+  }
   std::vector<std::pair<int, int>> out;
   int start = 0;
-  double acc = 0.0;
+  double acc = 0.0, cum = share[0];  // shares of the groups up to the open one
   for (int i = 0; i < n; ++i) {
     acc += cost[static_cast<size_t>(i)];
     const int closed = static_cast<int>(out.size());
-    if (closed < groups - 1 && i + 1 < n && acc >= total * double(closed + 1) / double(groups)) {
+    if (closed < groups - 1 && i + 1 < n && acc >= total * cum / wsum) {
       out.push_back({start, i + 1});
       start = i + 1;
+      cum += share[static_cast<size_t>(closed + 1)];
     }
   }
   if (start < n) out.push_back({start, n});
