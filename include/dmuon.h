@@ -355,8 +355,6 @@ DMUON_API int dmuon_selftest_wait_timeout(dmuon_context* ctx, int32_t timeout_us
  *   key 3: pipeline depth of the CTA-pair kernel (4 or 5 stages; default 4).
  *   key 4: tile order inside a problem (1 = longer tile dimension outer, the
  *          default; 0 = rows outer).  Takes effect at the next plan build.
- *   key 5: CTA-pair kernel loads the next tile's descriptor one tile ahead
- *          (1, default) or when the tile starts (0).
  *   key 6: CTA-pair kernel keeps symmetric products as upper blocks only and
  *          reads them through transposed loads (1) or stores mirrored copies
  *          of off-diagonal blocks (0).

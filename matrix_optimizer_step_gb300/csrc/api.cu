@@ -18,7 +18,7 @@ int g_tile_order = 1;
 // CTA-pair kernel: 1 = symmetric outputs stored as upper blocks only and read
 // through transposed loads, 0 = mirrored stores.
 int g_tri = 1;
-int g_tc2_stages_sel = 4, g_tc2_prefetch_sel = 1;
+int g_tc2_stages_sel = 4;
 // From the third iteration on (where X is read back in bf16 anyway), fold
 // the a*X term of the Combine into the Poly output: B + a I.  1 = on.
 int g_fold_diag = 1;
@@ -429,7 +429,7 @@ int dmuon_set_tuning(int32_t key, int32_t value) {
   }
   if (key == 3) {
     g_tc2_stages_sel = (value == 5) ? 5 : 4;
-    set_tc2_variant(g_tc2_stages_sel, g_tc2_prefetch_sel);
+    set_tc2_variant(g_tc2_stages_sel);
     return DMUON_OK;
   }
   if (key == 7) {
@@ -462,11 +462,6 @@ int dmuon_set_tuning(int32_t key, int32_t value) {
   }
   if (key == 6) {
     g_tri = value ? 1 : 0;
-    return DMUON_OK;
-  }
-  if (key == 5) {
-    g_tc2_prefetch_sel = value ? 1 : 0;
-    set_tc2_variant(g_tc2_stages_sel, g_tc2_prefetch_sel);
     return DMUON_OK;
   }
   return set_error(DMUON_ERR_INVALID_ARG, "set_tuning: unknown key");

@@ -111,7 +111,8 @@ __device__ __forceinline__ bool tri_below(int tri_bit, int k0, int row0) {
   return tri_bit && (k0 >> 8) < (row0 >> 8);
 }
 
-template <int STAGES, bool PREFETCH, bool FUSE, int EPI>
+// FUSE: the last Combine, which applies the update instead of storing X.
+template <int STAGES, bool FUSE, int EPI>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_of<EPI>(), 1)
     ns_tc2_kernel(const NsLaunch L) {
   static_assert(EPI == 4 || (EPI == 8 && !FUSE), "epilogue warp count");
@@ -180,8 +181,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_of<EPI>(), 1
     TileInfo cur{}, nxt{};
     if (t_begin < t_end) cur = load_tile_info(L, t_begin);
     for (int t = t_begin; t < t_end && ok; ++t) {
-      if (!PREFETCH) cur = load_tile_info(L, t);
-      if (PREFETCH && t + 1 < t_end) nxt = load_tile_info(L, t + 1);
+      if (t + 1 < t_end) nxt = load_tile_info(L, t + 1);
       const int tile_row0 = which ? cur.n0 : cur.m0;
       const int row0 = tile_row0 + 128 * static_cast<int>(rank);
       const CUtensorMap* map = L.maps + (which ? cur.map_b : cur.map_a);
@@ -192,7 +192,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_of<EPI>(), 1
       const int nk = cur.nk;
       // k-blocks before the operand's diagonal block come transposed.
       const int n_below = tri ? min(nk, (tile_row0 >> 8) * (256 / BK)) : 0;
-      if (PREFETCH) cur = nxt;
+      cur = nxt;
       for (int kb = 0; kb < nk; ++kb) {
         if (!mbar_wait_bounded_cluster(empty(stage), phase ^ 1u, abort_flag, L.err, kErrTimeoutProducer)) {
           ok = false;
@@ -239,14 +239,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_of<EPI>(), 1
       TileInfo cur{}, nxt{};
       if (t_begin < t_end) cur = load_tile_info(L, t_begin);
       for (int t = t_begin; t < t_end && ok; ++t, ++local) {
-        if (!PREFETCH) cur = load_tile_info(L, t);
-        if (PREFETCH && t + 1 < t_end) nxt = load_tile_info(L, t + 1);
+        if (t + 1 < t_end) nxt = load_tile_info(L, t + 1);
         const bool a_mn = (cur.majors & 1) != 0;
         const bool b_mn = (cur.majors & 2) != 0;
         const int tri = cur.tri;
         const int tile_m0 = cur.m0, tile_n0 = cur.n0;
         const int nk = cur.nk;
-        if (PREFETCH) cur = nxt;
+        cur = nxt;
         const int acc = local & 1;
         const uint32_t acc_phase = static_cast<uint32_t>(local >> 1) & 1u;
         if (!mbar_wait_bounded_cluster(tempty(acc), acc_phase ^ 1u, abort_flag, L.err, kErrTimeoutMma)) {
@@ -336,39 +335,36 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_of<EPI>(), 1
 }  // namespace
 
 static int g_tc2_stages = 4;
-static int g_tc2_prefetch = 1;
 
-void set_tc2_variant(int stages, int prefetch) {
-  g_tc2_stages = (stages == 5) ? 5 : 4;
-  g_tc2_prefetch = prefetch ? 1 : 0;
-}
+void set_tc2_variant(int stages) { g_tc2_stages = (stages == 5) ? 5 : 4; }
 
-template <int STAGES, bool PREFETCH, bool FUSE, int EPI>
+template <int STAGES, bool FUSE, int EPI>
 static cudaError_t launch_variant3(const NsLaunch& L, int n_pairs, cudaStream_t st) {
   static unsigned long long attr_mask = 0;
   constexpr size_t smem = smem_bytes<STAGES, EPI>();
   if (attr_needed_on_current_device(&attr_mask)) {
-    cudaError_t e = cudaFuncSetAttribute(ns_tc2_kernel<STAGES, PREFETCH, FUSE, EPI>,
+    cudaError_t e = cudaFuncSetAttribute(ns_tc2_kernel<STAGES, FUSE, EPI>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     attr_note_current_device(&attr_mask);
   }
-  ns_tc2_kernel<STAGES, PREFETCH, FUSE, EPI><<<2 * n_pairs, threads_of<EPI>(), smem, st>>>(L);
+  ns_tc2_kernel<STAGES, FUSE, EPI><<<2 * n_pairs, threads_of<EPI>(), smem, st>>>(L);
   return cudaGetLastError();
 }
 
-template <int STAGES, bool PREFETCH>
+// The fused update keeps 4 epilogue warps: it runs on long main loops only
+// (short ones store X and update in a separate pass), where more concurrent
+// W traffic slows the operand copies (measured +5 ms per Llama-3-8B step
+// with 8 warps and an aux-free epilogue).
+template <int STAGES>
 static cudaError_t launch_variant(const NsLaunch& L, int n_pairs, cudaStream_t st) {
-  if (L.fuse_update) return launch_variant3<STAGES, PREFETCH, true, 4>(L, n_pairs, st);
-  return L.epi8 ? launch_variant3<STAGES, PREFETCH, false, 8>(L, n_pairs, st)
-                : launch_variant3<STAGES, PREFETCH, false, 4>(L, n_pairs, st);
+  if (L.fuse_update) return launch_variant3<STAGES, true, 4>(L, n_pairs, st);
+  return L.epi8 ? launch_variant3<STAGES, false, 8>(L, n_pairs, st) : launch_variant3<STAGES, false, 4>(L, n_pairs, st);
 }
 
 cudaError_t launch_ns_tc2(const NsLaunch& L, int n_pairs, cudaStream_t st) {
   if (n_pairs <= 0) return cudaSuccess;
-  if (g_tc2_stages == 5)
-    return g_tc2_prefetch ? launch_variant<5, true>(L, n_pairs, st) : launch_variant<5, false>(L, n_pairs, st);
-  return g_tc2_prefetch ? launch_variant<4, true>(L, n_pairs, st) : launch_variant<4, false>(L, n_pairs, st);
+  return (g_tc2_stages == 5) ? launch_variant<5>(L, n_pairs, st) : launch_variant<4>(L, n_pairs, st);
 }
 
 // Largest number of CTA pairs of this kernel that can be resident at once.
@@ -376,7 +372,7 @@ int ns_tc2_max_pairs() {
   static int cached = -1;
   if (cached >= 0) return cached;
   constexpr size_t smem = smem_bytes<5, 8>();
-  if (cudaFuncSetAttribute(ns_tc2_kernel<5, true, false, 8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(ns_tc2_kernel<5, false, 8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem)) != cudaSuccess) {
     cudaGetLastError();
     return cached = 0;
@@ -386,7 +382,7 @@ int ns_tc2_max_pairs() {
   cfg.blockDim = dim3(threads_of<8>(), 1, 1);
   cfg.dynamicSmemBytes = smem;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, ns_tc2_kernel<5, true, false, 8>, &cfg) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&n, ns_tc2_kernel<5, false, 8>, &cfg) != cudaSuccess) {
     cudaGetLastError();
     n = 0;
   }

@@ -23,11 +23,11 @@
 namespace dmuon {
 
 // Process-wide tuning switches (dmuon_set_tuning; defined in api.cu).
-extern int g_ns_pairs, g_tile_order, g_tri, g_tc2_stages_sel, g_tc2_prefetch_sel, g_fold_diag, g_epi8_below,
+extern int g_ns_pairs, g_tile_order, g_tri, g_tc2_stages_sel, g_fold_diag, g_epi8_below,
     g_mom_groups;
 extern int64_t g_group_min_elems, g_host_group_min_elems;
 void set_tc_mn_swap(int v);
-void set_tc2_variant(int stages, int prefetch);
+void set_tc2_variant(int stages);
 
 // Plan slots of a context: 0 = one-group step, 1.. = overlapped momentum
 // groups, 65.. = host-pipeline groups.
