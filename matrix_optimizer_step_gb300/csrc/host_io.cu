@@ -6,6 +6,9 @@
 namespace dmuon {
 namespace {
 
+// Tensor count above which the host-buffer step uses equal group shares.
+constexpr int kShapedMaxTensors = 512;
+
 // ------------------------------------------------------------ host pipeline
 // Id of the CUDA allocation holding `p` (0 when the driver does not know it).
 uint64_t buffer_id(const void* p) {
@@ -78,10 +81,13 @@ std::vector<std::pair<int, int>> split_groups(const dmuon_matrix* mats, int n, i
   // Shares grow from both ends, 2^min(g, G-1-g, 3): the first group's
   // gradients (copied before any compute) and the last group's parameters
   // (copied after all compute) are small, the middle groups large and few.
+  // With many tensors the copies' fixed cost (several microseconds each)
+  // dominates instead, and equal groups spread it evenly over the step.
+  const bool shaped = n <= kShapedMaxTensors;
   std::vector<double> share(static_cast<size_t>(groups));
   double wsum = 0.0;
   for (int g = 0; g < groups; ++g) {
-    share[static_cast<size_t>(g)] = double(1 << std::min(std::min(g, groups - 1 - g), 3));
+    share[static_cast<size_t>(g)] = shaped ? double(1 << std::min(std::min(g, groups - 1 - g), 3)) : 1.0;
     wsum += share[static_cast<size_t>(g)];
   }
   std::vector<std::pair<int, int>> out;
