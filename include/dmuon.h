@@ -204,6 +204,11 @@ DMUON_API int dmuon_context_destroy(dmuon_context* ctx);
  * DMUON_ERR_TIMEOUT.  Muon steps on one context must not overlap on the
  * GPU (they share the context's workspace); an AdamW step of the same
  * context may run concurrently on another stream.
+ * A call whose tensor list, pointers and settings are unchanged since the
+ * previous call on the context enqueues kernel launches only (plan, tables
+ * and tensor maps are reused), so it can be captured into a CUDA graph and
+ * replayed; the graph fixes the hyper-parameters it was captured with.  The
+ * same holds for dmuon_adamw_step (whose step counter is then fixed too).
  */
 DMUON_API int dmuon_muon_step(dmuon_context* ctx, const dmuon_matrix* mats, int32_t n,
                     float lr, float momentum, float wd, int32_t ns_steps,
