@@ -65,8 +65,8 @@ int ensure_events(dmuon_context* ctx, size_t count) {
   return DMUON_OK;
 }
 
-// Consecutive groups of about equal Newton-Schulz work (element count when
-// there are no iterations), every group non-empty.
+// Consecutive groups by Newton-Schulz work (element count when there are no
+// iterations), every group non-empty; the shares are set below.
 std::vector<std::pair<int, int>> split_groups(const dmuon_matrix* mats, int n, int groups, int ns_steps) {
   std::vector<double> cost(static_cast<size_t>(n));
   double total = 0.0;

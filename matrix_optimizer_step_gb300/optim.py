@@ -8,6 +8,8 @@ marshals: every step runs in the CUDA library through the C ABI.
 
 from __future__ import annotations
 
+import ctypes
+
 import torch
 
 from . import capi
@@ -158,9 +160,9 @@ class OwnerStep:
         use_adam = adamw is not None and self._vecs is not None and self._vec_io is not None
         ah = capi.adamw_hparams(**adamw) if use_adam else None
         capi._check(capi.load_library().dmuon_step_host(
-            self.ctx, self._mats, self._mat_io, self._n_mats, capi.ctypes.byref(mh),
+            self.ctx, self._mats, self._mat_io, self._n_mats, ctypes.byref(mh),
             self._vecs if use_adam else None, self._vec_io if use_adam else None,
-            self._n_vecs if use_adam else 0, capi.ctypes.byref(ah) if use_adam else None,
+            self._n_vecs if use_adam else 0, ctypes.byref(ah) if use_adam else None,
             int(n_groups), capi._stream_handle(stream)))
 
     # ------------------------------------------------------------ misc
