@@ -300,18 +300,23 @@ def test_pair_kernel_agrees_with_one_cta_kernel(cuda_lib):
 VARIANT_SHAPES = [(256, 512), (512, 256), (520, 520), (200, 328), (1000, 130), (3, 4), (2, 96, 160)]
 
 
-@pytest.mark.parametrize("key,value", [(3, 5), (4, 0), (6, 0), (7, 0), (8, 0), (8, 1000000)])
-def test_pair_kernel_tuning_variants(cuda_lib, key, value):
+TUNING_DEFAULTS = {3: 4, 4: 1, 6: 1, 7: 1, 8: 32}
+
+
+@pytest.mark.parametrize("settings", [{3: 5}, {4: 0}, {6: 0}, {7: 0}, {8: 0}, {8: 1000000}, {8: 0, 7: 0}])
+def test_pair_kernel_tuning_variants(cuda_lib, settings):
     """5-stage ring, rows-outer tile order, mirrored symmetric outputs, a*X
-    added in every Combine epilogue (so the fused update reads aux), 4 or 8
-    epilogue warps in every launch: each selectable variant of the CTA-pair
-    kernel against the oracle."""
-    defaults = {3: 4, 4: 1, 6: 1, 7: 1, 8: 32}
-    cuda_lib.dmuon_set_tuning(key, value)
+    added in every Combine epilogue, 4 or 8 epilogue warps in every launch,
+    and the update fused into every step's last Combine (key 8 = 0), with
+    and without an aux operand there: each selectable variant of the
+    CTA-pair kernel against the oracle."""
     try:
-        res = run_muon(cuda_lib, VARIANT_SHAPES, seed=30 + key)[0]
+        for key, value in settings.items():
+            cuda_lib.dmuon_set_tuning(key, value)
+        res = run_muon(cuda_lib, VARIANT_SHAPES, seed=30 + sum(settings))[0]
     finally:
-        cuda_lib.dmuon_set_tuning(key, defaults[key])
+        for key in settings:
+            cuda_lib.dmuon_set_tuning(key, TUNING_DEFAULTS[key])
     for r in res:
         assert r["buf"] <= 1e-6 and r["param_exact"], r
         assert max(r["O_slices"]) <= bf16_tol(r["shape"]), r
