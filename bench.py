@@ -33,9 +33,11 @@ sys.path.insert(0, ROOT)
 
 L2_BYTES = 129 * 1024 * 1024  # GB300 L2
 
-# Sources compiled into the CTA-pair NS kernel: DRAM traffic measured by ncu
-# is reported only while all of them are unchanged since the capture.
-KERNEL_SOURCES = ("k_ns_tc2.cu", "ns_epilogue.cuh", "ptx.cuh", "internal.h")
+# Sources of the CTA-pair NS kernel and of the tile lists it runs (plan.cu
+# builds and balances them, step.cu picks one per launch): DRAM traffic
+# measured by ncu is reported only while all of them are unchanged since the
+# capture.
+KERNEL_SOURCES = ("k_ns_tc2.cu", "ns_epilogue.cuh", "ptx.cuh", "internal.h", "plan.cu", "step.cu")
 
 
 def kernel_source_sha():

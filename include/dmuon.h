@@ -380,6 +380,10 @@ DMUON_API int dmuon_selftest_wait_timeout(dmuon_context* ctx, int32_t timeout_us
  *          default 1024).
  *   key 11: smallest group of dmuon_step_host, in units of 2^10 elements
  *          (1..2^20, default 32768).
+ *   key 12: CTA-pair kernel: a launch (other than a fused update) whose
+ *          tiles average at least `value` 64-deep k-blocks runs 256 x 512
+ *          tiles wherever two adjacent column blocks exist (0..1e6, default
+ *          128; 0 = never).  Results do not depend on the setting.
  * Returns DMUON_ERR_INVALID_ARG for an unknown key.  Not thread-safe with
  * respect to concurrent steps.
  */

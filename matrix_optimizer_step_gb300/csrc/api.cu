@@ -25,6 +25,11 @@ int g_fold_diag = 1;
 // CTA-pair kernel: launches whose tiles average fewer 64-deep k-blocks than
 // this drain their accumulators with 8 epilogue warps instead of 4.
 int g_epi8_below = 32;
+// CTA-pair kernel: launches whose tiles average at least this many k-blocks
+// use 256 x 512 tiles where two column blocks fit (0 = never).
+// Measured on the Llama-3-8B and MoE sets: the Gram launches (mean 157 and
+// 224 k-blocks) gain 3-6 %; Poly and Combine (64) lose.
+int g_wide_min_kb = 128;
 // Momentum overlapped with Newton-Schulz: a large tensor list is cut into
 // this many groups with disjoint workspace regions, and group g+1's
 // momentum pass (HBM-bound) runs on a side stream while group g's
@@ -454,6 +459,11 @@ int dmuon_set_tuning(int32_t key, int32_t value) {
   if (key == 11) {
     if (value < 1 || value > (1 << 20)) return set_error(DMUON_ERR_INVALID_ARG, "set_tuning: key 11 value outside [1, 2^20]");
     g_host_group_min_elems = int64_t(value) << 10;
+    return DMUON_OK;
+  }
+  if (key == 12) {
+    if (value < 0 || value > 1000000) return set_error(DMUON_ERR_INVALID_ARG, "set_tuning: key 12 value outside [0, 1e6]");
+    g_wide_min_kb = value;
     return DMUON_OK;
   }
   if (key == 4) {

@@ -117,6 +117,10 @@ struct NsProblem {
 // as fp32 here and costs 2 bytes per element instead of 4.
 enum NsKind : int { kGram = 0, kPoly = 1, kCombine = 2 };
 
+// CTA-pair tile lists: bit 31 of a tile's problem index marks a 256 x 512
+// tile (column blocks tile_n and tile_n + 1).
+constexpr uint32_t kTileWideBit = 0x80000000u, kTileProbMask = 0x7FFFFFFFu;
+
 struct NsLaunch {
   const NsProblem* probs;
   const uint2* tiles;       // x = problem index, y = (tile_m << 16) | tile_n
@@ -143,6 +147,9 @@ struct NsLaunch {
   float diag;
   // CTA-pair kernel: 8 epilogue warps instead of 4 (not with fuse_update).
   int32_t epi8;
+  // CTA-pair kernel: the tile list holds 256 x 512 tiles (kTileWideBit);
+  // needs tri, excludes fuse_update.
+  int32_t wide;
 };
 
 // ---- launch wrappers (each returns the cudaError_t of its launch) ----

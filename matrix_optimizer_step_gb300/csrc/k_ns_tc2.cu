@@ -27,6 +27,19 @@
 // loaded from the transposed stored block as an M/N-contiguous tile, and the
 // MMA descriptor for that k-block says so (NsProblem::tri).
 //
+// Wide tiles (the WIDE instantiation): a tile may instead be 256 x 512, two
+// adjacent 256-column blocks that share the A rows.  Per k-block each CTA
+// then loads 128 rows of A and 2 x 128 rows of B (48 KiB, 3-stage ring) and
+// the leader issues two MMAs into two 256-column accumulators: 1.5x the
+// operand bytes for 2x the multiply-adds, which pays where the main loop is
+// long and the operand copies set the pace.  The two accumulators fill all
+// 512 TMEM columns, so a wide tile is not double-buffered against the next
+// one; the accumulator "slots" (column halves) are handed out in sequence
+// (a narrow tile takes one, a wide tile two), and each slot has its own
+// full/empty barriers.  In a wide tile the 4 epilogue warps of column half
+// h drain slot h's 256 columns and arrive twice on its empty barrier, so
+// every slot use still counts 16 arrivals.
+//
 // Every spin-wait is bounded; on a timeout the CTA records the error, stops
 // issuing, and both CTAs meet at the final cluster barrier before the pair
 // frees its TMEM.
@@ -44,7 +57,10 @@ namespace {
 constexpr int TILE = kTc2Tile;  // 256 x 256 per CTA pair
 constexpr int BK = 64;
 constexpr uint32_t HALF_BYTES = 128 * BK * 2;         // 16 KiB: 128 rows x 64 k, bf16
-constexpr uint32_t STAGE_BYTES = 2 * HALF_BYTES;      // A half + B half per CTA
+template <bool WIDE>
+__host__ __device__ constexpr uint32_t stage_bytes() {
+  return (WIDE ? 3 : 2) * HALF_BYTES;  // A half + one (or two) B halves per CTA
+}
 constexpr uint32_t MN_BOX_BYTES = 64 * 64 * 2;        // 8 KiB
 // Warps: 0 A producer, 1 MMA, 2 .. 2+EPI-1 epilogue, 2+EPI B producer.  The
 // epilogue has EPI = 4 warps (one per TMEM lane quarter) or 8 (two per lane
@@ -60,11 +76,13 @@ constexpr int threads_of() {
 }
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kStagingPerWarp = 2 * 4096;  // 2 boxes of 32 x 64 bf16
-template <int STAGES, int EPI>
+template <int STAGES, int EPI, bool WIDE = false>
 constexpr size_t smem_bytes() {
-  return 1024 + STAGES * STAGE_BYTES + EPI * kStagingPerWarp + (2 * STAGES + 5) * 8 + 16;
+  return 1024 + STAGES * stage_bytes<WIDE>() + EPI * kStagingPerWarp + (2 * STAGES + 5) * 8 + 16;
 }
 static_assert(smem_bytes<5, 8>() <= 227 * 1024, "shared memory budget");
+// 3 stages of 48 KiB: a fourth does not fit beside 8 warps' staging boxes.
+static_assert(smem_bytes<3, 8, true>() <= 227 * 1024, "shared memory budget (wide)");
 // Every CTA allocates all 512 TMEM columns, so two CTAs must never share an
 // SM: a second resident pair could hold one SM's TMEM while its partner waits
 // for the other's.  Asking for more than half of the SM's 228 KiB of shared
@@ -85,14 +103,16 @@ struct TileInfo {
   int m0, n0;  // tile origin (rows, columns) of the pair
   int map_a, map_b, z, majors, nk;
   int tri, map_a_t, map_b_t;
+  int wide;    // 1: 256 x 512 (two column blocks)
 };
 
 __device__ __forceinline__ TileInfo load_tile_info(const NsLaunch& L, int t) {
   const uint2 tile = L.tiles[t];
-  const NsProblem& P = L.probs[tile.x];
+  const NsProblem& P = L.probs[tile.x & kTileProbMask];
   TileInfo I;
   I.m0 = static_cast<int>(tile.y >> 16) * TILE;
   I.n0 = static_cast<int>(tile.y & 0xFFFFu) * TILE;
+  I.wide = (tile.x & kTileWideBit) ? 1 : 0;
   I.map_a = P.map_a;
   I.map_b = P.map_b;
   I.z = P.z;
@@ -112,10 +132,13 @@ __device__ __forceinline__ bool tri_below(int tri_bit, int k0, int row0) {
 }
 
 // FUSE: the last Combine, which applies the update instead of storing X.
-template <int STAGES, bool FUSE, int EPI>
+// WIDE: the tile list may hold 256 x 512 tiles.
+template <int STAGES, bool FUSE, int EPI, bool WIDE = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_of<EPI>(), 1)
     ns_tc2_kernel(const NsLaunch L) {
   static_assert(EPI == 4 || (EPI == 8 && !FUSE), "epilogue warp count");
+  static_assert(!WIDE || (EPI == 8 && !FUSE), "wide tiles: 8 epilogue warps, no fused update");
+  constexpr uint32_t STAGE_BYTES = stage_bytes<WIDE>();
   constexpr int kProducerBWarp = 2 + EPI;
   constexpr int kNumBars = 2 * STAGES + 2 + 2 + 1;
   extern __shared__ uint8_t smem_raw[];
@@ -183,15 +206,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_of<EPI>(), 1
     for (int t = t_begin; t < t_end && ok; ++t) {
       if (t + 1 < t_end) nxt = load_tile_info(L, t + 1);
       const int tile_row0 = which ? cur.n0 : cur.m0;
-      const int row0 = tile_row0 + 128 * static_cast<int>(rank);
       const CUtensorMap* map = L.maps + (which ? cur.map_b : cur.map_a);
       const CUtensorMap* map_t = L.maps + (which ? cur.map_b_t : cur.map_a_t);
       const bool mn = ((cur.majors >> which) & 1) != 0;
       const bool tri = ((cur.tri >> which) & 1) != 0;
       const int z = cur.z;
       const int nk = cur.nk;
-      // k-blocks before the operand's diagonal block come transposed.
-      const int n_below = tri ? min(nk, (tile_row0 >> 8) * (256 / BK)) : 0;
+      // B of a wide tile: two 256-row blocks of the operand.
+      const int nsub = (WIDE && which && cur.wide) ? 2 : 1;
       cur = nxt;
       for (int kb = 0; kb < nk; ++kb) {
         if (!mbar_wait_bounded_cluster(empty(stage), phase ^ 1u, abort_flag, L.err, kErrTimeoutProducer)) {
@@ -199,18 +221,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_of<EPI>(), 1
           break;
         }
         const uint32_t leader_full = mapa_shared(full(stage), 0);
-        if (leader) mbar_expect_tx(full(stage), 2 * HALF_BYTES);
+        if (leader) mbar_expect_tx(full(stage), 2 * HALF_BYTES * static_cast<uint32_t>(nsub));
         ++fills[stage];
-        const uint32_t dst = ring + stage * STAGE_BYTES + dst_off;
         const int k0 = kb * BK;
-        if (kb < n_below) {
-          tma_load_3d_pair(dst, map_t, leader_full, row0, k0, z);
-          tma_load_3d_pair(dst + MN_BOX_BYTES, map_t, leader_full, row0 + 64, k0, z);
-        } else if (!mn) {
-          tma_load_3d_pair(dst, map, leader_full, k0, row0, z);
-        } else {
-          tma_load_3d_pair(dst, map, leader_full, row0, k0, z);
-          tma_load_3d_pair(dst + MN_BOX_BYTES, map, leader_full, row0 + 64, k0, z);
+        for (int h = 0; h < nsub; ++h) {
+          const int blk_row0 = tile_row0 + TILE * h;
+          const int row0 = blk_row0 + 128 * static_cast<int>(rank);
+          const uint32_t dst = ring + stage * STAGE_BYTES + dst_off + static_cast<uint32_t>(h) * HALF_BYTES;
+          // k-blocks before the operand block's diagonal block come transposed.
+          if (tri && (k0 >> 8) < (blk_row0 >> 8)) {
+            tma_load_3d_pair(dst, map_t, leader_full, row0, k0, z);
+            tma_load_3d_pair(dst + MN_BOX_BYTES, map_t, leader_full, row0 + 64, k0, z);
+          } else if (!mn) {
+            tma_load_3d_pair(dst, map, leader_full, k0, row0, z);
+          } else {
+            tma_load_3d_pair(dst, map, leader_full, row0, k0, z);
+            tma_load_3d_pair(dst + MN_BOX_BYTES, map, leader_full, row0 + 64, k0, z);
+          }
         }
         if (++stage == STAGES) {
           stage = 0;
@@ -235,25 +262,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_of<EPI>(), 1
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      int local = 0;
+      int use = 0;  // accumulator slot uses so far (slot = use & 1)
       TileInfo cur{}, nxt{};
       if (t_begin < t_end) cur = load_tile_info(L, t_begin);
-      for (int t = t_begin; t < t_end && ok; ++t, ++local) {
+      for (int t = t_begin; t < t_end && ok; ++t) {
         if (t + 1 < t_end) nxt = load_tile_info(L, t + 1);
         const bool a_mn = (cur.majors & 1) != 0;
         const bool b_mn = (cur.majors & 2) != 0;
         const int tri = cur.tri;
         const int tile_m0 = cur.m0, tile_n0 = cur.n0;
         const int nk = cur.nk;
+        const int nsub = (WIDE && cur.wide) ? 2 : 1;
         cur = nxt;
-        const int acc = local & 1;
-        const uint32_t acc_phase = static_cast<uint32_t>(local >> 1) & 1u;
-        if (!mbar_wait_bounded_cluster(tempty(acc), acc_phase ^ 1u, abort_flag, L.err, kErrTimeoutMma)) {
-          ok = false;
-          break;
+        for (int h = 0; h < nsub && ok; ++h) {
+          const int u = use + h;
+          if (!mbar_wait_bounded_cluster(tempty(u & 1), (static_cast<uint32_t>(u >> 1) & 1u) ^ 1u, abort_flag, L.err,
+                                         kErrTimeoutMma))
+            ok = false;
         }
+        if (!ok) break;
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * TILE);
         for (int kb = 0; kb < nk; ++kb) {
           if (!mbar_wait_bounded_cluster(full(stage), phase, abort_flag, L.err, kErrTimeoutMma)) {
             ok = false;
@@ -261,15 +289,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_of<EPI>(), 1
           }
           tc_fence_after();
           const uint32_t sa = ring + stage * STAGE_BYTES;
-          const uint32_t sb = sa + HALF_BYTES;
           const bool a_is_mn = a_mn || tri_below(tri & 1, kb * BK, tile_m0);
-          const bool b_is_mn = b_mn || tri_below(tri & 2, kb * BK, tile_n0);
-          const uint32_t idesc = idesc_bf16_f32(TILE, TILE, a_is_mn, b_is_mn);
+          for (int h = 0; h < nsub; ++h) {
+            const uint32_t sb = sa + HALF_BYTES + static_cast<uint32_t>(h) * HALF_BYTES;
+            const bool b_is_mn = b_mn || tri_below(tri & 2, kb * BK, tile_n0 + TILE * h);
+            const uint32_t idesc = idesc_bf16_f32(TILE, TILE, a_is_mn, b_is_mn);
+            const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(((use + h) & 1) * TILE);
 #pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk) {
-            const uint64_t ad = a_is_mn ? desc_mn(sa, kk) : desc_k(sa, kk);
-            const uint64_t bd = b_is_mn ? desc_mn(sb, kk) : desc_k(sb, kk);
-            umma_bf16_pair(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+            for (int kk = 0; kk < BK / 16; ++kk) {
+              const uint64_t ad = a_is_mn ? desc_mn(sa, kk) : desc_k(sa, kk);
+              const uint64_t bd = b_is_mn ? desc_mn(sb, kk) : desc_k(sb, kk);
+              umma_bf16_pair(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+            }
           }
           umma_commit_pair_multicast(empty(stage), 0x3);
           if (++stage == STAGES) {
@@ -277,7 +308,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_of<EPI>(), 1
             phase ^= 1u;
           }
         }
-        if (ok) umma_commit_pair_multicast(tfull(acc), 0x3);
+        if (ok)
+          for (int h = 0; h < nsub; ++h) umma_commit_pair_multicast(tfull((use + h) & 1), 0x3);
+        use += nsub;
       }
       umma_commit_pair_multicast(drain, 0x1);
       volatile int no_abort = 0;
@@ -289,34 +322,46 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_of<EPI>(), 1
     // the two warps of one lane quarter take one column half each.
     const int quarter = warp & 3;
     const int half = (warp - 2) >> 2;
-    const int c_begin = (EPI == 8) ? 4 * half : 0;
-    const int c_end = (EPI == 8) ? c_begin + 4 : 8;
     const int row_in_tile = 128 * static_cast<int>(rank) + quarter * 32 + lane;
     const uint32_t my_staging = staging + static_cast<uint32_t>(warp - 2) * kStagingPerWarp;
     uint32_t box_count = 0;
-    int local = 0;
-    for (int t = t_begin; t < t_end; ++t, ++local) {
+    int use = 0;  // accumulator slot uses so far, as counted by the MMA issuer
+    for (int t = t_begin; t < t_end; ++t) {
       const uint2 tile = L.tiles[t];
-      const NsProblem& P = L.probs[tile.x];
+      const NsProblem& P = L.probs[tile.x & kTileProbMask];
       const int tm = static_cast<int>(tile.y >> 16), tn = static_cast<int>(tile.y & 0xFFFFu);
-      const int acc = local & 1;
-      const uint32_t acc_phase = static_cast<uint32_t>(local >> 1) & 1u;
+      const bool wide = WIDE && (tile.x & kTileWideBit) != 0;
+      // Narrow tile: every warp drains its column window of the one slot.
+      // Wide tile: the warps of column half h drain all 256 columns of slot
+      // (use + h), i.e. column block tn + h of the output.
+      const int u = wide ? use + half : use;
+      const int acc = u & 1;
+      const uint32_t acc_phase = static_cast<uint32_t>(u >> 1) & 1u;
+      const int sub_tn = wide ? tn + half : tn;
+      const int c_begin = (EPI == 8 && !wide) ? 4 * half : 0;
+      const int c_end = (EPI == 8 && !wide) ? c_begin + 4 : 8;
+      use += wide ? 2 : 1;
       if (!mbar_wait_bounded_cluster(tfull(acc), acc_phase, abort_flag, L.err, kErrTimeoutEpilogue)) break;
       tc_fence_after();
       const uint32_t t_lane =
           tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * TILE);
       if (FUSE)
-        ns_epilogue_tile<true>(L, P, tm * TILE, tn * TILE, row_in_tile, t_lane, false);
+        ns_epilogue_tile<true>(L, P, tm * TILE, sub_tn * TILE, row_in_tile, t_lane, false);
       else
-        ns_epilogue_tile_staged(L, P, tm * TILE, tn * TILE, row_in_tile, t_lane, !L.tri && P.sym && tm < tn,
+        ns_epilogue_tile_staged(L, P, tm * TILE, sub_tn * TILE, row_in_tile, t_lane, !L.tri && P.sym && tm < sub_tn,
                                 my_staging, box_count, c_begin, c_end);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
-        if (leader)
-          mbar_arrive(tempty(acc));
-        else
-          mbar_arrive_cluster(mapa_shared(tempty(acc), 0));
+        // A wide tile's slot is drained by half of the warps: each arrives
+        // twice, so the slot's empty barrier completes on the same count.
+        const int arrivals = wide ? 2 : 1;
+        for (int i = 0; i < arrivals; ++i) {
+          if (leader)
+            mbar_arrive(tempty(acc));
+          else
+            mbar_arrive_cluster(mapa_shared(tempty(acc), 0));
+        }
       }
     }
     if (lane == 0) bulk_wait_group<0>();  // staged TMA stores complete
@@ -338,17 +383,17 @@ static int g_tc2_stages = 4;
 
 void set_tc2_variant(int stages) { g_tc2_stages = (stages == 5) ? 5 : 4; }
 
-template <int STAGES, bool FUSE, int EPI>
+template <int STAGES, bool FUSE, int EPI, bool WIDE = false>
 static cudaError_t launch_variant3(const NsLaunch& L, int n_pairs, cudaStream_t st) {
   static unsigned long long attr_mask = 0;
-  constexpr size_t smem = smem_bytes<STAGES, EPI>();
+  constexpr size_t smem = smem_bytes<STAGES, EPI, WIDE>();
   if (attr_needed_on_current_device(&attr_mask)) {
-    cudaError_t e = cudaFuncSetAttribute(ns_tc2_kernel<STAGES, FUSE, EPI>,
+    cudaError_t e = cudaFuncSetAttribute(ns_tc2_kernel<STAGES, FUSE, EPI, WIDE>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     attr_note_current_device(&attr_mask);
   }
-  ns_tc2_kernel<STAGES, FUSE, EPI><<<2 * n_pairs, threads_of<EPI>(), smem, st>>>(L);
+  ns_tc2_kernel<STAGES, FUSE, EPI, WIDE><<<2 * n_pairs, threads_of<EPI>(), smem, st>>>(L);
   return cudaGetLastError();
 }
 
@@ -364,6 +409,10 @@ static cudaError_t launch_variant(const NsLaunch& L, int n_pairs, cudaStream_t s
 
 cudaError_t launch_ns_tc2(const NsLaunch& L, int n_pairs, cudaStream_t st) {
   if (n_pairs <= 0) return cudaSuccess;
+  if (L.wide) {
+    if (L.fuse_update || !L.tri) return cudaErrorInvalidValue;  // not built for these
+    return launch_variant3<3, false, 8, true>(L, n_pairs, st);
+  }
   return (g_tc2_stages == 5) ? launch_variant<5>(L, n_pairs, st) : launch_variant<4>(L, n_pairs, st);
 }
 

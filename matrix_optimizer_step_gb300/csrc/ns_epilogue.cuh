@@ -245,9 +245,9 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
 // warp's stores hit distinct banks) and lane 0 writes the box with one TMA
 // tile store (asynchronous, edges clipped by the hardware).  Two 4 KiB
 // buffers per warp alternate; before refilling one, lane 0 waits until the
-// store issued two boxes earlier has finished reading it.  The optional fp32
-// copy (first iteration) and the mirrored copy (when symmetric outputs are
-// not kept as upper blocks) are still stored directly.  The warp covers the
+// store issued two boxes earlier has finished reading it.  The mirrored
+// copy (when symmetric outputs are not kept as upper blocks) is still
+// stored directly.  The warp covers the
 // 32-column chunks [c_begin, c_end) of the tile (c_begin even: whole boxes).
 __device__ __forceinline__ void ns_epilogue_tile_staged(const NsLaunch& L, const NsProblem& P, int m0, int n0,
                                                         int row_in_tile, uint32_t t_lane, bool mirror,

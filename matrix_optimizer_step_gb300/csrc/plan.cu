@@ -49,33 +49,51 @@ int make_map(EncodeTiledFn enc, CUtensorMap* out, void* base, int64_t inner, int
 
 // Build the tile list of one phase and balance it over persistent CTAs.
 // Tile geometry: 0 = fp32 CUDA-core tiles, 1 = one-CTA tcgen05 tiles,
-// 2 = CTA-pair tcgen05 tiles.  `slots` = persistent CTAs (or CTA pairs).
+// 2 = CTA-pair tcgen05 tiles, 3 = CTA-pair tiles where two adjacent column
+// blocks of one row block form a 256 x 512 tile (kTileWideBit) wherever both
+// exist (for a symmetric output: both on or above the diagonal).
+// `slots` = persistent CTAs (or CTA pairs).
 int build_phase_tiles(const std::vector<NsProblem>& probs, int geometry, int slots, PhaseTiles& out) {
   const bool fp32 = geometry == 0;
+  const bool wide = geometry == 3;
   const int bm = geometry == 0 ? kSimtBM : geometry == 1 ? kTcBM : kTc2Tile;
   const int bn = geometry == 0 ? kSimtBN : geometry == 1 ? kTcBN : kTc2Tile;
   std::vector<uint2> tiles;
   std::vector<int64_t> cost;
+  double kb_sum = 0.0;
   for (size_t p = 0; p < probs.size(); ++p) {
     const NsProblem& P = probs[p];
     const int tm = (P.M + bm - 1) / bm, tn = (P.N + bn - 1) / bn;
-    const int64_t c = (P.K + kTcBK - 1) / kTcBK + 2;
+    if (tm > 0xFFFF || tn > 0xFFFF) return set_error(DMUON_ERR_SHAPE, "matrix too large for the tile index");
+    const int64_t kb = (P.K + kTcBK - 1) / kTcBK;
+    // A wide tile moves 1.5x the operand bytes of a narrow one per k-block.
+    const int64_t c = kb + 2, c_wide = kb + kb / 2 + 3;
+    auto add = [&](int i, int j, bool w) {
+      const uint32_t x = static_cast<uint32_t>(p) | (w ? kTileWideBit : 0u);
+      tiles.push_back(make_uint2(x, (static_cast<uint32_t>(i) << 16) | static_cast<uint32_t>(j)));
+      cost.push_back(w ? c_wide : c);
+      kb_sum += static_cast<double>(kb);
+    };
     // Tiles of equal cost run in list order, so consecutive tiles run at the
     // same time: walk the longer tile dimension in the outer loop, so a wave
     // shares few panels of the larger operand (which then stay in L2).
     const bool n_outer = g_tile_order && tn > tm;
-    for (int a = 0; a < (n_outer ? tn : tm); ++a)
-      for (int b = 0; b < (n_outer ? tm : tn); ++b) {
-        const int i = n_outer ? b : a, j = n_outer ? a : b;
-        if (P.sym && (i * bm) / bn > j) continue;  // below the diagonal: mirrored
-        tiles.push_back(make_uint2(static_cast<uint32_t>(p), (static_cast<uint32_t>(i) << 16) | static_cast<uint32_t>(j)));
-        cost.push_back(c);
+    const int jstep = wide ? 2 : 1;
+    if (n_outer) {
+      for (int j = 0; j < tn; j += jstep)
+        for (int i = 0; i < tm; ++i) {
+          if (P.sym && (i * bm) / bn > j) continue;  // below the diagonal: mirrored
+          add(i, j, wide && j + 1 < tn);
+        }
+    } else {
+      for (int i = 0; i < tm; ++i) {
+        const int j0 = P.sym ? (i * bm) / bn : 0;  // first block on or above the diagonal
+        for (int j = j0; j < tn; j += (wide && j + 1 < tn) ? 2 : 1) add(i, j, wide && j + 1 < tn);
       }
+    }
   }
   out.n_tiles = static_cast<int32_t>(tiles.size());
-  double kb = 0.0;
-  for (int64_t c : cost) kb += static_cast<double>(c - 2);
-  out.mean_kblocks = tiles.empty() ? 0.0 : kb / static_cast<double>(tiles.size());
+  out.mean_kblocks = tiles.empty() ? 0.0 : kb_sum / static_cast<double>(tiles.size());
   if (fp32) {
     out.n_ctas = out.n_tiles;
     int st = upload(out.tiles, tiles);
@@ -407,6 +425,8 @@ int build_muon_plan(dmuon_context* ctx, MuonPlan& P, const dmuon_matrix* mats, i
       if (st != DMUON_OK) return st;
       const int pairs = std::max(1, std::min(ctx->num_sms / 2, ns_tc2_max_pairs()));
       st = build_phase_tiles(var[kind][0], 2, pairs, P.phase2[kind]);
+      if (st != DMUON_OK) return st;
+      st = build_phase_tiles(var[kind][0], 3, pairs, P.phase2w[kind]);
       if (st != DMUON_OK) return st;
     }
   }

@@ -24,7 +24,7 @@ namespace dmuon {
 
 // Process-wide tuning switches (dmuon_set_tuning; defined in api.cu).
 extern int g_ns_pairs, g_tile_order, g_tri, g_tc2_stages_sel, g_fold_diag, g_epi8_below,
-    g_mom_groups;
+    g_mom_groups, g_wide_min_kb;
 extern int64_t g_group_min_elems, g_host_group_min_elems;
 void set_tc_mn_swap(int v);
 void set_tc2_variant(int stages);
@@ -165,6 +165,7 @@ struct MuonPlan {
   DevBuf probs[3][4], probs_f32[3][2];
   PhaseTiles phase[3];      // one-CTA tensor-core tiles
   PhaseTiles phase2[3];     // CTA-pair tensor-core tiles
+  PhaseTiles phase2w[3];    // CTA-pair tiles with 256 x 512 tiles where they fit
   PhaseTiles phase_f32[3];  // fp32 CUDA-core tiles
   void release() {
     chunks_dev.release();
@@ -176,7 +177,7 @@ struct MuonPlan {
     maps.release();
     for (auto& k : probs)
       for (auto& p : k) p.release();
-    for (auto* ph : {phase, phase2, phase_f32})
+    for (auto* ph : {phase, phase2, phase2w, phase_f32})
       for (int k = 0; k < 3; ++k) {
         ph[k].tiles.release();
         ph[k].cta_begin.release();

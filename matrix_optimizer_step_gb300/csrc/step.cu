@@ -131,7 +131,13 @@ int muon_launch_ns(dmuon_context* ctx, MuonSlot& S, float lr, float wd, int32_t 
           T.wd = wd;
         }
         T.tri = (pairs && g_tri) ? 1 : 0;
-        const PhaseTiles& PT = pairs ? P.phase2[kind] : P.phase[kind];
+        // 256 x 512 tiles where the main loops are long enough to pay for an
+        // accumulator that is not double-buffered.
+        T.wide = (T.tri && !T.fuse_update && g_wide_min_kb > 0 && P.phase2w[kind].n_tiles > 0 &&
+                  P.phase2[kind].mean_kblocks >= static_cast<double>(g_wide_min_kb))
+                     ? 1
+                     : 0;
+        const PhaseTiles& PT = pairs ? (T.wide ? P.phase2w[kind] : P.phase2[kind]) : P.phase[kind];
         T.epi8 = (!T.fuse_update && PT.mean_kblocks < static_cast<double>(g_epi8_below)) ? 1 : 0;
         T.tiles = static_cast<const uint2*>(PT.tiles.p);
         T.cta_begin = static_cast<const int32_t*>(PT.cta_begin.p);

@@ -297,19 +297,23 @@ def test_pair_kernel_agrees_with_one_cta_kernel(cuda_lib):
 
 # ----------------------------------------------- every selectable kernel path
 
-VARIANT_SHAPES = [(256, 512), (512, 256), (520, 520), (200, 328), (1000, 130), (3, 4), (2, 96, 160)]
+VARIANT_SHAPES = [(256, 512), (512, 256), (520, 520), (200, 328), (1000, 130), (3, 4), (2, 96, 160), (300, 700),
+                  (700, 600)]
 
 
-TUNING_DEFAULTS = {3: 4, 4: 1, 6: 1, 7: 1, 8: 32}
+TUNING_DEFAULTS = {3: 4, 4: 1, 6: 1, 7: 1, 8: 32, 12: 128}
 
 
-@pytest.mark.parametrize("settings", [{3: 5}, {4: 0}, {6: 0}, {7: 0}, {8: 0}, {8: 1000000}, {8: 0, 7: 0}])
+@pytest.mark.parametrize("settings", [{3: 5}, {4: 0}, {6: 0}, {7: 0}, {8: 0}, {8: 1000000}, {8: 0, 7: 0},
+                                      {12: 1}, {12: 1, 7: 0}, {12: 1, 8: 1000000}, {12: 1, 4: 0}, {12: 0}])
 def test_pair_kernel_tuning_variants(cuda_lib, settings):
     """5-stage ring, rows-outer tile order, mirrored symmetric outputs, a*X
     added in every Combine epilogue, 4 or 8 epilogue warps in every launch,
-    and the update fused into every step's last Combine (key 8 = 0), with
-    and without an aux operand there: each selectable variant of the
-    CTA-pair kernel against the oracle."""
+    the update fused into every step's last Combine (key 8 = 0), with and
+    without an aux operand there, 256 x 512 tiles in every launch they fit
+    (key 12 = 1; with aux, unfused last Combine, rows-outer order) or in
+    none (key 12 = 0): each selectable variant of the CTA-pair kernel
+    against the oracle."""
     try:
         for key, value in settings.items():
             cuda_lib.dmuon_set_tuning(key, value)

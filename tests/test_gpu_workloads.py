@@ -135,6 +135,18 @@ def test_llama3_8b_sampled(cuda_lib):
 
 
 @pytest.mark.slow
+def test_llama3_8b_sampled_wide_tiles(cuda_lib):
+    """Every launch that can (all but the fused last product) on 256 x 512
+    tiles of the CTA-pair kernel."""
+    cuda_lib.dmuon_set_tuning(12, 1)
+    try:
+        res = _run(cuda_lib, "llama3_8b", ["layers.1.v", "layers.12.o", "layers.5.up", "layers.21.down"])
+    finally:
+        cuda_lib.dmuon_set_tuning(12, 128)
+    assert len(res) == 4
+
+
+@pytest.mark.slow
 def test_moe_experts_sampled(cuda_lib):
     names = ["layers.0.experts.w1", "layers.2.experts.w2"]
     res = _run(cuda_lib, "moe_experts", names, slice_pick=[3, 7])
