@@ -15,7 +15,7 @@
 //   * tcgen05.commit with a two-CTA multicast frees the ring slot in both
 //     CTAs and hands the accumulator to both CTAs' epilogue warps, which run
 //     the shared fused epilogue on their own 128 rows and then arrive on the
-//     leader's `tempty` barrier (8 arrivals: 4 warps per CTA).
+//     leader's `tempty` barrier (one arrival per epilogue warp of both CTAs).
 // Per SM and per 16-deep k-step the operands are 128 x 16 of A and 128 x 16
 // of B (8 KiB) for 128 x 256 x 16 multiply-adds, against 12 KiB in the
 // one-CTA kernel: two thirds of the shared-memory fill and L2 read traffic
@@ -31,8 +31,9 @@
 // adjacent 256-column blocks that share the A rows.  Per k-block each CTA
 // then loads 128 rows of A and 2 x 128 rows of B (48 KiB, 3-stage ring) and
 // the leader issues two MMAs into two 256-column accumulators: 1.5x the
-// operand bytes for 2x the multiply-adds, which pays where the main loop is
-// long and the operand copies set the pace.  The two accumulators fill all
+// operand bytes for 2x the multiply-adds.  Measured, that pays only where
+// the main loop is long (the Gram of the large classes: a few per cent);
+// the host picks the launches.  The two accumulators fill all
 // 512 TMEM columns, so a wide tile is not double-buffered against the next
 // one; the accumulator "slots" (column halves) are handed out in sequence
 // (a narrow tile takes one, a wide tile two), and each slot has its own
