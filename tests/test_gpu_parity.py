@@ -298,7 +298,7 @@ def test_pair_kernel_agrees_with_one_cta_kernel(cuda_lib):
 # ----------------------------------------------- every selectable kernel path
 
 VARIANT_SHAPES = [(256, 512), (512, 256), (520, 520), (200, 328), (1000, 130), (3, 4), (2, 96, 160), (300, 700),
-                  (700, 600)]
+                  (700, 600), (2, 300, 600)]
 
 
 TUNING_DEFAULTS = {3: 4, 4: 1, 6: 1, 7: 1, 8: 32, 12: 128}
