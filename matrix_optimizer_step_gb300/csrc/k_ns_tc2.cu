@@ -291,16 +291,35 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_of<EPI>(), 1
           tc_fence_after();
           const uint32_t sa = ring + stage * STAGE_BYTES;
           const bool a_is_mn = a_mn || tri_below(tri & 1, kb * BK, tile_m0);
-          for (int h = 0; h < nsub; ++h) {
-            const uint32_t sb = sa + HALF_BYTES + static_cast<uint32_t>(h) * HALF_BYTES;
-            const bool b_is_mn = b_mn || tri_below(tri & 2, kb * BK, tile_n0 + TILE * h);
+          if (nsub == 1) {
+            const uint32_t sb = sa + HALF_BYTES;
+            const bool b_is_mn = b_mn || tri_below(tri & 2, kb * BK, tile_n0);
             const uint32_t idesc = idesc_bf16_f32(TILE, TILE, a_is_mn, b_is_mn);
-            const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(((use + h) & 1) * TILE);
+            const uint32_t d_tmem = tmem_base + static_cast<uint32_t>((use & 1) * TILE);
 #pragma unroll
             for (int kk = 0; kk < BK / 16; ++kk) {
               const uint64_t ad = a_is_mn ? desc_mn(sa, kk) : desc_k(sa, kk);
               const uint64_t bd = b_is_mn ? desc_mn(sb, kk) : desc_k(sb, kk);
               umma_bf16_pair(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+            }
+          } else {
+            // Both column halves per 16-deep k-step, the second taking A
+            // from the collector buffer the first filled.
+            const uint32_t sb0 = sa + HALF_BYTES, sb1 = sa + 2 * HALF_BYTES;
+            const bool b0_mn = b_mn || tri_below(tri & 2, kb * BK, tile_n0);
+            const bool b1_mn = b_mn || tri_below(tri & 2, kb * BK, tile_n0 + TILE);
+            const uint32_t idesc0 = idesc_bf16_f32(TILE, TILE, a_is_mn, b0_mn);
+            const uint32_t idesc1 = idesc_bf16_f32(TILE, TILE, a_is_mn, b1_mn);
+            const uint32_t d0 = tmem_base + static_cast<uint32_t>((use & 1) * TILE);
+            const uint32_t d1 = tmem_base + static_cast<uint32_t>(((use + 1) & 1) * TILE);
+#pragma unroll
+            for (int kk = 0; kk < BK / 16; ++kk) {
+              const uint64_t ad = a_is_mn ? desc_mn(sa, kk) : desc_k(sa, kk);
+              const uint64_t bd0 = b0_mn ? desc_mn(sb0, kk) : desc_k(sb0, kk);
+              const uint64_t bd1 = b1_mn ? desc_mn(sb1, kk) : desc_k(sb1, kk);
+              const uint32_t acc = (kb | kk) != 0 ? 1u : 0u;
+              umma_bf16_pair_a_fill(d0, ad, bd0, idesc0, acc);
+              umma_bf16_pair_a_lastuse(d1, ad, bd1, idesc1, acc);
             }
           }
           umma_commit_pair_multicast(empty(stage), 0x3);

@@ -291,6 +291,29 @@ __device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t adesc, 
       : "memory");
 }
 
+// Two MMAs that share A (the two column halves of a 256 x 512 tile): the
+// first reads A from shared memory into the tensor core's A collector
+// buffer, the second takes A from there and releases it, so A is read from
+// shared memory once for both.  The A descriptor must be the same.
+__device__ __forceinline__ void umma_bf16_pair_a_fill(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                                      uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16.collector::a::fill [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void umma_bf16_pair_a_lastuse(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                                         uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16.collector::a::lastuse [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Arrive once on the barrier at address `bar` in every CTA of `cta_mask`
 // when all tensor-core work issued so far by this thread has completed.
 __device__ __forceinline__ void umma_commit_pair_multicast(uint32_t bar, uint16_t cta_mask) {

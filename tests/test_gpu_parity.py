@@ -326,6 +326,33 @@ def test_pair_kernel_tuning_variants(cuda_lib, settings):
         assert max(r["O_slices"]) <= bf16_tol(r["shape"]), r
 
 
+def test_wide_tiles_bit_identical_to_narrow(cuda_lib):
+    """A 256 x 512 tile accumulates each output element over the same
+    k-steps in the same order as two 256 x 256 tiles, so a step on wide
+    tiles everywhere they fit (key 12 = 1) gives the same bits as one on
+    narrow tiles only (key 12 = 0)."""
+    shapes = [(520, 520), (300, 700), (700, 600), (2, 300, 600), (1024, 1536), (1536, 768)]
+    outs = []
+    for wide in (1, 0):
+        cuda_lib.dmuon_set_tuning(12, wide)
+        try:
+            g = torch.Generator().manual_seed(11)
+            W = [(torch.randn(s, generator=g) * 0.02).cuda() for s in shapes]
+            Bf = [torch.zeros(s).cuda() for s in shapes]
+            G = [torch.randn(s, generator=g).to(torch.bfloat16).cuda() for s in shapes]
+            Pd = [torch.empty(s, device="cuda", dtype=torch.bfloat16) for s in shapes]
+            step = cuda_lib.OwnerStep(0)
+            step.set_muon(W, Bf, G, Pd)
+            step.muon_step(0.02, 0.95, 0.01, 5, A, B, C)
+            step.sync()
+            step.close()
+            outs.append([w.cpu() for w in W] + [p.cpu() for p in Pd])
+        finally:
+            cuda_lib.dmuon_set_tuning(12, TUNING_DEFAULTS[12])
+    for a_, b_ in zip(outs[0], outs[1]):
+        assert torch.equal(a_, b_)
+
+
 # ------------------------------------------------------------- degenerate shapes
 
 EDGE_SHAPES = [(1, 4096), (4096, 1), (1, 1), (2, 3), (17, 1000), (1000, 17), (7, 7), (1, 2, 3), (300, 1),
