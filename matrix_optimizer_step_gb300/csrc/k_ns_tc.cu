@@ -18,8 +18,8 @@
 //   warps 2..5  epilogue: each warp owns one 32-lane quarter of TMEM
 //               (warp % 4), reads its rows 32 columns at a time with
 //               tcgen05.ld, applies the phase's fused epilogue (scale;
-//               b*A + c*acc; a*X + acc) and stores bf16 (plus an fp32 copy
-//               where the problem asks for one) to global memory, then
+//               b*A + c*acc; a*X + acc) and stores bf16 (plus the bf16
+//               remainder where the problem asks for one) to global memory, then
 //               releases the accumulator (`tempty[a]`).
 // The two accumulators let the epilogue of tile i overlap the main loop of
 // tile i+1.

@@ -1,9 +1,10 @@
 // Fused epilogue of one Newton-Schulz output tile, shared by the one-CTA and
 // the CTA-pair tcgen05 kernels.  One epilogue warp drains its 32 TMEM lanes
 // (rows) of the accumulator, 32 columns at a time, applies the phase's
-// epilogue (see NsKind) and stores bf16 (plus the optional fp32 copy, plus the
-// transposed copy of a symmetric off-diagonal block) -- or, in the last
-// Combine of a step, applies the parameter update to W in place of storing X.
+// epilogue (see NsKind) and stores bf16 (plus, in the first iterations, the
+// bf16 remainder v - bf16(v), and the transposed copy of a symmetric
+// off-diagonal block where one is kept) -- or, in the last Combine of a step,
+// applies the parameter update to W in place of storing X.
 #pragma once
 
 #include <stdint.h>
