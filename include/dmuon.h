@@ -126,7 +126,10 @@ DMUON_API int dmuon_lpt_assign_layered(const int64_t* sizes, const int32_t* laye
  *   momentum    fp32, read and written (the momentum buffer)
  *   grad        fp32 or bf16 per grad_dtype, read only
  *   param_bf16  bf16 (raw uint16 bits), written, may be NULL (no bf16 copy)
- * master, momentum and param_bf16 must not overlap one another or grad.
+ * master, momentum and param_bf16 must not overlap one another, any grad, or
+ * any written buffer of another tensor of the same call (grads may share
+ * memory).  Every entry point checks this on the host, before any launch,
+ * and fails with DMUON_ERR_INVALID_ARG naming the two ranges.
  * Reachable means memory of the context's device, managed memory, or
  * page-locked host memory mapped into the device's address space
  * (cudaHostAlloc / cudaHostRegister with mapping): the kernels then read
@@ -148,7 +151,9 @@ typedef struct dmuon_matrix {
 /* One AdamW-route tensor, flattened: numel contiguous elements, every
  * pointer reachable from the context's device in the sense given for
  * dmuon_matrix (checked the same way).  master/exp_avg/exp_avg_sq fp32
- * read+write, grad read only, param_bf16 written (may be NULL). */
+ * read+write, grad read only, param_bf16 written (may be NULL).  The
+ * written buffers follow dmuon_matrix's no-overlap rule (also across the
+ * Muon and AdamW lists of one dmuon_step_host call). */
 typedef struct dmuon_vector {
   int64_t numel;
   int32_t grad_dtype;    /* DMUON_DTYPE_F32 or DMUON_DTYPE_BF16 */

@@ -5,6 +5,8 @@
 // k_ns_tc2.cu, k_ns_tc.cu, k_ns_simt.cu).
 #include "runtime.h"
 
+#include <algorithm>
+
 #include <new>
 
 namespace dmuon {
@@ -235,6 +237,86 @@ int validate_muon_call(const dmuon_matrix* mats, int32_t n, float lr, float mome
   return DMUON_OK;
 }
 
+// Memory the step writes must not be shared: no written range (master,
+// momentum, bf16 param; AdamW master and moments) may overlap another
+// written range or any gradient, within a tensor or across the tensors of a
+// call (two entries writing the same memory race).  Gradients are only read
+// and may overlap each other.  Host only: the ranges are sorted by start and
+// each gradient is searched among them.
+namespace {
+struct Span {
+  uintptr_t lo, hi;  // [lo, hi)
+  int route;         // 0 Muon, 1 AdamW
+  int idx;
+  const char* what;
+};
+}  // namespace
+
+int check_no_overlap(const dmuon_matrix* mats, int n, const dmuon_vector* vecs, int nv) {
+  std::vector<Span> w, r;
+  auto add = [](std::vector<Span>& v, const void* p, int64_t bytes, int route, int idx, const char* what) {
+    if (!p || bytes <= 0) return;
+    const uintptr_t lo = reinterpret_cast<uintptr_t>(p);
+    v.push_back(Span{lo, lo + static_cast<uintptr_t>(bytes), route, idx, what});
+  };
+  for (int i = 0; i < n; ++i) {
+    const dmuon_matrix& M = mats[i];
+    int64_t numel = 1;
+    for (int d = 0; d < M.rank; ++d) numel *= M.shape[d];
+    add(w, M.master, 4 * numel, 0, i, "master");
+    add(w, M.momentum, 4 * numel, 0, i, "momentum");
+    add(w, M.param_bf16, 2 * numel, 0, i, "param");
+    add(r, M.grad, (M.grad_dtype == DMUON_DTYPE_BF16 ? 2 : 4) * numel, 0, i, "grad");
+  }
+  for (int i = 0; i < nv; ++i) {
+    const dmuon_vector& V = vecs[i];
+    add(w, V.master, 4 * V.numel, 1, i, "master");
+    add(w, V.exp_avg, 4 * V.numel, 1, i, "exp_avg");
+    add(w, V.exp_avg_sq, 4 * V.numel, 1, i, "exp_avg_sq");
+    add(w, V.param_bf16, 2 * V.numel, 1, i, "param");
+    add(r, V.grad, (V.grad_dtype == DMUON_DTYPE_BF16 ? 2 : 4) * V.numel, 1, i, "grad");
+  }
+  static const char* route_name[2] = {"Muon", "AdamW"};
+  auto fail = [&](const Span& a, const Span& b) {
+    char buf[200];
+    snprintf(buf, sizeof buf, "%s tensor %d: %s overlaps %s tensor %d: %s (memory the step writes must not be shared)",
+             route_name[a.route], a.idx, a.what, route_name[b.route], b.idx, b.what);
+    return set_error(DMUON_ERR_INVALID_ARG, buf);
+  };
+  std::sort(w.begin(), w.end(), [](const Span& a, const Span& b) { return a.lo < b.lo; });
+  for (size_t k = 1; k < w.size(); ++k)
+    if (w[k].lo < w[k - 1].hi) return fail(w[k - 1], w[k]);
+  for (const Span& g : r) {
+    // The written span with the largest start below g.hi is the only one
+    // that can overlap g, since written spans are disjoint and sorted.
+    auto it = std::lower_bound(w.begin(), w.end(), g.hi, [](const Span& a, uintptr_t v) { return a.lo < v; });
+    if (it != w.begin()) {
+      const Span& c = *(it - 1);
+      if (c.hi > g.lo) return fail(c, g);
+    }
+  }
+  return DMUON_OK;
+}
+
+// The same check, skipped when the descriptor arrays are byte-for-byte the
+// ones that passed last time on this context.
+int check_no_overlap_cached(dmuon_context* ctx, const dmuon_matrix* mats, int n, const dmuon_vector* vecs, int nv) {
+  std::vector<uint8_t> key;
+  key.reserve(sizeof(dmuon_matrix) * static_cast<size_t>(n) + sizeof(dmuon_vector) * static_cast<size_t>(nv) + 8);
+  const int32_t counts[2] = {n, nv};
+  key.insert(key.end(), reinterpret_cast<const uint8_t*>(counts), reinterpret_cast<const uint8_t*>(counts) + 8);
+  if (n > 0)
+    key.insert(key.end(), reinterpret_cast<const uint8_t*>(mats),
+               reinterpret_cast<const uint8_t*>(mats) + sizeof(dmuon_matrix) * static_cast<size_t>(n));
+  if (nv > 0)
+    key.insert(key.end(), reinterpret_cast<const uint8_t*>(vecs),
+               reinterpret_cast<const uint8_t*>(vecs) + sizeof(dmuon_vector) * static_cast<size_t>(nv));
+  if (key == ctx->checked_overlap) return DMUON_OK;
+  const int st = check_no_overlap(mats, n, vecs, nv);
+  if (st == DMUON_OK) ctx->checked_overlap.swap(key);
+  return st;
+}
+
 // Argument checks of an AdamW step (host only, before any CUDA call).
 int validate_adamw_call(const dmuon_vector* ts, int32_t n, float lr, float beta1, float beta2, float eps,
                         float wd, int64_t step) {
@@ -331,6 +413,8 @@ int dmuon_muon_step(dmuon_context* ctx, const dmuon_matrix* mats, int32_t n, flo
   if (!ctx) return set_error(DMUON_ERR_INVALID_ARG, "muon_step: null context");
   int st = validate_muon_call(mats, n, lr, momentum, wd, ns_steps, a, b, c, flags);
   if (st != DMUON_OK || n == 0) return st;
+  st = check_no_overlap_cached(ctx, mats, n, nullptr, 0);
+  if (st != DMUON_OK) return st;
   DeviceGuard guard(ctx->device);
   st = ensure_device(ctx);
   if (st != DMUON_OK) return st;
@@ -352,6 +436,8 @@ int dmuon_adamw_step(dmuon_context* ctx, const dmuon_vector* ts, int32_t n, floa
   if (!ctx) return set_error(DMUON_ERR_INVALID_ARG, "adamw_step: null context");
   int st = validate_adamw_call(ts, n, lr, beta1, beta2, eps, wd, step);
   if (st != DMUON_OK || n == 0) return st;
+  st = check_no_overlap_cached(ctx, nullptr, 0, ts, n);
+  if (st != DMUON_OK) return st;
   DeviceGuard guard(ctx->device);
   st = ensure_device(ctx);
   if (st != DMUON_OK) return st;

@@ -133,6 +133,8 @@ int dmuon_step_host(dmuon_context* ctx, const dmuon_matrix* mats, const dmuon_ho
                              adamw->step);
     if (st != DMUON_OK) return st;
   }
+  st = check_no_overlap_cached(ctx, mats, n_mats, vecs, n_vecs);
+  if (st != DMUON_OK) return st;
   char buf[160];
   for (int i = 0; i < n_mats; ++i) {
     if (!mat_io[i].grad_host || (mat_io[i].param_host && !mats[i].param_bf16)) {

@@ -5,6 +5,8 @@
 
 #include <vector>
 
+#include "../../include/dmuon.h"
+
 namespace dmuon {
 
 // Record `msg` as the calling thread's last error and return `status`.
@@ -15,5 +17,9 @@ void clear_error();
 // in which items were placed (descending size, ties by index).
 int lpt_assign_impl(const int64_t* sizes, int32_t n_items, int32_t n_slots, int32_t* out_slot,
                     int64_t* out_load, std::vector<int32_t>* order_out);
+
+// DMUON_ERR_INVALID_ARG (with the two ranges named) when memory a step
+// writes overlaps other written memory or a gradient (see api.cu).
+int check_no_overlap(const dmuon_matrix* mats, int n, const dmuon_vector* vecs, int nv);
 
 }  // namespace dmuon

@@ -103,6 +103,7 @@ extern "C" int dmuon_muon_step_noalloc(const dmuon_matrix* mat, float lr, float 
     return set_error(DMUON_ERR_INVALID_ARG, "muon_step_noalloc: null master, momentum or grad");
   if (M.grad_dtype != DMUON_DTYPE_F32 && M.grad_dtype != DMUON_DTYPE_BF16)
     return set_error(DMUON_ERR_DTYPE, "muon_step_noalloc: grad dtype");
+  if (check_no_overlap(mat, 1, nullptr, 0) != DMUON_OK) return DMUON_ERR_INVALID_ARG;
   const int64_t m = M.shape[M.rank - 2], n = M.shape[M.rank - 1];
   const int64_t p = std::min(m, n), q = std::max(m, n);
   const bool tall = m > n;

@@ -288,6 +288,8 @@ struct dmuon_context {
   dmuon::Profiler prof;
   // AdamW descriptor array whose pointers last passed the reachability check.
   std::vector<uint8_t> checked_vecs;
+  // Descriptor arrays (Muon, AdamW) that last passed the overlap check.
+  std::vector<uint8_t> checked_overlap;
   // Host pipeline: copy streams, events, cached groups and copy lists.
   cudaStream_t h2d = nullptr, d2h = nullptr;
   std::vector<cudaEvent_t> events;
@@ -333,6 +335,7 @@ int ensure_device(dmuon_context* ctx);
 int check_matrices_reachable(dmuon_context* ctx, std::vector<uint8_t>& checked, const dmuon_matrix* mats,
                              int n);
 int check_vectors_reachable(dmuon_context* ctx, const dmuon_vector* ts, int n);
+int check_no_overlap_cached(dmuon_context* ctx, const dmuon_matrix* mats, int n, const dmuon_vector* vecs, int nv);
 int validate_muon_call(const dmuon_matrix* mats, int32_t n, float lr, float momentum, float wd,
                        int32_t ns_steps, float a, float b, float c, uint32_t flags);
 int validate_adamw_call(const dmuon_vector* ts, int32_t n, float lr, float beta1, float beta2, float eps,

@@ -97,7 +97,7 @@ def test_muon_step_host_validation_without_gpu(mos):
         d = capi.DmuonMatrix()
         d.rank = 1
         d.shape[0] = 128
-        d.master = d.momentum = d.grad = 256
+        d.master, d.momentum, d.grad = 1 << 20, 2 << 20, 3 << 20  # fake, never dereferenced
         with pytest.raises(mos.DmuonError) as e:
             mos.dmuon_muon_step(ctx, [d], 0.02, 0.95, 0.01, 5, 3.4445, -4.775, 2.0315, stream=0)
         assert e.value.status == capi.DMUON_ERR_RANK_LT2
@@ -130,6 +130,76 @@ def test_muon_step_host_validation_without_gpu(mos):
         mos.dmuon_context_destroy(ctx)
 
 
+def test_overlapping_written_memory_rejected_without_gpu(mos):
+    """Memory a step writes (master, momentum, bf16 param; AdamW master and
+    moments) may not overlap other written memory or a gradient, within a
+    tensor or across tensors; gradients may share memory.  Checked on the
+    host before any CUDA call (fake pointers, never dereferenced)."""
+    capi = mos.capi
+    MiB = 1 << 20
+
+    def mat(master, momentum, grad, param=None, shape=(8, 16)):
+        d = capi.DmuonMatrix()
+        d.rank = len(shape)
+        for i, s in enumerate(shape):
+            d.shape[i] = s
+        d.master, d.momentum, d.grad = master, momentum, grad
+        d.param_bf16 = param
+        d.grad_dtype = capi.DMUON_DTYPE_BF16
+        return d
+
+    def vec(master, m, v, grad, numel=100, param=None):
+        t = capi.DmuonVector()
+        t.numel = numel
+        t.master, t.exp_avg, t.exp_avg_sq, t.grad = master, m, v, grad
+        t.param_bf16 = param
+        t.grad_dtype = capi.DMUON_DTYPE_F32
+        return t
+
+    def muon_status(mats):
+        try:
+            mos.dmuon_muon_step(ctx, mats, 0.02, 0.95, 0.01, 5, 3.4445, -4.775, 2.0315, stream=0)
+            return 0, ""
+        except mos.DmuonError as e:
+            return e.status, str(e)
+
+    ctx = mos.dmuon_context_create(0)
+    try:
+        # 8 x 16 fp32 = 512 bytes per buffer.
+        bad = [
+            [mat(1 * MiB, 1 * MiB + 256, 3 * MiB)],                    # master / momentum, same tensor
+            [mat(1 * MiB, 2 * MiB, 1 * MiB + 500)],                    # grad inside master
+            [mat(1 * MiB, 2 * MiB, 3 * MiB, param=2 * MiB + 510)],     # param inside momentum
+            [mat(1 * MiB, 2 * MiB, 3 * MiB), mat(4 * MiB, 1 * MiB + 4, 5 * MiB)],  # across tensors
+            [mat(1 * MiB, 2 * MiB, 3 * MiB), mat(4 * MiB, 5 * MiB, 2 * MiB)],      # grad = other's momentum
+        ]
+        for mats in bad:
+            status, msg = muon_status(mats)
+            assert status == capi.DMUON_ERR_INVALID_ARG and "overlaps" in msg, (status, msg)
+        good = [
+            [mat(1 * MiB, 1 * MiB + 512, 3 * MiB, param=1 * MiB + 1024)],  # adjacent, not overlapping
+            [mat(1 * MiB, 2 * MiB, 3 * MiB), mat(4 * MiB, 5 * MiB, 3 * MiB)],  # shared gradient
+        ]
+        for mats in good:
+            status, msg = muon_status(mats)
+            assert "overlaps" not in msg, msg  # fails later only for want of a device here
+        with pytest.raises(mos.DmuonError) as e:
+            mos.dmuon_adamw_step(ctx, [vec(1 * MiB, 2 * MiB, 3 * MiB, 4 * MiB),
+                                       vec(5 * MiB, 2 * MiB + 396, 6 * MiB, 7 * MiB)],
+                                 1e-3, 0.9, 0.95, 1e-8, 0.0, 1, stream=0)
+        assert e.value.status == capi.DMUON_ERR_INVALID_ARG and "overlaps" in str(e.value)
+        # Across the two routes of one host-buffer step.
+        hp = capi.muon_hparams(0.02, 0.95, 0.01)
+        ap = capi.adamw_hparams(1e-3, 0.9, 0.95, 1e-8, 0.0, 1)
+        with pytest.raises(mos.DmuonError) as e:
+            capi.dmuon_step_host(ctx, [mat(1 * MiB, 2 * MiB, 3 * MiB)], [capi.DmuonHostIO(512, None)], hp,
+                                 vecs=[vec(1 * MiB + 64, 5 * MiB, 6 * MiB, 7 * MiB)],
+                                 vec_io=[capi.DmuonHostIO(512, None)], adamw=ap, stream=0)
+        assert e.value.status == capi.DMUON_ERR_INVALID_ARG and "overlaps" in str(e.value)
+    finally:
+        mos.dmuon_context_destroy(ctx)
+
+
 def test_golden_last_two_dims_accepted_ranks(mos):
     """The pages' table: [128] is rejected (rank 1); [8,16] and [4,8,16] pass
     host validation (they only fail later for lack of a device here)."""
@@ -144,7 +214,7 @@ def test_golden_last_two_dims_accepted_ranks(mos):
             d.rank = len(case["shape"])
             for i, s in enumerate(case["shape"]):
                 d.shape[i] = s
-            d.master = d.momentum = d.grad = 256
+            d.master, d.momentum, d.grad = 1 << 20, 2 << 20, 3 << 20  # fake, never dereferenced
             d.grad_dtype = capi.DMUON_DTYPE_BF16
             try:
                 mos.dmuon_muon_step(ctx, [d], 0.02, 0.95, 0.01, 5, 3.4445, -4.775, 2.0315, stream=0)
@@ -195,7 +265,7 @@ def test_step_host_host_validation_without_gpu(mos):
         d = capi.DmuonMatrix()
         d.rank = 2
         d.shape[0], d.shape[1] = 8, 16
-        d.master = d.momentum = d.grad = 256
+        d.master, d.momentum, d.grad = 1 << 20, 2 << 20, 3 << 20  # fake, never dereferenced
         d.grad_dtype = capi.DMUON_DTYPE_BF16
         io = capi.DmuonHostIO(512, None)
         for groups in (0, 65):

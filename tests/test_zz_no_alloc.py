@@ -71,7 +71,7 @@ def test_noalloc_rejects_tensor_over_the_static_limit(cuda_lib):
     d.rank = 2
     d.shape[0], d.shape[1] = 4096, 4096  # needs ~256 MiB of scratch
     d.grad_dtype = capi.DMUON_DTYPE_BF16
-    d.master = d.momentum = d.grad = 256  # never dereferenced: rejected first
+    d.master, d.momentum, d.grad = 1 << 30, 2 << 30, 3 << 30  # never dereferenced: rejected first
     with pytest.raises(mos.DmuonError) as e:
         mos.dmuon_muon_step_noalloc(d, 0.02, 0.95, 0.01, 5, A, B, C)
     assert e.value.status == capi.DMUON_ERR_SHAPE
