@@ -120,6 +120,34 @@ def test_ns_orthonormal_rows_map_to_scaled_copy():
     np.testing.assert_allclose(out, s * G, atol=1e-12)
 
 
+@pytest.mark.parametrize("shape", [(7, 11), (11, 7)])
+def test_muon_step_signed_partial_permutation_closed_form(shape):
+    # The full step on a gradient with one +-1 per row (per column when
+    # m > n) and zero momentum: u = (1 + mu) G, every singular value of X0 is
+    # s = (1 + mu) / ((1 + mu) sqrt(p) + eps), so O = +-p^5(s) on the pattern
+    # and 0 elsewhere, and W' = W (1 - lr wd) - lr sqrt(max(1, m/n)) O.
+    m, n = shape
+    p = min(m, n)
+    r = _rng(17)
+    perm = r.permutation(max(m, n))[:p]
+    sign = r.choice([-1.0, 1.0], p)
+    G = np.zeros((m, n))
+    if m <= n:
+        G[np.arange(p), perm] = sign
+    else:
+        G[perm, np.arange(p)] = sign
+    W = r.standard_normal((m, n)) * 0.02
+    lr, mu, wd = 0.02, 0.95, 0.01
+    out = omuon.muon_step(W, np.zeros((m, n)), G, lr, mu, wd, 5, A, B, C)
+    s = (1 + mu) / ((1 + mu) * math.sqrt(p) + omuon.NS_EPS)
+    for _ in range(5):
+        s = A * s + B * s ** 3 + C * s ** 5
+    np.testing.assert_allclose(out["O"], s * G, atol=1e-12)
+    scale = math.sqrt(max(1.0, m / n))
+    np.testing.assert_allclose(out["W"], W * (1 - lr * wd) - lr * scale * s * G, atol=1e-12)
+    np.testing.assert_array_equal(out["buf"], G)
+
+
 def test_ns_zero_matrix():
     out = omuon.newton_schulz(np.zeros((6, 9)), A, B, C, 5)
     assert np.all(out == 0)
