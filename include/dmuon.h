@@ -356,9 +356,6 @@ DMUON_API int dmuon_selftest_wait_timeout(dmuon_context* ctx, int32_t timeout_us
 
 /*
  * dmuon_set_tuning -- process-wide tuning switches of the kernels.
- *   key 1: operand-descriptor variant of the tcgen05 path for M/N-contiguous
- *          operands (0 = LBO spans 64-element MN blocks, the default;
- *          1 = the two offsets exchanged).  Kept for layout bring-up tests.
  *   key 2: tensor-core kernel of the Newton-Schulz phases (1 = CTA pairs,
  *          cta_group::2, on 256 x 256 tiles and, per key 12, 256 x 512
  *          ones, the default; 0 = one CTA per 128 x 256 tile).

@@ -510,10 +510,6 @@ int dmuon_profile_read(dmuon_context* ctx, double* ms_out, int64_t* count_out) {
 
 int dmuon_set_tuning(int32_t key, int32_t value) {
   clear_error();
-  if (key == 1) {
-    set_tc_mn_swap(value ? 1 : 0);
-    return DMUON_OK;
-  }
   if (key == 2) {
     g_ns_pairs = value ? 1 : 0;
     return DMUON_OK;

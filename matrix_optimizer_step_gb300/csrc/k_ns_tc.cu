@@ -85,13 +85,12 @@ __device__ __forceinline__ uint64_t desc_kmajor(uint32_t base, int kk) {
 }
 // MN-major SW128 operand: 64-element MN blocks 8 KiB apart (LBO), 8-row k
 // groups 1024 B apart (SBO).  Advancing k by 16 rows moves 2048 bytes.
-__device__ __forceinline__ uint64_t desc_mnmajor(uint32_t base, int kk, int swap) {
-  return swap ? smem_desc_sw128(base + 2048u * kk, 1024u, MN_BOX_BYTES)
-              : smem_desc_sw128(base + 2048u * kk, MN_BOX_BYTES, 1024u);
+__device__ __forceinline__ uint64_t desc_mnmajor(uint32_t base, int kk) {
+  return smem_desc_sw128(base + 2048u * kk, MN_BOX_BYTES, 1024u);
 }
 
 template <bool FUSE>
-__global__ void __launch_bounds__(kThreads, 1) ns_tc_kernel(const NsLaunch L, int mn_swap) {
+__global__ void __launch_bounds__(kThreads, 1) ns_tc_kernel(const NsLaunch L) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -228,8 +227,8 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_kernel(const NsLaunch L, in
           const uint32_t sb = sa + A_BYTES;
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
-            const uint64_t ad = a_mn ? desc_mnmajor(sa, kk, mn_swap) : desc_kmajor(sa, kk);
-            const uint64_t bd = b_mn ? desc_mnmajor(sb, kk, mn_swap) : desc_kmajor(sb, kk);
+            const uint64_t ad = a_mn ? desc_mnmajor(sa, kk) : desc_kmajor(sa, kk);
+            const uint64_t bd = b_mn ? desc_mnmajor(sb, kk) : desc_kmajor(sb, kk);
             umma_bf16(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
           }
           umma_commit(bars.e(stage));
@@ -281,10 +280,6 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_kernel(const NsLaunch L, in
 
 }  // namespace
 
-static int g_mn_swap = 0;
-
-void set_tc_mn_swap(int v) { g_mn_swap = v; }
-
 template <bool FUSE>
 static cudaError_t launch_tc_variant(const NsLaunch& L, int n_ctas, cudaStream_t st) {
   static unsigned long long attr_mask = 0;
@@ -294,7 +289,7 @@ static cudaError_t launch_tc_variant(const NsLaunch& L, int n_ctas, cudaStream_t
     if (e != cudaSuccess) return e;
     attr_note_current_device(&attr_mask);
   }
-  ns_tc_kernel<FUSE><<<n_ctas, kThreads, kSmemBytes, st>>>(L, g_mn_swap);
+  ns_tc_kernel<FUSE><<<n_ctas, kThreads, kSmemBytes, st>>>(L);
   return cudaGetLastError();
 }
 

@@ -26,7 +26,6 @@ namespace dmuon {
 extern int g_ns_pairs, g_tile_order, g_tri, g_tc2_stages_sel, g_fold_diag, g_epi8_below,
     g_mom_groups, g_wide_min_kb;
 extern int64_t g_group_min_elems, g_host_group_min_elems;
-void set_tc_mn_swap(int v);
 void set_tc2_variant(int stages);
 
 // Plan slots of a context: 0 = one-group step, 1.. = overlapped momentum

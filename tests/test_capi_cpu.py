@@ -292,7 +292,7 @@ def test_step_host_host_validation_without_gpu(mos):
 
 def test_set_tuning_rejects_unknown_keys_and_bad_values(mos):
     capi = mos.capi
-    for key, value in ((0, 1), (5, 0), (13, 1), (12, -1), (-3, 0), (8, -1), (9, 0), (9, 17), (10, 0), (10, 70000), (11, 0), (11, 1 << 21)):
+    for key, value in ((0, 1), (1, 0), (1, 1), (5, 0), (13, 1), (12, -1), (-3, 0), (8, -1), (9, 0), (9, 17), (10, 0), (10, 70000), (11, 0), (11, 1 << 21)):
         with pytest.raises(mos.DmuonError) as e:
             mos.dmuon_set_tuning(key, value)
         assert e.value.status == capi.DMUON_ERR_INVALID_ARG, (key, value)

@@ -148,25 +148,6 @@ def test_plain_momentum_and_zero_grad(cuda_lib):
     assert r["buf"] <= 1e-6 and r["O"] <= 2e-2, r
 
 
-def test_mn_major_descriptor_variant_report(cuda_lib, capsys):
-    """Both operand-descriptor variants for M/N-contiguous tiles, reported;
-    the default must be the one that matches the oracle."""
-    shapes = [(256, 512), (512, 256)]
-    errs = {}
-    for v in (0, 1):
-        cuda_lib.dmuon_set_tuning(1, v)
-        cuda_lib.dmuon_set_tuning(2, 0)  # the descriptor switch lives in the one-CTA kernel
-        try:
-            res = run_muon(cuda_lib, shapes, seed=7)[0]
-        finally:
-            cuda_lib.dmuon_set_tuning(1, 0)
-            cuda_lib.dmuon_set_tuning(2, 1)
-        errs[v] = [r["O"] for r in res]
-    with capsys.disabled():
-        print(f"\nMN-major descriptor variants: default {errs[0]}  exchanged {errs[1]}")
-    assert max(errs[0]) <= 2e-2
-
-
 def test_deterministic(cuda_lib):
     a = run_muon(cuda_lib, [(200, 328), (328, 200)], seed=8)[0]
     b = run_muon(cuda_lib, [(200, 328), (328, 200)], seed=8)[0]
