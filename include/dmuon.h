@@ -227,34 +227,49 @@ DMUON_API int dmuon_muon_step(dmuon_context* ctx, const dmuon_matrix* mats, int3
  * allocation through its own pool, code that must not grow its memory after
  * start-up, or code that must not risk the implicit device synchronisation
  * of cudaMalloc/cudaFree.  It computes what dmuon_muon_step computes for
- * `mat` on the bf16 tensor-core path, but needs no context: all scratch
- * (Newton-Schulz buffers, norm partials, descriptor tables, tensor maps)
- * lives in one static device array of 64 MiB that every GPU loading this
- * library holds until the process exits, and the host tables are built in a
- * static 1 MiB host buffer.  No cudaMalloc, cudaFree or other allocating
- * routine is called.
+ * `mat`, with the same precision policy (bf16 tensor cores for slices with
+ * min(m, n) >= 64; the fp32 CUDA-core kernel for min(m, n) < 64 or with
+ * DMUON_FLAG_FP32_NS), but needs no context: all scratch (Newton-Schulz
+ * buffers, norm partials, descriptor tables, tensor maps, the device error
+ * word) lives in one static device array of 64 MiB that every GPU loading
+ * this library holds until the process exits, and the host tables are built
+ * in a static 1 MiB host buffer.  No cudaMalloc, cudaFree or other
+ * allocating routine is called.
  *
  *   mat      host pointer to one descriptor (rank 2..4; leading dims are
  *            separate matrices), device tensors as for dmuon_muon_step
- *   flags    0 or DMUON_FLAG_NESTEROV (DMUON_FLAG_FP32_NS is rejected)
+ *   flags    DMUON_FLAG_NESTEROV and/or DMUON_FLAG_FP32_NS
  *   others   as for dmuon_muon_step; stream = cudaStream_t of the caller
  *
- * Limits: the tensor's scratch (about 8 bytes per element of every m x n
- * slice plus 8 bytes per element of every p x p Gram, p = min(m, n), plus
- * tables) must fit in 64 MiB -- e.g. one 2048 x 2048 matrix -- else
- * DMUON_ERR_SHAPE with the byte counts in dmuon_last_error().
+ * Works on the current device.  Limits: the tensor's scratch must fit in
+ * 64 MiB -- on the bf16 path about 6 bytes per element of every m x n slice
+ * plus 6 bytes per element of every p x p Gram (p = min(m, n)), e.g. one
+ * 2048 x 2048 matrix; on the fp32 path 8 and 8 -- and its tables in 1 MiB,
+ * else DMUON_ERR_SHAPE with the byte counts in dmuon_last_error().  The
+ * shape checks of dmuon_muon_step apply as well.
  * The first call on a device looks up the array's device address with
  * cudaGetSymbolAddress (once per device, with that device current); make
  * that first call before any stream capture.  Every call shares the one
  * array and it keeps the previous call's contents: calls whose work
  * overlaps on the GPU (different streams, or different host threads without
- * ordering) race on it.  The device error word lives in the array too; it
- * is cleared at the start of each call and is not reported.
+ * ordering) race on it.
+ * Device-side waits are bounded; one that runs out records its site in the
+ * array's error word and its kernel returns.  The word is not cleared by a
+ * step: dmuon_muon_step_noalloc_sync reports and clears it.
  * Errors: as dmuon_muon_step, plus DMUON_ERR_SHAPE for the size limit.
  */
 DMUON_API int dmuon_muon_step_noalloc(const dmuon_matrix* mat, float lr, float momentum, float wd,
                                       int32_t ns_steps, float a, float b, float c, uint32_t flags,
                                       void* stream);
+
+/*
+ * dmuon_muon_step_noalloc_sync -- wait for `stream`, then read and clear the
+ * error word of dmuon_muon_step_noalloc on the current device (a synchronous
+ * copy from the static array; nothing is allocated).  Returns
+ * DMUON_ERR_TIMEOUT if a bounded wait ran out since the last such read,
+ * DMUON_ERR_CUDA if the stream reported an error, else DMUON_OK.
+ */
+DMUON_API int dmuon_muon_step_noalloc_sync(void* stream);
 
 /*
  * dmuon_adamw_step -- one AdamW step over n flattened tensors ("Pure DMuon
@@ -349,8 +364,10 @@ DMUON_API int dmuon_sync(dmuon_context* ctx, void* stream);
  * Launches one block that waits on a barrier nothing will complete, giving
  * up after timeout_us microseconds (1..2,000,000); the kernel records the
  * timeout and returns normally, leaving the context usable.  A following
- * dmuon_sync() returns DMUON_ERR_TIMEOUT.  Used by the failure-detection
- * tests; never part of an optimizer step.
+ * dmuon_sync() returns DMUON_ERR_TIMEOUT.  With ctx == NULL the timeout is
+ * recorded in the error word of dmuon_muon_step_noalloc on the current
+ * device instead, and dmuon_muon_step_noalloc_sync() reports it.  Used by
+ * the failure-detection tests; never part of an optimizer step.
  */
 DMUON_API int dmuon_selftest_wait_timeout(dmuon_context* ctx, int32_t timeout_us, void* stream);
 

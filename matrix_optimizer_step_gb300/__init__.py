@@ -26,6 +26,7 @@ from .capi import (  # noqa: F401
     dmuon_lpt_assign_layered,
     dmuon_muon_step,
     dmuon_muon_step_noalloc,
+    dmuon_muon_step_noalloc_sync,
     dmuon_profile,
     dmuon_profile_read,
     dmuon_selftest_wait_timeout,

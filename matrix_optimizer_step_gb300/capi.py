@@ -38,6 +38,7 @@ EXPORTED = (
     "dmuon_context_destroy", "dmuon_muon_step", "dmuon_adamw_step", "dmuon_sync",
     "dmuon_selftest_wait_timeout", "dmuon_set_tuning", "dmuon_kernel_launches", "dmuon_profile",
     "dmuon_profile_read", "dmuon_muon_step_noalloc", "dmuon_lpt_assign_layered", "dmuon_step_host",
+    "dmuon_muon_step_noalloc_sync",
 )
 
 KERNEL_KINDS = ("momentum", "norm", "ns_gram", "ns_poly", "ns_combine", "update", "adamw")
@@ -127,6 +128,7 @@ def load_library(path=LIB_PATH):
         "dmuon_profile_read": (ctypes.c_int, [vp, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(i64)]),
         "dmuon_muon_step_noalloc": (ctypes.c_int, [ctypes.POINTER(DmuonMatrix), f32, f32, f32, i32, f32, f32,
                                                    f32, ctypes.c_uint32, vp]),
+        "dmuon_muon_step_noalloc_sync": (ctypes.c_int, [vp]),
         "dmuon_step_host": (ctypes.c_int, [vp, ctypes.POINTER(DmuonMatrix), ctypes.POINTER(DmuonHostIO), i32,
                                            ctypes.POINTER(DmuonMuonHparams), ctypes.POINTER(DmuonVector),
                                            ctypes.POINTER(DmuonHostIO), i32, ctypes.POINTER(DmuonAdamwHparams),
@@ -303,6 +305,12 @@ def dmuon_muon_step_noalloc(mat, lr, momentum, wd, ns_steps, a, b, c, flags=DMUO
     _check(load_library().dmuon_muon_step_noalloc(
         ctypes.byref(mat), float(lr), float(momentum), float(wd), int(ns_steps), float(a), float(b),
         float(c), int(flags), _stream_handle(stream)))
+
+
+def dmuon_muon_step_noalloc_sync(stream=None):
+    """Wait for ``stream``; raise DmuonError(DMUON_ERR_TIMEOUT) if a bounded
+    device-side wait of the allocation-free entry point ran out."""
+    _check(load_library().dmuon_muon_step_noalloc_sync(_stream_handle(stream)))
 
 
 def muon_hparams(lr, momentum, wd, ns_steps=5, a=3.4445, b=-4.7750, c=2.0315, nesterov=True, fp32_ns=False):

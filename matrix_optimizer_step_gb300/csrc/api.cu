@@ -463,9 +463,16 @@ int dmuon_sync(dmuon_context* ctx, void* stream) {
 
 int dmuon_selftest_wait_timeout(dmuon_context* ctx, int32_t timeout_us, void* stream) {
   clear_error();
-  if (!ctx) return set_error(DMUON_ERR_INVALID_ARG, "selftest: null context");
   if (timeout_us < 1 || timeout_us > 2000000)
     return set_error(DMUON_ERR_INVALID_ARG, "selftest: timeout_us outside [1, 2000000]");
+  if (!ctx) {
+    // The allocation-free entry point's error word on the current device.
+    int* word = nullptr;
+    const int st = noalloc_error_word(&word);
+    if (st != DMUON_OK) return st;
+    const cudaError_t e = launch_selftest_wait(word, 1000ll * timeout_us, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? DMUON_OK : cuda_fail(e, "selftest launch");
+  }
   DeviceGuard guard(ctx->device);
   int st = ensure_device(ctx);
   if (st != DMUON_OK) return st;

@@ -300,3 +300,46 @@ def test_set_tuning_rejects_unknown_keys_and_bad_values(mos):
     for key, value, default in ((8, 0, 32), (9, 4, 1), (10, 1, 1024), (11, 1, 32768), (7, 0, 1), (12, 0, 128)):
         mos.dmuon_set_tuning(key, value)
         mos.dmuon_set_tuning(key, default)
+
+
+def test_noalloc_validation_without_gpu(mos):
+    """The allocation-free entry point applies dmuon_muon_step's shape checks
+    and its own size limit on the host, before any CUDA call, and without
+    overflowing its size sums (fake pointers: never dereferenced)."""
+    capi = mos.capi
+
+    def desc(shape, dtype=capi.DMUON_DTYPE_BF16):
+        d = capi.DmuonMatrix()
+        d.rank = len(shape)
+        for i, s in enumerate(shape[:4]):
+            d.shape[i] = s
+        d.grad_dtype = dtype
+        d.master, d.momentum, d.grad = 1 << 40, 2 << 40, 3 << 40
+        return d
+
+    def status(d, flags=capi.DMUON_FLAG_NESTEROV):
+        with pytest.raises(mos.DmuonError) as e:
+            mos.dmuon_muon_step_noalloc(d, 0.02, 0.95, 0.01, 5, 3.4445, -4.775, 2.0315, flags=flags, stream=0)
+        return e.value.status, str(e.value)
+
+    # Products that would wrap 2^64 in a naive size sum, and a slice of 2^62 elements.
+    assert status(desc((1 << 31, 1 << 31, 8, 8)))[0] == capi.DMUON_ERR_SHAPE
+    assert status(desc((1 << 31, 1 << 31)))[0] == capi.DMUON_ERR_SHAPE
+    assert status(desc((1 << 20, 1 << 20, 2)))[0] == capi.DMUON_ERR_SHAPE
+    assert status(desc((65536 * 128 + 1, 1)))[0] == capi.DMUON_ERR_SHAPE
+    # Over the static limit: message names it.
+    st, msg = status(desc((4096, 4096)))
+    assert st == capi.DMUON_ERR_SHAPE and "static limit" in msg
+    st, msg = status(desc((2048, 2048)), flags=capi.DMUON_FLAG_FP32_NS)  # fp32 path: 8 B per element per X
+    assert st == capi.DMUON_ERR_SHAPE and "static limit" in msg
+    st, msg = status(desc((40000, 8, 8)))  # small scratch, tables over 1 MiB
+    assert st == capi.DMUON_ERR_SHAPE and "static limit" in msg
+    # Other checks of the main entry point.
+    assert status(desc((5,)))[0] == capi.DMUON_ERR_RANK_LT2
+    assert status(desc((2, 2, 2, 2, 2)))[0] == capi.DMUON_ERR_SHAPE
+    assert status(desc((0, 8)))[0] == capi.DMUON_ERR_SHAPE
+    assert status(desc((8, 8), dtype=7))[0] == capi.DMUON_ERR_DTYPE
+    assert status(desc((8, 8)), flags=4)[0] == capi.DMUON_ERR_INVALID_ARG
+    d = desc((8, 8))
+    d.momentum = d.master  # written memory shared
+    assert status(d)[0] == capi.DMUON_ERR_INVALID_ARG
