@@ -121,7 +121,9 @@ def _oracle_sample(wl):
     Muon matrices (with their own inputs) and a 4M-element AdamW slice."""
     from matrix_optimizer_step_gb300 import workloads as W
 
-    picks = {"llama3_8b": ["layers.0.q", "layers.0.k", "layers.0.v"],
+    # Llama-3-8B: one matrix of each of layer 0's shape classes but `o` and
+    # `up`/`down` (whose p = 4096 classes share q's and gate's flop rates).
+    picks = {"llama3_8b": ["layers.0.q", "layers.0.k", "layers.0.v", "layers.0.gate"],
              "llama3_8b_layer": ["layers.0.k"],
              "moe_experts": [], "many_small": [s.name for s in wl.matrices[:48]],
              "gpt2_small": [s.name for s in wl.matrices[:12]],
@@ -159,14 +161,21 @@ def _oracle_time(wl, sample):
 
     h = wl.hyper
     mats, adam = sample
-    t0 = time.perf_counter()
     flops = 0
+    rate = {}  # (p, q) -> seconds per dense NS flop, from the sampled matrices of that class
+    t_muon = 0.0
     for spec, W0, G in mats:
+        t0 = time.perf_counter()
         omuon.muon_step(W0, np.zeros_like(W0), G, h["lr"], h["momentum"], h["wd"], h["ns_steps"],
                         h["a"], h["b"], h["c"])
+        dt = time.perf_counter() - t0
+        t_muon += dt
         m, n = spec.mn
-        flops += W.ns_flops(m, n, h["ns_steps"]) * (W0.size // (m * n))
-    t_muon = time.perf_counter() - t0
+        f = W.ns_flops(m, n, h["ns_steps"]) * (W0.size // (m * n))
+        flops += f
+        key = (min(m, n), max(m, n))
+        s0, f0 = rate.get(key, (0.0, 0))
+        rate[key] = (s0 + dt, f0 + f)
     t_adam = 0.0
     if adam is not None:
         n, w, g = adam
@@ -174,8 +183,21 @@ def _oracle_time(wl, sample):
         oadamw.adamw_step(w, np.zeros(n), np.zeros(n), g, h["adam_lr"], h["beta1"], h["beta2"],
                           h["adam_eps"], h["adam_wd"], 1)
         t_adam = time.perf_counter() - t1
-    total_flops = W.workload_ns_flops(wl)
-    est = t_muon * total_flops / max(flops, 1)
+    # Each matrix of the workload at its own class's measured rate where the
+    # sample holds that class, else at the rate of the sampled class with
+    # the same p (the Gram size), else at the sample's overall rate.
+    overall = t_muon / max(flops, 1)
+    est = 0.0
+    for spec in wl.matrices:
+        m, n = spec.mn
+        key = (min(m, n), max(m, n))
+        f = W.ns_flops(m, n, h["ns_steps"]) * spec.n_slices
+        if key in rate:
+            r = rate[key][0] / rate[key][1]
+        else:
+            same_p = [k for k in rate if k[0] == key[0]]
+            r = (sum(rate[k][0] for k in same_p) / sum(rate[k][1] for k in same_p)) if same_p else overall
+        est += f * r
     if adam is not None:
         est += t_adam * wl.adamw_numel / adam[0]
     return t_muon + t_adam, flops, est
@@ -187,7 +209,24 @@ def _sample_desc(wl, sample):
     more = f" (+{len(mats) - 6} more)" if len(mats) > 6 else ""
     ad = f"; AdamW on {adam[0]} elements" if adam else ""
     return (f"float64 oracle Muon step on {len(mats)} matrices ({names}{more}){ad}; full-step time "
-            f"extrapolated by NS flop share (Muon) and element count (AdamW)")
+            f"extrapolated per shape class by NS flops at the sampled class's rate (Muon) and by element "
+            f"count (AdamW)")
+
+
+def _clock_normalized(achieved, peak, clk):
+    """NS throughput per GHz of the SM clock sampled during the timed region,
+    beside the measured sustained peak per GHz of the clock sampled while
+    that peak was measured: separates kernel gains from power-cap luck."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if not achieved or not clk or not clk.get("sm_mhz") or not os.path.exists(p):
+        return None
+    ref_mhz = json.load(open(p)).get("clocks_under_load", {}).get("sm_mhz_median")
+    if not ref_mhz:
+        return None
+    a = achieved / (clk["sm_mhz"] / 1e3)
+    b = peak / (ref_mhz / 1e3)
+    return {"achieved_tflops_per_ghz": a, "peak_tflops_per_ghz": b, "frac": a / b,
+            "sm_mhz": clk["sm_mhz"], "peak_sm_mhz": ref_mhz}
 
 
 def cpu_cores():
@@ -213,8 +252,11 @@ def run_reference(args, wl, rank, world):
     if rank != 0:
         return
     sample = _oracle_sample(wl)
+    # Warm-up steps (untimed) only warm the host BLAS threads and caches: the
+    # smallest sampled matrix does that as well as the whole sample.
+    warm = (sorted(sample[0], key=lambda t: t[1].size)[:1], sample[1])
     for _ in range(args.warmup):
-        _oracle_time(wl, sample)
+        _oracle_time(wl, warm)
     ests, secs = [], []
     for _ in range(args.steps):
         s, flops, est = _oracle_time(wl, sample)
@@ -395,10 +437,12 @@ def run_ours(args, wl, rank, world, local_rank):
     ns_ms = sum(prof[k][0] for k in ("ns_gram", "ns_poly", "ns_combine")) / args.steps
     ns_launches = sum(prof[k][1] for k in ("ns_gram", "ns_poly", "ns_combine"))
     ns_tflops = ns_flops / (ns_ms / 1e3) / 1e12 if ns_ms > 0 else None
-    # Roofline on the flops the symmetric kernels execute (upper triangles of
-    # X X^T and A A), not the dense count, so the fraction is not inflated.
-    ns_exec = W.workload_ns_flops_executed(wl) if not h["fp32_ns"] else ns_flops
-    ns_exec_tflops = ns_exec / (ns_ms / 1e3) / 1e12 if ns_ms > 0 else None
+    # Roofline on the algorithmic flops of the symmetric iteration (upper
+    # triangles of X X^T and A A, i.e. p(p+1)/2 dot products each), not the
+    # dense count, so the fraction is not inflated.  The kernels compute the
+    # diagonal 256-blocks in full, so they execute slightly more than this.
+    ns_alg = W.workload_ns_flops_algorithmic(wl) if not h["fp32_ns"] else ns_flops
+    ns_alg_tflops = ns_alg / (ns_ms / 1e3) / 1e12 if ns_ms > 0 else None
     # Streaming kernels: bytes of the passes that actually ran as their own
     # launches (the update runs inside the last NS product on the bf16 path).
     ew_parts = {"momentum": W.momentum_bytes(wl), "adamw": W.adamw_bytes(wl)}
@@ -410,6 +454,17 @@ def run_ours(args, wl, rank, world, local_rank):
     ew_detail = {k: {"ms": prof[k][0] / args.steps,
                      "GB/s": (v / (prof[k][0] / args.steps / 1e3) / 1e9) if prof[k][0] > 0 else None}
                  for k, v in ew_parts.items()}
+    # The same kernels on the algorithmic bytes per element of the scope
+    # table (momentum 12 with bf16 grads, update 12, AdamW 28): the X0 low
+    # half the momentum pass also writes is not counted as work.
+    ew_alg = {"momentum": W.momentum_bytes_algorithmic(wl), "adamw": W.adamw_bytes(wl)}
+    if "update" in ew_parts:
+        ew_alg["update"] = W.update_bytes(wl)
+    ew_alg_gbs = sum(ew_alg.values()) / (ew_ms / 1e3) / 1e9 if ew_ms > 0 else None
+    for k, v in ew_alg.items():
+        ew_detail[k]["GB/s_algorithmic"] = (v / (prof[k][0] / args.steps / 1e3) / 1e9) if prof[k][0] > 0 else None
+        ew_detail[k]["frac_algorithmic"] = (ew_detail[k]["GB/s_algorithmic"] / peaks["hbm_gbs"]
+                                            if ew_detail[k]["GB/s_algorithmic"] else None)
     peak = peaks["bf16_sustained"]
     traffic = None
     tpath = os.path.join(ROOT, "profiles", "ns_tc_traffic.json")
@@ -430,19 +485,23 @@ def run_ours(args, wl, rank, world, local_rank):
                    "state": "fp32 master/momentum/AdamW moments, bf16 grads and params",
                    "l2": l2_note, "parallelism": f"replicas x{world}",
                    "adamw": "side stream beside the Muon step" if args.overlap_adamw else "after the Muon step"},
+        "flops_basis": "dense_count",
         "ns_tflops_dense_count": ns_tflops,
-        "ns_tflops_executed": ns_exec_tflops,
-        "ns_tflop_per_step": {"dense_count": ns_flops / 1e12, "executed": ns_exec / 1e12},
+        "ns_tflops_algorithmic": ns_alg_tflops,
+        "ns_tflop_per_step": {"dense_count": ns_flops / 1e12, "algorithmic": ns_alg / 1e12},
         "ns_dense_count_frac_of_bf16_sustained": (ns_tflops / peak) if ns_tflops else None,
-        "roofline": {"bound": "tensor", "kernel": "ns_tc2_kernel (all NS phases, executed flops)",
-                     "achieved": ns_exec_tflops, "peak": peak, "unit": "TFLOP/s",
-                     "frac": (ns_exec_tflops / peak) if ns_exec_tflops else None,
-                     "frac_of_burst": (ns_exec_tflops / peaks["bf16_burst"]) if ns_exec_tflops else None,
+        "roofline": {"bound": "tensor", "kernel": "ns_tc2_kernel (all NS phases, algorithmic flops)",
+                     "achieved": ns_alg_tflops, "peak": peak, "unit": "TFLOP/s",
+                     "frac": (ns_alg_tflops / peak) if ns_alg_tflops else None,
+                     "frac_of_burst": (ns_alg_tflops / peaks["bf16_burst"]) if ns_alg_tflops else None,
                      "peak_src": f"{peaks['src']} bf16 sustained",
-                     "traffic": traffic, "launches_per_step": ns_launches / args.steps},
+                     "traffic": traffic, "launches_per_step": ns_launches / args.steps,
+                     "clock_normalized": _clock_normalized(ns_alg_tflops, peak, clk)},
         "elementwise": {"bound": "hbm", "achieved": ew_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                         "frac": (ew_gbs / peaks["hbm_gbs"]) if ew_gbs else None,
-                        "bytes_per_step": ew_bytes, "kernels": ew_detail},
+                        "bytes_per_step": ew_bytes, "achieved_algorithmic": ew_alg_gbs,
+                        "frac_algorithmic": (ew_alg_gbs / peaks["hbm_gbs"]) if ew_alg_gbs else None,
+                        "bytes_per_step_algorithmic": sum(ew_alg.values()), "kernels": ew_detail},
         "kernel_ms_per_step": {k: v[0] / args.steps for k, v in prof.items()},
         "gpu_launches": launches,
         "e2e": {"value": world * ns_flops / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s",

@@ -254,16 +254,18 @@ def ns_flops(m, n, steps):
     return steps * (4 * p * p * q + 2 * p ** 3)
 
 
-def ns_flops_executed(m, n, steps):
-    """Flops the symmetric kernels execute: the Gram X X^T and the square
-    A A are symmetric, so only their upper triangle is formed (p(p+1)/2
-    dot products each), while B X is computed in full."""
+def ns_flops_algorithmic(m, n, steps):
+    """Algorithmic flops of the symmetric iteration: the Gram X X^T and the
+    square A A are symmetric, so only their upper triangle needs forming
+    (p(p+1)/2 dot products each), while B X is computed in full.  The
+    tensor-core kernels form whole 256-blocks on the diagonal, so they
+    execute slightly more than this count."""
     p, q = min(m, n), max(m, n)
     return steps * (p * (p + 1) * q + p * (p + 1) * p + 2 * p * p * q)
 
 
-def workload_ns_flops_executed(wl):
-    return sum(ns_flops_executed(*s.mn, wl.hyper["ns_steps"]) * s.n_slices for s in wl.matrices)
+def workload_ns_flops_algorithmic(wl):
+    return sum(ns_flops_algorithmic(*s.mn, wl.hyper["ns_steps"]) * s.n_slices for s in wl.matrices)
 
 
 def workload_ns_flops(wl):
@@ -276,6 +278,15 @@ def momentum_bytes(wl):
     low half on the bf16 path, fp32 in the fp32 mode and for the small
     classes that run in fp32)."""
     xb = 4
+    return sum(s.numel * ((2 if s.grad_dtype == torch.bfloat16 else 4) + 8 + xb) for s in wl.matrices)
+
+
+def momentum_bytes_algorithmic(wl):
+    """Algorithmic HBM bytes of the momentum pass: grad read, momentum
+    read+write, X0 write in the Newton-Schulz operand type (2 bytes bf16,
+    4 in the fp32 mode); the X0 low half the bf16 path also writes is a
+    design choice, not counted."""
+    xb = 4 if wl.hyper["fp32_ns"] else 2
     return sum(s.numel * ((2 if s.grad_dtype == torch.bfloat16 else 4) + 8 + xb) for s in wl.matrices)
 
 
