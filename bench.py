@@ -11,8 +11,11 @@ matrices, 6.98e9 elements, plus 1.05e9 AdamW elements).
 
 value = dense Newton-Schulz TFLOP per step (all ranks) / step time, so the
 unit is TFLOP/s of the whole step; ms_per_step is the step time itself.
-Under torchrun each rank runs its own copy of the workload (weak scaling)
-and the slowest rank's time counts.  ``--impl reference`` times the float64
+Under torchrun (N > 1) the default is the owner-partitioned step of one
+model over the N ranks (strong scaling: every tensor stepped once, by its
+owner, with the collectives of the pages' routes); ``--mode replicas`` runs
+an independent copy per rank instead (weak scaling).  The slowest rank's
+time counts.  ``--impl reference`` times the float64
 CPU oracle on a bounded sample of the same workload.
 """
 
@@ -519,6 +522,178 @@ def run_ours(args, wl, rank, world, local_rank):
     print(json.dumps(line), flush=True)
     step.close()
 
+# ------------------------------------------------ owner-partitioned (N > 1)
+SHARDED_NAMES = ("embed_tokens", "word_embeddings", "wte", "lm_head")
+
+
+def _route(spec):
+    """Route of an AdamW-side tensor by the pages' policy: embedding and
+    output tables "sharded_adamw", everything else "adamw"."""
+    return "sharded_adamw" if any(k in spec.name for k in SHARDED_NAMES) else "adamw"
+
+
+def run_owner(args, wl, rank, world, local_rank, dist):
+    """One optimizer step of the whole model over `world` ranks, the pages'
+    way: every Muon / small-AdamW tensor stepped once, by its owner, after
+    the mean gradient is reduced to it; parameters broadcast from owners;
+    embedding-like tables sharded (reduce_scatter / all_gather).  Total work
+    is one model's step whatever the rank count (strong scaling)."""
+    import torch
+
+    import matrix_optimizer_step_gb300 as mos
+    from matrix_optimizer_step_gb300 import workloads as W
+    from matrix_optimizer_step_gb300.owner_dist import DistributedOwnerStep, OwnerLayout
+
+    dev_index = local_rank % torch.cuda.device_count()
+    torch.cuda.set_device(dev_index)
+    dev = torch.device("cuda", dev_index)
+    mos.load_library()
+    for kv in args.tuning:
+        k, v = kv.split("=")
+        mos.dmuon_set_tuning(int(k), int(v))
+    h = wl.hyper
+    adam_idx = [j for j, v in enumerate(wl.vectors) if _route(v) == "adamw"]
+    shard_idx = [j for j, v in enumerate(wl.vectors) if _route(v) == "sharded_adamw"]
+    L = OwnerLayout.build([s.shape for s in wl.matrices], [wl.vectors[j].numel for j in adam_idx],
+                          [wl.vectors[j].numel for j in shard_idx], world, ns_steps=h["ns_steps"])
+    ds = DistributedOwnerStep(L, device=dev)
+    order = [("m", i) for i in range(len(wl.matrices))] + [("v", j) for j in adam_idx] + [("v", j) for j in shard_idx]
+    for t, (kind, i) in enumerate(order):
+        w = W.master_init(wl.matrices[i], i, dev) if kind == "m" else W.vector_init(wl.vectors[i], i, dev)
+        ds.load_weight(t, w)
+        del w
+    # This rank's gradients (each data-parallel rank has its own).
+    for t, (kind, i) in enumerate(order):
+        g = (W.muon_grad(wl, wl.matrices[i], i, step=rank, device=dev) if kind == "m"
+             else W.vector_grad(wl.vectors[i], i, step=rank, device=dev))
+        ds.grads()[t].copy_(g.reshape(ds.grads()[t].shape))
+        del g
+    g_save = (ds.grad_flat.clone(), ds.sp_grad_flat.clone())  # the gradients every step starts from
+    muon_kw = dict(lr=h["lr"], momentum=h["momentum"], wd=h["wd"], ns_steps=h["ns_steps"], a=h["a"], b=h["b"],
+                   c=h["c"], nesterov=h["nesterov"], fp32_ns=h["fp32_ns"])
+    t_counter = [0]
+    stream = torch.cuda.current_stream()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    phase_ms = [0.0, 0.0, 0.0]
+
+    def one_step(timed):
+        t_counter[0] += 1
+        adam_kw = dict(lr=h["adam_lr"], beta1=h["beta1"], beta2=h["beta2"], eps=h["adam_eps"], wd=h["adam_wd"],
+                       step=t_counter[0])
+        # The gradients of a fresh backward pass (a reduce leaves the
+        # non-owners' copies undefined).
+        ds.grad_flat.copy_(g_save[0])
+        ds.sp_grad_flat.copy_(g_save[1])
+        ev[0].record(stream)
+        ds.reduce_grads()
+        ev[1].record(stream)
+        ds.local_step(muon_kw, adam_kw, stream=stream)
+        ev[2].record(stream)
+        ds.publish_params()
+        ev[3].record(stream)
+        if timed:
+            torch.cuda.synchronize()
+            for k in range(3):
+                phase_ms[k] += ev[k].elapsed_time(ev[k + 1])
+
+    for _ in range(args.warmup):
+        one_step(False)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(dev_index)
+    clocks.start()
+    ds.stepper.profile(True)
+    ds.stepper.profile_read()
+    launches0 = ds.stepper.kernel_launches()
+    dist.barrier()
+    torch.cuda.synchronize()
+    total_ms = 0.0
+    for _ in range(args.steps):
+        one_step(True)
+        total_ms += sum(ev[k].elapsed_time(ev[k + 1]) for k in range(3))
+    torch.cuda.synchronize()
+    dist.barrier()
+    launches = ds.stepper.kernel_launches() - launches0
+    prof = ds.stepper.profile_read()
+    ds.stepper.profile(False)
+    clk = clocks.stop()
+    ms = reduce_max_over_ranks(total_ms / args.steps, dist, dev)
+    ns_ms = sum(prof[k][0] for k in ("ns_gram", "ns_poly", "ns_combine")) / args.steps
+    mine_muon = [i for i in L.owned(rank) if i < len(wl.matrices)]
+    own_alg = sum(W.ns_flops_algorithmic(*wl.matrices[i].mn, h["ns_steps"]) * wl.matrices[i].n_slices
+                  for i in mine_muon)
+    own_tflops = own_alg / (ns_ms / 1e3) / 1e12 if ns_ms > 0 else 0.0
+    stats = torch.tensor([ns_ms, phase_ms[0] / args.steps, phase_ms[1] / args.steps, phase_ms[2] / args.steps,
+                          own_tflops, float(launches)], dtype=torch.float64,
+                         device=dev if args.dist_backend == "nccl" else "cpu")  # gloo gathers host tensors
+    gathered = [torch.empty_like(stats) for _ in range(world)]
+    dist.all_gather(gathered, stats)
+    per_rank = [g.tolist() for g in gathered]
+
+    # End to end: this rank's gradients in from page-locked host memory, the
+    # step, the bf16 parameters out (copies and step one after the other).
+    host_g = torch.empty(ds.grad_flat.shape, dtype=ds.grad_flat.dtype, pin_memory=True)
+    host_sg = torch.empty(ds.sp_grad_flat.shape, dtype=ds.sp_grad_flat.dtype, pin_memory=True)
+    host_p = torch.empty(ds.param_flat.shape, dtype=torch.bfloat16, pin_memory=True)
+    host_sp = torch.empty(ds.sp_param_flat.shape, dtype=torch.bfloat16, pin_memory=True)
+    host_g.copy_(g_save[0])
+    host_sg.copy_(g_save[1])
+    e2e_steps = max(1, min(args.steps, 3))
+    dist.barrier()
+    torch.cuda.synchronize()
+    x0, x1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    x0.record(stream)
+    for _ in range(e2e_steps):
+        t_counter[0] += 1
+        ds.grad_flat.copy_(host_g, non_blocking=True)
+        ds.sp_grad_flat.copy_(host_sg, non_blocking=True)
+        ds.step(muon_kw, dict(lr=h["adam_lr"], beta1=h["beta1"], beta2=h["beta2"], eps=h["adam_eps"],
+                              wd=h["adam_wd"], step=t_counter[0]), stream=stream)
+        host_p.copy_(ds.param_flat, non_blocking=True)
+        host_sp.copy_(ds.sp_param_flat, non_blocking=True)
+    x1.record(stream)
+    torch.cuda.synchronize()
+    dist.barrier()
+    e2e_ms = reduce_max_over_ranks(x0.elapsed_time(x1) / e2e_steps, dist, dev)
+    h2d = world * (host_g.numel() * host_g.element_size() + host_sg.numel() * host_sg.element_size())
+    d2h = world * (host_p.numel() + host_sp.numel()) * 2
+    ds.stepper.sync()
+    if rank != 0:
+        ds.close()
+        return
+    peaks = _peaks()
+    ns_flops = W.workload_ns_flops(wl)
+    peak = peaks["bf16_sustained"]
+    ach = min(r[4] for r in per_rank)
+    line = {
+        "metric": METRIC, "value": ns_flops / (ms / 1e3) / 1e12, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "strong", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": _workload_desc(wl), "ns_steps": h["ns_steps"],
+                   "ns_operands": "bf16 operands, fp32 accumulate",
+                   "state": "fp32 master/momentum/AdamW moments on owners only, bf16 grads and params on every rank",
+                   "l2": "inputs larger than L2 (no flush needed)",
+                   "parallelism": f"owner x{world}: mean grads reduced to owners, owners step, bf16 params "
+                                  f"broadcast; embedding tables reduce_scatter / all_gather",
+                   "backend": args.dist_backend},
+        "flops_basis": "dense_count",
+        "roofline": {"bound": "tensor", "kernel": "ns_tc2_kernel (owned tensors' NS phases, algorithmic flops; "
+                                                  "slowest rank)",
+                     "achieved": ach, "peak": peak, "unit": "TFLOP/s", "frac": ach / peak if ach else None,
+                     "peak_src": f"{peaks['src']} bf16 sustained", "traffic": None},
+        "owner": {"per_rank": [{"ns_ms": r[0], "reduce_ms": r[1], "step_ms": r[2], "publish_ms": r[3],
+                                "ns_tflops_algorithmic": r[4], "launches": int(r[5])} for r in per_rank],
+                  "owned_elements": [sum(math.prod(L.muon_shapes[i]) if i < len(L.muon_shapes)
+                                         else L.adamw_numels[i - len(L.muon_shapes)] for i in L.owned(r))
+                                     for r in range(world)]},
+        "gpu_launches": int(sum(r[5] for r in per_rank)),
+        "e2e": {"value": ns_flops / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                "api": "DistributedOwnerStep.step with host copies before and after"},
+        "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+    ds.close()
+
 
 def main():
     ap = argparse.ArgumentParser()
@@ -533,6 +708,11 @@ def main():
     ap.add_argument("--overlap-adamw", action="store_true",
                     help="run the AdamW step on a side stream beside the Muon step (OwnerStep.step); "
                          "per-kernel AdamW times then include waiting for SMs")
+    ap.add_argument("--mode", choices=("owner", "replicas"), default="owner",
+                    help="with --gpus N > 1: the owner-partitioned step of one model (default), or N "
+                         "independent replicas of the one-GPU step")
+    ap.add_argument("--dist-backend", choices=("nccl", "gloo"), default="nccl",
+                    help="process-group backend for N > 1 (gloo only to check the code path)")
     ap.add_argument("--tuning", action="append", default=[],
                     help="KEY=VALUE passed to dmuon_set_tuning before the run")
     args = ap.parse_args()
@@ -550,9 +730,12 @@ def main():
     if world > 1:
         import torch.distributed as dist
 
-        dist.init_process_group("nccl")
+        dist.init_process_group(args.dist_backend)
     try:
-        run_ours(args, wl, rank, world, local_rank)
+        if world > 1 and args.mode == "owner":
+            run_owner(args, wl, rank, world, local_rank, dist)
+        else:
+            run_ours(args, wl, rank, world, local_rank)
     finally:
         if world > 1:
             import torch.distributed as dist

@@ -150,6 +150,11 @@ def workload(name, tiny_extra=True):
             vecs += [VectorSpec("norm", (4096,)),
                      VectorSpec("embed_tokens", (128256, 4096)),
                      VectorSpec("lm_head", (128256, 4096))]
+        else:
+            # One layer's share of the step, with a 16384-row slice of the
+            # embedding on the AdamW route (67M elements, 1.9 GB of AdamW
+            # traffic: larger than L2, small enough for a profiler capture).
+            vecs.append(VectorSpec("embed_tokens_rows_0_16383", (16384, 4096)))
         return Workload(name, mats, vecs, _hyper(), grad_kind="student_t_rank8")
     if name == "moe_experts":
         g = torch.Generator().manual_seed(5)
