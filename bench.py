@@ -420,6 +420,14 @@ def run_ours(args, wl, rank, world, local_rank):
     e2e_ms = reduce_max_over_ranks(x0.elapsed_time(x1) / e2e_steps, dist, dev)
     h2d = g_flat.numel() * g_flat.element_size()
     d2h = p_flat.numel() * p_flat.element_size()
+    # One more host-buffer step with the library's timeline on: when the
+    # gradient copies, each group's compute and the parameter copies ended.
+    step.profile(True)
+    e2e_step()
+    tl = step.host_timeline()
+    step.profile_read()
+    step.profile(False)
+    step.sync(stream)
     # The host link's own rate in this run (one plain copy each way), which
     # bounds e2e from below once the copies are the longer side.
     link = {}
@@ -431,7 +439,37 @@ def run_ours(args, wl, rank, world, local_rank):
         x1.record(stream)
         torch.cuda.synchronize()
         link[name] = nbytes / (x0.elapsed_time(x1) / 1e3) / 1e9
+    # Both directions at once (the pipelined step overlaps them).
+    side = torch.cuda.Stream(device=dev)
+    torch.cuda.synchronize()
+    x0.record(stream)
+    side.wait_event(x0)
+    g_flat.copy_(host_g, non_blocking=True)
+    with torch.cuda.stream(side):
+        host_p.copy_(p_flat, non_blocking=True)
+    stream.wait_stream(side)
+    x1.record(stream)
+    torch.cuda.synchronize()
+    link["both_ways_gbs"] = (h2d + d2h) / (x0.elapsed_time(x1) / 1e3) / 1e9
     del host_g, host_p
+    # The end-to-end time's own bound: the longest of the gradient copies,
+    # the parameter copies and the device-only step, plus what the pipeline
+    # cannot hide -- the first group's gradients before any compute and the
+    # last group's parameters after it (both taken from the timeline).
+    e2e_detail = None
+    if tl is not None and tl["groups"]:
+        first_in = tl["groups"][0][0]
+        last_out = tl["end"] - tl["groups"][-1][1]
+        bound = max(h2d / (link["h2d_gbs"] * 1e9) * 1e3, d2h / (link["d2h_gbs"] * 1e9) * 1e3,
+                    (h2d + d2h) / (link["both_ways_gbs"] * 1e9) * 1e3, ms) + first_in + last_out
+        e2e_detail = {
+            "lower_bound_ms": bound, "frac_of_bound": bound / e2e_ms,
+            "timeline_ms": {"h2d_done": tl["h2d_done"], "compute_done": tl["groups"][-1][1], "end": tl["end"],
+                            "first_group_h2d": first_in, "last_group_d2h": last_out,
+                            "compute_waiting_for_h2d": sum(max(0.0, g[0] - (tl["groups"][i - 1][1] if i else 0.0))
+                                                           for i, g in enumerate(tl["groups"]))},
+            "groups": len(tl["groups"]),
+        }
 
     if rank != 0:
         return
@@ -510,7 +548,7 @@ def run_ours(args, wl, rank, world, local_rank):
         "e2e": {"value": world * ns_flops / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": e2e_steps, "api": "dmuon_step_host", "n_groups": args.e2e_groups,
-                "host_link": link},
+                "host_link": link, "attribution": e2e_detail},
         "clocks": clk,
     }
     if not args.no_cpu_baseline:
@@ -631,10 +669,13 @@ def run_owner(args, wl, rank, world, local_rank, dist):
 
     # End to end: this rank's gradients in from page-locked host memory, the
     # step, the bf16 parameters out (copies and step one after the other).
+    # One page-locked buffer per flat serves both directions (the parameters
+    # come back where the gradients came from), halving the pinned host
+    # memory of N ranks on one host; later steps then read the previous
+    # step's parameters as gradients, which changes no timing.
     host_g = torch.empty(ds.grad_flat.shape, dtype=ds.grad_flat.dtype, pin_memory=True)
     host_sg = torch.empty(ds.sp_grad_flat.shape, dtype=ds.sp_grad_flat.dtype, pin_memory=True)
-    host_p = torch.empty(ds.param_flat.shape, dtype=torch.bfloat16, pin_memory=True)
-    host_sp = torch.empty(ds.sp_param_flat.shape, dtype=torch.bfloat16, pin_memory=True)
+    host_p, host_sp = host_g, host_sg
     host_g.copy_(g_save[0])
     host_sg.copy_(g_save[1])
     e2e_steps = max(1, min(args.steps, 3))

@@ -438,6 +438,23 @@ DMUON_API int dmuon_profile(dmuon_context* ctx, int32_t enable);
 DMUON_API int dmuon_profile_read(dmuon_context* ctx, double* ms_out, int64_t* count_out);
 
 /*
+ * dmuon_profile_host_timeline -- where the time of a host-buffer step went.
+ * For the last dmuon_step_host call made on the context while profiling was
+ * enabled (dmuon_profile), waits for its events and writes, in
+ * milliseconds since the call's work started on its stream:
+ *   ms_out[0]            all gradient copies (host to device) done
+ *   ms_out[1]            all copies done (the step's end)
+ *   ms_out[2 + 3g + 0]   group g's gradient copies done
+ *   ms_out[2 + 3g + 1]   group g's compute done
+ *   ms_out[2 + 3g + 2]   group g's parameter copies (device to host) done
+ * for the call's G groups (*n_groups_out = G; 0 and nothing written if no
+ * such call was recorded).  capacity = doubles available in ms_out; fewer
+ * than 2 + 3G gives DMUON_ERR_INVALID_ARG (with *n_groups_out set).
+ */
+DMUON_API int dmuon_profile_host_timeline(dmuon_context* ctx, double* ms_out, int32_t capacity,
+                                          int32_t* n_groups_out);
+
+/*
  * dmuon_kernel_launches -- number of kernels the context has launched since
  * it was created (host-side count, for benchmarking).  Returns -1 for NULL.
  */

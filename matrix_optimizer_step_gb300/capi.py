@@ -38,7 +38,7 @@ EXPORTED = (
     "dmuon_context_destroy", "dmuon_muon_step", "dmuon_adamw_step", "dmuon_sync",
     "dmuon_selftest_wait_timeout", "dmuon_set_tuning", "dmuon_kernel_launches", "dmuon_profile",
     "dmuon_profile_read", "dmuon_muon_step_noalloc", "dmuon_lpt_assign_layered", "dmuon_step_host",
-    "dmuon_muon_step_noalloc_sync",
+    "dmuon_muon_step_noalloc_sync", "dmuon_profile_host_timeline",
 )
 
 KERNEL_KINDS = ("momentum", "norm", "ns_gram", "ns_poly", "ns_combine", "update", "adamw")
@@ -129,6 +129,8 @@ def load_library(path=LIB_PATH):
         "dmuon_muon_step_noalloc": (ctypes.c_int, [ctypes.POINTER(DmuonMatrix), f32, f32, f32, i32, f32, f32,
                                                    f32, ctypes.c_uint32, vp]),
         "dmuon_muon_step_noalloc_sync": (ctypes.c_int, [vp]),
+        "dmuon_profile_host_timeline": (ctypes.c_int, [vp, ctypes.POINTER(ctypes.c_double), i32,
+                                                       ctypes.POINTER(i32)]),
         "dmuon_step_host": (ctypes.c_int, [vp, ctypes.POINTER(DmuonMatrix), ctypes.POINTER(DmuonHostIO), i32,
                                            ctypes.POINTER(DmuonMuonHparams), ctypes.POINTER(DmuonVector),
                                            ctypes.POINTER(DmuonHostIO), i32, ctypes.POINTER(DmuonAdamwHparams),
@@ -296,6 +298,21 @@ def dmuon_profile_read(ctx):
     cnt = (ctypes.c_int64 * n)()
     _check(load_library().dmuon_profile_read(ctx, ms, cnt))
     return {k: (ms[i], cnt[i]) for i, k in enumerate(KERNEL_KINDS)}
+
+
+def dmuon_profile_host_timeline(ctx):
+    """Timeline of the last host-buffer step made while profiling (ms since
+    its start): {"h2d_done", "end", "groups": [(h2d_done, compute_done,
+    d2h_done), ...]}, or None if none was recorded."""
+    lib = load_library()
+    n = ctypes.c_int32()
+    cap = 2 + 3 * 64
+    buf = (ctypes.c_double * cap)()
+    _check(lib.dmuon_profile_host_timeline(ctx, buf, cap, ctypes.byref(n)))
+    if n.value == 0:
+        return None
+    return {"h2d_done": buf[0], "end": buf[1],
+            "groups": [tuple(buf[2 + 3 * g + k] for k in range(3)) for g in range(n.value)]}
 
 
 def dmuon_muon_step_noalloc(mat, lr, momentum, wd, ns_steps, a, b, c, flags=DMUON_FLAG_NESTEROV,

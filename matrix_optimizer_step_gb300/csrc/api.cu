@@ -391,6 +391,8 @@ int dmuon_context_destroy(dmuon_context* ctx) {
     ctx->events.clear();
     for (cudaEvent_t e : ctx->side_events) cudaEventDestroy(e);
     ctx->side_events.clear();
+    for (cudaEvent_t e : ctx->tl_events) cudaEventDestroy(e);
+    ctx->tl_events.clear();
     if (ctx->side) cudaStreamDestroy(ctx->side);
     ctx->side = nullptr;
     if (ctx->h2d) cudaStreamDestroy(ctx->h2d);

@@ -241,11 +241,28 @@ int dmuon_step_host(dmuon_context* ctx, const dmuon_matrix* mats, const dmuon_ho
   }
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // Timeline (profiling only): timing events beside the ordering events.
+  const bool tl = ctx->prof.on;
+  ctx->tl_groups = -1;
+  if (tl) {
+    while (ctx->tl_events.size() < 3 + 3 * static_cast<size_t>(G)) {
+      cudaEvent_t e = nullptr;
+      DM_CUDA(cudaEventCreate(&e));
+      ctx->tl_events.push_back(e);
+    }
+  }
+  auto mark = [&](size_t i, cudaStream_t on) {
+    if (tl) cudaEventRecord(ctx->tl_events[i], on);
+  };
   DM_CUDA(cudaEventRecord(ev(kStart), s));
+  mark(0, s);
   DM_CUDA(cudaStreamWaitEvent(ctx->h2d, ev(kStart), 0));
   DM_CUDA(cudaStreamWaitEvent(ctx->d2h, ev(kStart), 0));
   // Whatever happens below, `stream` ends up ordered after both copy streams.
   auto join = [&](int status) {
+    mark(1, ctx->h2d);
+    mark(2, ctx->d2h);
+    if (tl && status == DMUON_OK) ctx->tl_groups = G;
     if (cudaEventRecord(ev(kEndH2d), ctx->h2d) != cudaSuccess || cudaEventRecord(ev(kEndD2h), ctx->d2h) != cudaSuccess ||
         cudaStreamWaitEvent(s, ev(kEndH2d), 0) != cudaSuccess || cudaStreamWaitEvent(s, ev(kEndD2h), 0) != cudaSuccess) {
       if (status == DMUON_OK) return cuda_fail(cudaGetLastError(), "step_host: joining the copy streams");
@@ -256,6 +273,7 @@ int dmuon_step_host(dmuon_context* ctx, const dmuon_matrix* mats, const dmuon_ho
   for (int g = 0; g < G; ++g) {
     if ((st = enqueue_runs(H.in[static_cast<size_t>(g)], cudaMemcpyHostToDevice, ctx->h2d)) != DMUON_OK) return join(st);
     if (cudaEventRecord(ev_in(g), ctx->h2d) != cudaSuccess) return join(cuda_fail(cudaGetLastError(), "step_host"));
+    mark(3 + 3 * static_cast<size_t>(g), ctx->h2d);
     if (g == 0 && n_vecs > 0) {
       if ((st = enqueue_runs(H.a_in, cudaMemcpyHostToDevice, ctx->h2d)) != DMUON_OK) return join(st);
       if (cudaEventRecord(ev(kAdamIn), ctx->h2d) != cudaSuccess) return join(cuda_fail(cudaGetLastError(), "step_host"));
@@ -282,11 +300,39 @@ int dmuon_step_host(dmuon_context* ctx, const dmuon_matrix* mats, const dmuon_ho
     if (st != DMUON_OK) return join(st);
     if (cudaEventRecord(ev_done(g), s) != cudaSuccess || cudaStreamWaitEvent(ctx->d2h, ev_done(g), 0) != cudaSuccess)
       return join(cuda_fail(cudaGetLastError(), "step_host"));
+    mark(4 + 3 * static_cast<size_t>(g), s);
     if ((st = enqueue_runs(H.out[static_cast<size_t>(g)], cudaMemcpyDeviceToHost, ctx->d2h)) != DMUON_OK) return join(st);
+    mark(5 + 3 * static_cast<size_t>(g), ctx->d2h);
     if (g == 0 && n_vecs > 0 && (st = adam()) != DMUON_OK) return join(st);
   }
   if (G == 0 && n_vecs > 0 && (st = adam()) != DMUON_OK) return join(st);
   return join(DMUON_OK);
+}
+
+int dmuon_profile_host_timeline(dmuon_context* ctx, double* ms_out, int32_t capacity, int32_t* n_groups_out) {
+  clear_error();
+  if (!ctx || !ms_out || !n_groups_out || capacity < 0)
+    return set_error(DMUON_ERR_INVALID_ARG, "profile_host_timeline: null argument or negative capacity");
+  *n_groups_out = 0;
+  if (ctx->tl_groups < 0) return DMUON_OK;
+  const int G = ctx->tl_groups;
+  *n_groups_out = G;
+  if (capacity < 2 + 3 * G) return set_error(DMUON_ERR_INVALID_ARG, "profile_host_timeline: capacity < 2 + 3 * groups");
+  DeviceGuard guard(ctx->device);
+  auto at = [&](size_t i, double* out) -> int {
+    DM_CUDA(cudaEventSynchronize(ctx->tl_events[i]));
+    float ms = 0.f;
+    DM_CUDA(cudaEventElapsedTime(&ms, ctx->tl_events[0], ctx->tl_events[i]));
+    *out = ms;
+    return DMUON_OK;
+  };
+  int st;
+  if ((st = at(1, &ms_out[0])) != DMUON_OK || (st = at(2, &ms_out[1])) != DMUON_OK) return st;
+  for (int g = 0; g < G; ++g)
+    for (int k = 0; k < 3; ++k)
+      if ((st = at(3 + 3 * static_cast<size_t>(g) + static_cast<size_t>(k), &ms_out[2 + 3 * g + k])) != DMUON_OK)
+        return st;
+  return DMUON_OK;
 }
 
 }  // extern "C"

@@ -296,6 +296,12 @@ struct dmuon_context {
   // Overlapped momentum: side stream and its events.
   cudaStream_t side = nullptr;
   std::vector<cudaEvent_t> side_events;
+  // Timeline of the last host-buffer step made while profiling: timing
+  // events at the start, the end of all gradient copies, the end of all
+  // copies, and per group the end of its gradient copies, of its compute and
+  // of its parameter copies.  tl_groups < 0: none recorded.
+  std::vector<cudaEvent_t> tl_events;
+  int tl_groups = -1;
 };
 
 namespace dmuon {

@@ -175,6 +175,10 @@ class OwnerStep:
     def profile_read(self):
         return capi.dmuon_profile_read(self.ctx)
 
+    def host_timeline(self):
+        """Timeline of the last step_host call made while profiling."""
+        return capi.dmuon_profile_host_timeline(self.ctx)
+
     def kernel_launches(self):
         return capi.dmuon_kernel_launches(self.ctx)
 

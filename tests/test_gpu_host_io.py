@@ -142,3 +142,40 @@ def test_step_host_refuses_pageable_host_memory(cuda_lib):
         assert torch.equal(W, W0)
     finally:
         cuda_lib.dmuon_context_destroy(ctx)
+
+
+def test_step_host_timeline_is_ordered(small_host_groups):
+    """With profiling on, dmuon_step_host records when each group's gradient
+    copies, compute and parameter copies ended; the times follow the
+    pipeline's order: a group computes after its gradients arrived and after
+    the previous group computed, its parameters leave after it computed,
+    and the step ends with the last copy."""
+    mos = small_host_groups
+    dev = torch.device("cuda")
+    st = _state(31, SHAPES, VEC_NUMELS, dev)
+    hg, hv = _host_grads(32, st)
+    hp = [torch.empty(t.shape, dtype=torch.bfloat16).pin_memory() for t in st["P"]]
+    hvp = [torch.empty(t.shape, dtype=torch.bfloat16).pin_memory() for t in st["vP"]]
+    step = mos.OwnerStep(0)
+    step.set_muon(st["W"], st["B"], st["G"], st["P"])
+    step.set_adamw(st["vW"], st["vm"], st["vv"], st["vG"], st["vP"])
+    step.set_host_io(hg, hp, hv, hvp)
+    adam = dict(lr=1e-3, beta1=0.9, beta2=0.95, eps=1e-8, wd=0.0, step=1)
+    assert step.host_timeline() is None
+    step.profile(True)
+    step.step_host(HP, adam, n_groups=3)
+    tl = step.host_timeline()
+    step.profile_read()
+    step.profile(False)
+    step.sync()
+    assert tl is not None and len(tl["groups"]) == 3
+    prev_compute = 0.0
+    for h2d, comp, d2h in tl["groups"]:
+        assert 0.0 <= h2d <= tl["h2d_done"] + 1e-3
+        assert comp >= max(h2d, prev_compute) - 1e-3
+        assert d2h >= comp - 1e-3 and d2h <= tl["end"] + 1e-3
+        prev_compute = comp
+    # Without profiling nothing new is recorded: the last timeline stays.
+    step.step_host(HP, dict(adam, step=2), n_groups=3)
+    step.sync()
+    step.close()
