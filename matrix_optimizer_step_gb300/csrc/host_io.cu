@@ -243,8 +243,8 @@ int dmuon_step_host(dmuon_context* ctx, const dmuon_matrix* mats, const dmuon_ho
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // Timeline (profiling only): timing events beside the ordering events.
   const bool tl = ctx->prof.on;
-  ctx->tl_groups = -1;
   if (tl) {
+    ctx->tl_groups = -1;
     while (ctx->tl_events.size() < 3 + 3 * static_cast<size_t>(G)) {
       cudaEvent_t e = nullptr;
       DM_CUDA(cudaEventCreate(&e));

@@ -178,4 +178,5 @@ def test_step_host_timeline_is_ordered(small_host_groups):
     # Without profiling nothing new is recorded: the last timeline stays.
     step.step_host(HP, dict(adam, step=2), n_groups=3)
     step.sync()
+    assert step.host_timeline() == tl
     step.close()
