@@ -372,7 +372,10 @@ DMUON_API int dmuon_sync(dmuon_context* ctx, void* stream);
 DMUON_API int dmuon_selftest_wait_timeout(dmuon_context* ctx, int32_t timeout_us, void* stream);
 
 /*
- * dmuon_set_tuning -- process-wide tuning switches of the kernels.
+ * dmuon_set_tuning -- process-wide defaults of the kernel and planning
+ * policy.  Every context copies them when it is created
+ * (dmuon_context_create); contexts that exist already keep their own copy,
+ * which dmuon_context_set_tuning changes.  Keys and values:
  *   key 2: tensor-core kernel of the Newton-Schulz phases (1 = CTA pairs,
  *          cta_group::2, on 256 x 256 tiles and, per key 12, 256 x 512
  *          ones, the default; 0 = one CTA per 128 x 256 tile).
@@ -403,10 +406,22 @@ DMUON_API int dmuon_selftest_wait_timeout(dmuon_context* ctx, int32_t timeout_us
  *          tiles average at least `value` 64-deep k-blocks runs 256 x 512
  *          tiles wherever two adjacent column blocks exist (0..1e6, default
  *          128; 0 = never).  Results do not depend on the setting.
- * Returns DMUON_ERR_INVALID_ARG for an unknown key.  Not thread-safe with
- * respect to concurrent steps.
+ * Results never depend on keys 3, 4, 6, 9, 10, 11 and 12 (bit for bit); key
+ * 2 changes the kernel and key 7 and 8 the rounding points, all within the
+ * documented tolerances.
+ * Returns DMUON_ERR_INVALID_ARG for an unknown key or a value out of range
+ * (nothing changes then).  Thread-safe (the defaults are guarded by a lock).
  */
 DMUON_API int dmuon_set_tuning(int32_t key, int32_t value);
+
+/*
+ * dmuon_context_set_tuning -- the same keys and values as dmuon_set_tuning,
+ * for one context only (its copy of the defaults).  Takes effect at the
+ * context's next step.  Must not be called while another thread uses the
+ * context.  Errors: DMUON_ERR_INVALID_ARG for a null context, an unknown
+ * key or a value out of range (nothing changes then).
+ */
+DMUON_API int dmuon_context_set_tuning(dmuon_context* ctx, int32_t key, int32_t value);
 
 /* Kernel kinds reported by dmuon_profile_read. */
 enum {

@@ -21,6 +21,7 @@ from .capi import (  # noqa: F401
     dmuon_adamw_step,
     dmuon_context_create,
     dmuon_context_destroy,
+    dmuon_context_set_tuning,
     dmuon_kernel_launches,
     dmuon_lpt_assign,
     dmuon_lpt_assign_layered,

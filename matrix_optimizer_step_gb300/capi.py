@@ -38,7 +38,7 @@ EXPORTED = (
     "dmuon_context_destroy", "dmuon_muon_step", "dmuon_adamw_step", "dmuon_sync",
     "dmuon_selftest_wait_timeout", "dmuon_set_tuning", "dmuon_kernel_launches", "dmuon_profile",
     "dmuon_profile_read", "dmuon_muon_step_noalloc", "dmuon_lpt_assign_layered", "dmuon_step_host",
-    "dmuon_muon_step_noalloc_sync", "dmuon_profile_host_timeline",
+    "dmuon_muon_step_noalloc_sync", "dmuon_profile_host_timeline", "dmuon_context_set_tuning",
 )
 
 KERNEL_KINDS = ("momentum", "norm", "ns_gram", "ns_poly", "ns_combine", "update", "adamw")
@@ -123,6 +123,7 @@ def load_library(path=LIB_PATH):
         "dmuon_sync": (ctypes.c_int, [vp, vp]),
         "dmuon_selftest_wait_timeout": (ctypes.c_int, [vp, i32, vp]),
         "dmuon_set_tuning": (ctypes.c_int, [i32, i32]),
+        "dmuon_context_set_tuning": (ctypes.c_int, [vp, i32, i32]),
         "dmuon_kernel_launches": (i64, [vp]),
         "dmuon_profile": (ctypes.c_int, [vp, i32]),
         "dmuon_profile_read": (ctypes.c_int, [vp, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(i64)]),
@@ -280,7 +281,13 @@ def dmuon_selftest_wait_timeout(ctx, timeout_us, stream=None):
 
 
 def dmuon_set_tuning(key, value):
+    """Process-wide default of one tuning key (contexts created later copy it)."""
     _check(load_library().dmuon_set_tuning(int(key), int(value)))
+
+
+def dmuon_context_set_tuning(ctx, key, value):
+    """One tuning key of one context."""
+    _check(load_library().dmuon_context_set_tuning(ctx, int(key), int(value)))
 
 
 def dmuon_kernel_launches(ctx):

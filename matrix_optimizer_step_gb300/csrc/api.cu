@@ -7,47 +7,52 @@
 
 #include <algorithm>
 
+#include <mutex>
 #include <new>
 
 namespace dmuon {
 
 
-// Which tensor-core kernel runs the NS phases: 1 = CTA pairs on 256 x 256
-// tiles (default), 0 = one CTA per 128 x 256 tile.
-int g_ns_pairs = 1;
-// Tile order inside one problem: 1 = longer tile dimension outer, 0 = rows outer.
-int g_tile_order = 1;
-// CTA-pair kernel: 1 = symmetric outputs stored as upper blocks only and read
-// through transposed loads, 0 = mirrored stores.
-int g_tri = 1;
-int g_tc2_stages_sel = 4;
-// From the third iteration on (where X is read back in bf16 anyway), fold
-// the a*X term of the Combine into the Poly output: B + a I.  1 = on.
-int g_fold_diag = 1;
-// CTA-pair kernel: launches whose tiles average fewer 64-deep k-blocks than
-// this drain their accumulators with 8 epilogue warps instead of 4.
-int g_epi8_below = 32;
-// CTA-pair kernel: launches whose tiles average at least this many k-blocks
-// use 256 x 512 tiles where two column blocks fit (0 = never).
-// Measured on the Llama-3-8B and MoE sets: the Gram launches (mean 157 and
-// 224 k-blocks) gain 3-6 %; Poly and Combine (64) lose.
-int g_wide_min_kb = 128;
-// Momentum overlapped with Newton-Schulz: a large tensor list is cut into
-// this many groups with disjoint workspace regions, and group g+1's
-// momentum pass (HBM-bound) runs on a side stream while group g's
-// Newton-Schulz products (tensor-core-bound) run on the caller's stream.
-// 1 (the default) = one group, everything on the caller's stream.  A group
-// gets at least g_group_min_elems elements (2^30 by default): smaller groups
-// leave their launches too few tiles to fill the GPU, which costs more than
-// the hidden momentum pass saves (measured: a GPT-2-sized list in 4 groups
-// runs 40 % slower, the Llama-3-8B set 1 % faster).  Off by default: the
-// gain is small, and kernels sharing the GPU make per-kernel timings
-// (and the rooflines computed from them) describe the contention rather
-// than the kernels.
-int g_mom_groups = 1;
-int64_t g_group_min_elems = int64_t(1) << 30;
-// Host-buffer step: smallest group (elements).
-int64_t g_host_group_min_elems = int64_t(1) << 25;
+// Defaults copied into every new context (dmuon_set_tuning).
+namespace {
+std::mutex g_tuning_mu;
+Tuning g_tuning_defaults;
+}  // namespace
+
+int apply_tuning(Tuning& t, int32_t key, int32_t value) {
+  switch (key) {
+    case 2: t.ns_pairs = value ? 1 : 0; return DMUON_OK;
+    case 3: t.tc2_stages = (value == 5) ? 5 : 4; return DMUON_OK;
+    case 4: t.tile_order = value ? 1 : 0; return DMUON_OK;
+    case 6: t.tri = value ? 1 : 0; return DMUON_OK;
+    case 7: t.fold_diag = value ? 1 : 0; return DMUON_OK;
+    case 8:
+      if (value < 0 || value > 1000000) return set_error(DMUON_ERR_INVALID_ARG, "set_tuning: key 8 value outside [0, 1e6]");
+      t.epi8_below = value;
+      return DMUON_OK;
+    case 9:
+      if (value < 1 || value > 16) return set_error(DMUON_ERR_INVALID_ARG, "set_tuning: key 9 value outside [1, 16]");
+      t.mom_groups = value;
+      return DMUON_OK;
+    case 10:
+      if (value < 1 || value > 65536)
+        return set_error(DMUON_ERR_INVALID_ARG, "set_tuning: key 10 value outside [1, 65536]");
+      t.group_min_elems = int64_t(value) << 20;
+      return DMUON_OK;
+    case 11:
+      if (value < 1 || value > (1 << 20))
+        return set_error(DMUON_ERR_INVALID_ARG, "set_tuning: key 11 value outside [1, 2^20]");
+      t.host_group_min_elems = int64_t(value) << 10;
+      return DMUON_OK;
+    case 12:
+      if (value < 0 || value > 1000000)
+        return set_error(DMUON_ERR_INVALID_ARG, "set_tuning: key 12 value outside [0, 1e6]");
+      t.wide_min_kb = value;
+      return DMUON_OK;
+    default:
+      return set_error(DMUON_ERR_INVALID_ARG, "set_tuning: unknown key");
+  }
+}
 
 // ------------------------------------------------------------------ errors
 namespace {
@@ -373,6 +378,10 @@ int dmuon_context_create(dmuon_context** out, int32_t device) {
   dmuon_context* c = new (std::nothrow) dmuon_context();
   if (!c) return set_error(DMUON_ERR_NOMEM, "context_create: host allocation failed");
   c->device = device;
+  {
+    std::lock_guard<std::mutex> lock(g_tuning_mu);
+    c->tune = g_tuning_defaults;
+  }
   *out = c;
   return DMUON_OK;
 }
@@ -422,7 +431,8 @@ int dmuon_muon_step(dmuon_context* ctx, const dmuon_matrix* mats, int32_t n, flo
   if (st != DMUON_OK) return st;
   int64_t total = 0;
   for (int i = 0; i < n; ++i) total += matrix_elems(mats[i]);
-  const int groups = static_cast<int>(std::min<int64_t>({int64_t(g_mom_groups), int64_t(n), total / g_group_min_elems}));
+  const int groups =
+      static_cast<int>(std::min<int64_t>({int64_t(ctx->tune.mom_groups), int64_t(n), total / ctx->tune.group_min_elems}));
   if (groups > 1)
     return muon_step_overlapped(ctx, mats, n, groups, lr, momentum, wd, ns_steps, a, b, c, flags,
                                 static_cast<cudaStream_t>(stream));
@@ -519,53 +529,20 @@ int dmuon_profile_read(dmuon_context* ctx, double* ms_out, int64_t* count_out) {
 
 int dmuon_set_tuning(int32_t key, int32_t value) {
   clear_error();
-  if (key == 2) {
-    g_ns_pairs = value ? 1 : 0;
-    return DMUON_OK;
-  }
-  if (key == 3) {
-    g_tc2_stages_sel = (value == 5) ? 5 : 4;
-    set_tc2_variant(g_tc2_stages_sel);
-    return DMUON_OK;
-  }
-  if (key == 7) {
-    g_fold_diag = value ? 1 : 0;
-    return DMUON_OK;
-  }
-  if (key == 8) {
-    if (value < 0 || value > 1000000) return set_error(DMUON_ERR_INVALID_ARG, "set_tuning: key 8 value outside [0, 1e6]");
-    g_epi8_below = value;
-    return DMUON_OK;
-  }
-  if (key == 9) {
-    if (value < 1 || value > 16) return set_error(DMUON_ERR_INVALID_ARG, "set_tuning: key 9 value outside [1, 16]");
-    g_mom_groups = value;
-    return DMUON_OK;
-  }
-  if (key == 10) {
-    if (value < 1 || value > 65536) return set_error(DMUON_ERR_INVALID_ARG, "set_tuning: key 10 value outside [1, 65536]");
-    g_group_min_elems = int64_t(value) << 20;
-    return DMUON_OK;
-  }
-  if (key == 11) {
-    if (value < 1 || value > (1 << 20)) return set_error(DMUON_ERR_INVALID_ARG, "set_tuning: key 11 value outside [1, 2^20]");
-    g_host_group_min_elems = int64_t(value) << 10;
-    return DMUON_OK;
-  }
-  if (key == 12) {
-    if (value < 0 || value > 1000000) return set_error(DMUON_ERR_INVALID_ARG, "set_tuning: key 12 value outside [0, 1e6]");
-    g_wide_min_kb = value;
-    return DMUON_OK;
-  }
-  if (key == 4) {
-    g_tile_order = value ? 1 : 0;
-    return DMUON_OK;
-  }
-  if (key == 6) {
-    g_tri = value ? 1 : 0;
-    return DMUON_OK;
-  }
-  return set_error(DMUON_ERR_INVALID_ARG, "set_tuning: unknown key");
+  std::lock_guard<std::mutex> lock(g_tuning_mu);
+  Tuning t = g_tuning_defaults;
+  const int st = apply_tuning(t, key, value);
+  if (st == DMUON_OK) g_tuning_defaults = t;
+  return st;
+}
+
+int dmuon_context_set_tuning(dmuon_context* ctx, int32_t key, int32_t value) {
+  clear_error();
+  if (!ctx) return set_error(DMUON_ERR_INVALID_ARG, "context_set_tuning: null context");
+  Tuning t = ctx->tune;
+  const int st = apply_tuning(t, key, value);
+  if (st == DMUON_OK) ctx->tune = t;
+  return st;
 }
 
 }  // extern "C"

@@ -183,13 +183,13 @@ int dmuon_step_host(dmuon_context* ctx, const dmuon_matrix* mats, const dmuon_ho
         if ((st = check_page_locked(vec_io[i].grad_host, "grad_host", i)) != DMUON_OK) return st;
         if ((st = check_page_locked(vec_io[i].param_host, "param_host", i)) != DMUON_OK) return st;
       }
-      // Groups of fewer than g_host_group_min_elems elements leave their
+      // Groups of fewer than host_group_min_elems elements leave their
       // launches too few tiles to fill the GPU (a GPT-2-sized list in 16
       // groups ran twice as long as in 2), so short lists get fewer groups.
       int64_t elems = 0;
       for (int i = 0; i < n_mats; ++i) elems += matrix_elems(mats[i]);
       const int groups =
-          static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(n_groups, elems / g_host_group_min_elems)));
+          static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(n_groups, elems / ctx->tune.host_group_min_elems)));
       H.groups = split_groups(mats, n_mats, groups, n_mats > 0 ? muon->ns_steps : 0);
       const size_t G = H.groups.size();
       H.in.resize(G);

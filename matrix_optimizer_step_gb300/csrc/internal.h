@@ -150,6 +150,8 @@ struct NsLaunch {
   // CTA-pair kernel: the tile list holds 256 x 512 tiles (kTileWideBit);
   // needs tri, excludes fuse_update.
   int32_t wide;
+  // CTA-pair kernel: ring depth of the 256 x 256 tiles (4 or 5).
+  int32_t stages;
 };
 
 // ---- launch wrappers (each returns the cudaError_t of its launch) ----

@@ -134,11 +134,14 @@ __device__ __forceinline__ bool tri_below(int tri_bit, int k0, int row0) {
 
 // FUSE: the last Combine, which applies the update instead of storing X.
 // WIDE: the tile list may hold 256 x 512 tiles.
-template <int STAGES, bool FUSE, int EPI, bool WIDE = false>
+// PIPE: the launch reads no aux operand, and the epilogue drains TMEM with
+// the next chunk's load in flight (ns_epilogue_tile_staged_pipe).
+template <int STAGES, bool FUSE, int EPI, bool WIDE = false, bool PIPE = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_of<EPI>(), 1)
     ns_tc2_kernel(const NsLaunch L) {
   static_assert(EPI == 4 || (EPI == 8 && !FUSE), "epilogue warp count");
   static_assert(!WIDE || (EPI == 8 && !FUSE), "wide tiles: 8 epilogue warps, no fused update");
+  static_assert(!PIPE || !FUSE, "pipelined drain: plain stores only");
   constexpr uint32_t STAGE_BYTES = stage_bytes<WIDE>();
   constexpr int kProducerBWarp = 2 + EPI;
   constexpr int kNumBars = 2 * STAGES + 2 + 2 + 1;
@@ -367,6 +370,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_of<EPI>(), 1
           tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * TILE);
       if (FUSE)
         ns_epilogue_tile<true>(L, P, tm * TILE, sub_tn * TILE, row_in_tile, t_lane, false);
+      else if (PIPE)
+        ns_epilogue_tile_staged_pipe(L, P, tm * TILE, sub_tn * TILE, row_in_tile, t_lane, my_staging, box_count,
+                                     c_begin, c_end);
       else
         ns_epilogue_tile_staged(L, P, tm * TILE, sub_tn * TILE, row_in_tile, t_lane, !L.tri && P.sym && tm < sub_tn,
                                 my_staging, box_count, c_begin, c_end);
@@ -399,21 +405,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_of<EPI>(), 1
 
 }  // namespace
 
-static int g_tc2_stages = 4;
-
-void set_tc2_variant(int stages) { g_tc2_stages = (stages == 5) ? 5 : 4; }
-
-template <int STAGES, bool FUSE, int EPI, bool WIDE = false>
+template <int STAGES, bool FUSE, int EPI, bool WIDE = false, bool PIPE = false>
 static cudaError_t launch_variant3(const NsLaunch& L, int n_pairs, cudaStream_t st) {
   static unsigned long long attr_mask = 0;
   constexpr size_t smem = smem_bytes<STAGES, EPI, WIDE>();
   if (attr_needed_on_current_device(&attr_mask)) {
-    cudaError_t e = cudaFuncSetAttribute(ns_tc2_kernel<STAGES, FUSE, EPI, WIDE>,
+    cudaError_t e = cudaFuncSetAttribute(ns_tc2_kernel<STAGES, FUSE, EPI, WIDE, PIPE>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     attr_note_current_device(&attr_mask);
   }
-  ns_tc2_kernel<STAGES, FUSE, EPI, WIDE><<<2 * n_pairs, threads_of<EPI>(), smem, st>>>(L);
+  ns_tc2_kernel<STAGES, FUSE, EPI, WIDE, PIPE><<<2 * n_pairs, threads_of<EPI>(), smem, st>>>(L);
   return cudaGetLastError();
 }
 
@@ -431,9 +433,12 @@ cudaError_t launch_ns_tc2(const NsLaunch& L, int n_pairs, cudaStream_t st) {
   if (n_pairs <= 0) return cudaSuccess;
   if (L.wide) {
     if (L.fuse_update || !L.tri) return cudaErrorInvalidValue;  // not built for these
-    return launch_variant3<3, false, 8, true>(L, n_pairs, st);
+    // No aux operand: the Gram, and a Combine whose a*X is folded into B.
+    const bool no_aux = L.kind == kGram || (L.kind == kCombine && L.a == 0.f);
+    return no_aux ? launch_variant3<3, false, 8, true, true>(L, n_pairs, st)
+                  : launch_variant3<3, false, 8, true>(L, n_pairs, st);
   }
-  return (g_tc2_stages == 5) ? launch_variant<5>(L, n_pairs, st) : launch_variant<4>(L, n_pairs, st);
+  return (L.stages == 5) ? launch_variant<5>(L, n_pairs, st) : launch_variant<4>(L, n_pairs, st);
 }
 
 // Largest number of CTA pairs of this kernel that can be resident at once.

@@ -375,3 +375,90 @@ __device__ __forceinline__ void ns_epilogue_tile_staged(const NsLaunch& L, const
 }
 
 }  // namespace dmuon
+
+namespace dmuon {
+
+// The staged epilogue for launches without an aux operand (the Gram, and the
+// Combine once a*X is folded into the polynomial matrix), with the TMEM
+// drain software-pipelined: the load of chunk cc+1 is in flight while chunk
+// cc is scaled, packed and staged, so the TMEM latency is paid once per tile
+// instead of once per chunk.  Used by the 256 x 512 tiles, whose epilogue is
+// not hidden behind another tile's main loop (their two accumulators fill
+// all of TMEM).  Same arithmetic as ns_epilogue_tile_staged with beta = 0,
+// so the results are bit-identical.
+__device__ __forceinline__ void ns_epilogue_tile_staged_pipe(const NsLaunch& L, const NsProblem& P, int m0, int n0,
+                                                             int row_in_tile, uint32_t t_lane, uint32_t stage_smem,
+                                                             uint32_t& box_count, int c_begin, int c_end) {
+  constexpr int BN = 256;
+  const int lane = threadIdx.x & 31;
+  float alpha = 1.f;
+  if (L.gscale && L.gpow > 0) {
+    const float s = L.gscale[P.slice];
+    alpha = (L.gpow == 2) ? s * s : s;
+  }
+  const float diag = (L.kind == kPoly) ? L.diag : 0.f;
+  const int row = m0 + row_in_tile;
+  const int warp_row0 = row - lane;
+  if (warp_row0 >= P.M) return;  // no row of this warp is in the output
+  const CUtensorMap* map_out = L.maps + P.map_out;
+  const bool has_lo = P.out_lo != nullptr;
+  const CUtensorMap* map_out_lo = has_lo ? L.maps + P.map_out_lo : nullptr;
+  const int n_boxes = (min(BN, P.N - n0) + 63) / 64;
+  const int cc_end = min(c_end, 2 * n_boxes);
+  if (c_begin >= cc_end) return;
+  uint32_t nxt[32];
+  __syncwarp();
+  tmem_ld_32x32b_x32(t_lane + static_cast<uint32_t>(c_begin * 32), nxt);
+#pragma unroll 1
+  for (int cc = c_begin; cc < cc_end; ++cc) {
+    const int col0 = n0 + cc * 32;
+    tmem_ld_wait_regs(nxt);
+    float v[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      v[j] = alpha * __uint_as_float(nxt[j]);
+      if (row == col0 + j) v[j] += diag;
+    }
+    __syncwarp();
+    if (cc + 1 < cc_end) tmem_ld_32x32b_x32(t_lane + static_cast<uint32_t>((cc + 1) * 32), nxt);
+    const uint32_t buf = has_lo ? stage_smem : stage_smem + (box_count & 1u) * 4096u;
+    if ((cc & 1) == 0) {
+      if (lane == 0) {
+        if (has_lo)
+          bulk_wait_group_read<0>();
+        else
+          bulk_wait_group_read<1>();
+      }
+      __syncwarp();
+    }
+    const uint32_t swz = static_cast<uint32_t>(lane) * 128u;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t j = static_cast<uint32_t>(4 * (cc & 1) + i);
+      const uint32_t off = swz + ((j ^ static_cast<uint32_t>(lane & 7)) << 4);
+      st_shared_v4(buf + off, pack_bf16x2(v[8 * i], v[8 * i + 1]), pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
+                   pack_bf16x2(v[8 * i + 4], v[8 * i + 5]), pack_bf16x2(v[8 * i + 6], v[8 * i + 7]));
+      if (has_lo)
+        st_shared_v4(buf + 4096u + off, pack_bf16x2_remainder(v[8 * i], v[8 * i + 1]),
+                     pack_bf16x2_remainder(v[8 * i + 2], v[8 * i + 3]),
+                     pack_bf16x2_remainder(v[8 * i + 4], v[8 * i + 5]),
+                     pack_bf16x2_remainder(v[8 * i + 6], v[8 * i + 7]));
+    }
+    if (cc & 1) {
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_3d(map_out, buf, n0 + 64 * (cc >> 1), warp_row0, P.z);
+        if (has_lo) tma_store_3d(map_out_lo, buf + 4096u, n0 + 64 * (cc >> 1), warp_row0, P.z);
+        bulk_commit_group();
+      }
+      ++box_count;
+    }
+  }
+  if (has_lo) {
+    if (lane == 0) bulk_wait_group_read<0>();
+    __syncwarp();
+  }
+}
+
+}  // namespace dmuon

@@ -18,9 +18,9 @@
 
 namespace dmuon {
 
-std::string plan_key(const dmuon_matrix* mats, int n, bool fp32) {
+std::string plan_key(const dmuon_matrix* mats, int n, bool fp32, int tile_order) {
   std::string k = fp32 ? "f32|" : "bf16|";
-  k += "o" + std::to_string(g_tile_order) + "|";
+  k += "o" + std::to_string(tile_order) + "|";
   for (int i = 0; i < n; ++i) {
     k += std::to_string(mats[i].rank);
     for (int d = 0; d < mats[i].rank; ++d) k += ":" + std::to_string(mats[i].shape[d]);
@@ -53,7 +53,8 @@ int make_map(EncodeTiledFn enc, CUtensorMap* out, void* base, int64_t inner, int
 // blocks of one row block form a 256 x 512 tile (kTileWideBit) wherever both
 // exist (for a symmetric output: both on or above the diagonal).
 // `slots` = persistent CTAs (or CTA pairs).
-int build_phase_tiles(const std::vector<NsProblem>& probs, int geometry, int slots, PhaseTiles& out) {
+int build_phase_tiles(const std::vector<NsProblem>& probs, int geometry, int slots, int tile_order,
+                      PhaseTiles& out) {
   const bool fp32 = geometry == 0;
   const bool wide = geometry == 3;
   const int bm = geometry == 0 ? kSimtBM : geometry == 1 ? kTcBM : kTc2Tile;
@@ -77,7 +78,7 @@ int build_phase_tiles(const std::vector<NsProblem>& probs, int geometry, int slo
     // Tiles of equal cost run in list order, so consecutive tiles run at the
     // same time: walk the longer tile dimension in the outer loop, so a wave
     // shares few panels of the larger operand (which then stay in L2).
-    const bool n_outer = g_tile_order && tn > tm;
+    const bool n_outer = tile_order && tn > tm;
     const int jstep = wide ? 2 : 1;
     if (n_outer) {
       for (int j = 0; j < tn; j += jstep)
@@ -417,16 +418,16 @@ int build_muon_plan(dmuon_context* ctx, MuonPlan& P, const dmuon_matrix* mats, i
   }
   for (int kind = 0; kind < 3; ++kind) {
     if (!var_f32[kind][0].empty()) {
-      st = build_phase_tiles(var_f32[kind][0], 0, ctx->num_sms, P.phase_f32[kind]);
+      st = build_phase_tiles(var_f32[kind][0], 0, ctx->num_sms, ctx->tune.tile_order, P.phase_f32[kind]);
       if (st != DMUON_OK) return st;
     }
     if (!var[kind][0].empty()) {
-      st = build_phase_tiles(var[kind][0], 1, ctx->num_sms, P.phase[kind]);
+      st = build_phase_tiles(var[kind][0], 1, ctx->num_sms, ctx->tune.tile_order, P.phase[kind]);
       if (st != DMUON_OK) return st;
       const int pairs = std::max(1, std::min(ctx->num_sms / 2, ns_tc2_max_pairs()));
-      st = build_phase_tiles(var[kind][0], 2, pairs, P.phase2[kind]);
+      st = build_phase_tiles(var[kind][0], 2, pairs, ctx->tune.tile_order, P.phase2[kind]);
       if (st != DMUON_OK) return st;
-      st = build_phase_tiles(var[kind][0], 3, pairs, P.phase2w[kind]);
+      st = build_phase_tiles(var[kind][0], 3, pairs, ctx->tune.tile_order, P.phase2w[kind]);
       if (st != DMUON_OK) return st;
     }
   }

@@ -22,11 +22,51 @@
 
 namespace dmuon {
 
-// Process-wide tuning switches (dmuon_set_tuning; defined in api.cu).
-extern int g_ns_pairs, g_tile_order, g_tri, g_tc2_stages_sel, g_fold_diag, g_epi8_below,
-    g_mom_groups, g_wide_min_kb;
-extern int64_t g_group_min_elems, g_host_group_min_elems;
-void set_tc2_variant(int stages);
+// Kernel and planning policy of a context (dmuon_context_set_tuning).  A new
+// context copies the process-wide defaults (dmuon_set_tuning, api.cu).
+struct Tuning {
+  // Which tensor-core kernel runs the NS phases: 1 = CTA pairs on 256 x 256
+  // tiles, 0 = one CTA per 128 x 256 tile.
+  int ns_pairs = 1;
+  // Tile order inside one problem: 1 = longer tile dimension outer, 0 = rows outer.
+  int tile_order = 1;
+  // CTA-pair kernel: 1 = symmetric outputs stored as upper blocks only and
+  // read through transposed loads, 0 = mirrored stores.
+  int tri = 1;
+  // Ring depth of the CTA-pair kernel (4 or 5).
+  int tc2_stages = 4;
+  // From the third iteration on (where X is read back in bf16 anyway), fold
+  // the a*X term of the Combine into the Poly output: B + a I.  1 = on.
+  int fold_diag = 1;
+  // CTA-pair kernel: launches whose tiles average fewer 64-deep k-blocks
+  // than this drain their accumulators with 8 epilogue warps instead of 4,
+  // and a last Combine that short is not fused with the update.
+  int epi8_below = 32;
+  // CTA-pair kernel: launches whose tiles average at least this many
+  // k-blocks use 256 x 512 tiles where two column blocks fit (0 = never).
+  // Measured on the Llama-3-8B and MoE sets: the Gram launches (mean 157
+  // and 224 k-blocks) gain 3-6 %.
+  int wide_min_kb = 128;
+  // Momentum overlapped with Newton-Schulz: a large tensor list is cut into
+  // this many groups with disjoint workspace regions, and group g+1's
+  // momentum pass (HBM-bound) runs on a side stream while group g's
+  // Newton-Schulz products (tensor-core-bound) run on the caller's stream.
+  // 1 = one group, everything on the caller's stream.  A group gets at
+  // least group_min_elems elements: smaller groups leave their launches too
+  // few tiles to fill the GPU, which costs more than the hidden momentum
+  // pass saves (measured: a GPT-2-sized list in 4 groups runs 40 % slower,
+  // the Llama-3-8B set 1 % faster).  Off by default: the gain is small, and
+  // kernels sharing the GPU make per-kernel timings (and the rooflines
+  // computed from them) describe the contention rather than the kernels.
+  int mom_groups = 1;
+  int64_t group_min_elems = int64_t(1) << 30;
+  // Host-buffer step: smallest group (elements).
+  int64_t host_group_min_elems = int64_t(1) << 25;
+};
+
+// Apply one (key, value) pair of dmuon_set_tuning to `t`; DMUON_ERR_INVALID_ARG
+// for an unknown key or a value out of range (api.cu).
+int apply_tuning(Tuning& t, int32_t key, int32_t value);
 
 // Plan slots of a context: 0 = one-group step, 1.. = overlapped momentum
 // groups, 65.. = host-pipeline groups.
@@ -275,6 +315,7 @@ struct Profiler {
 
 struct dmuon_context {
   int device = 0;
+  dmuon::Tuning tune;
   bool dev_ready = false;
   int num_sms = 0;
   int64_t launches = 0;
@@ -347,7 +388,7 @@ int validate_adamw_call(const dmuon_vector* ts, int32_t n, float lr, float beta1
                         float wd, int64_t step);
 
 // ---- plan.cu
-std::string plan_key(const dmuon_matrix* mats, int n, bool fp32);
+std::string plan_key(const dmuon_matrix* mats, int n, bool fp32, int tile_order);
 int layout_plan(MuonPlan& P, const dmuon_matrix* mats, int n, bool fp32, size_t ws_base);
 size_t plan_ws_bytes(const dmuon_matrix* mats, int n, bool fp32);
 int ensure_workspace(dmuon_context* ctx, size_t bytes);

@@ -20,7 +20,7 @@ MuonSlot* get_slot(dmuon_context* ctx, size_t i) {
 // workspace region changed or the workspace was reallocated since.
 int prepare_slot(dmuon_context* ctx, MuonSlot& S, const dmuon_matrix* mats, int n, bool fp32,
                  size_t ws_base) {
-  const std::string key = plan_key(mats, n, fp32);
+  const std::string key = plan_key(mats, n, fp32, ctx->tune.tile_order);
   if (key == S.plan.key && S.plan.ws_epoch == ctx->ws_epoch && S.plan.ws_base == ws_base) return DMUON_OK;
   int st = build_muon_plan(ctx, S.plan, mats, n, fp32, key, ws_base);
   if (st != DMUON_OK) S.plan.release();
@@ -98,9 +98,10 @@ int muon_launch_ns(dmuon_context* ctx, MuonSlot& S, float lr, float wd, int32_t 
   // tiles' main loops are short: there the epilogue sets the pace, and a
   // plain X store by 8 epilogue warps followed by the streaming update pass
   // is faster (GPT-2 set: 380 us fused against 120 + ~160 us).
-  const bool pairs = g_ns_pairs != 0;
+  const Tuning& tu = ctx->tune;
+  const bool pairs = tu.ns_pairs != 0;
   const PhaseTiles& last_combine = pairs ? P.phase2[kCombine] : P.phase[kCombine];
-  const bool fuse_last = last_combine.mean_kblocks >= static_cast<double>(g_epi8_below);
+  const bool fuse_last = last_combine.mean_kblocks >= static_cast<double>(tu.epi8_below);
   for (int it = 0; it < ns_steps; ++it) {
     const int variant = it < 2 ? 2 + it : (it & 1);
     for (int kind = kGram; kind <= kCombine; ++kind) {
@@ -117,7 +118,7 @@ int muon_launch_ns(dmuon_context* ctx, MuonSlot& S, float lr, float wd, int32_t 
       if (P.phase[kind].n_tiles > 0) {
         NsLaunch T = L;
         T.probs = static_cast<const NsProblem*>(P.probs[kind][variant].p);
-        if (g_fold_diag && it >= 2) {
+        if (tu.fold_diag && it >= 2) {
           // X' = a X + B X = (a I + B) X: the Poly adds a on B's diagonal and
           // the Combine reads no aux.
           if (kind == kPoly) T.diag = a;
@@ -130,15 +131,16 @@ int muon_launch_ns(dmuon_context* ctx, MuonSlot& S, float lr, float wd, int32_t 
           T.lr = lr;
           T.wd = wd;
         }
-        T.tri = (pairs && g_tri) ? 1 : 0;
+        T.tri = (pairs && tu.tri) ? 1 : 0;
+        T.stages = tu.tc2_stages;
         // 256 x 512 tiles where the main loops are long enough to pay for an
         // accumulator that is not double-buffered.
-        T.wide = (T.tri && !T.fuse_update && g_wide_min_kb > 0 && P.phase2w[kind].n_tiles > 0 &&
-                  P.phase2[kind].mean_kblocks >= static_cast<double>(g_wide_min_kb))
+        T.wide = (T.tri && !T.fuse_update && tu.wide_min_kb > 0 && P.phase2w[kind].n_tiles > 0 &&
+                  P.phase2[kind].mean_kblocks >= static_cast<double>(tu.wide_min_kb))
                      ? 1
                      : 0;
         const PhaseTiles& PT = pairs ? (T.wide ? P.phase2w[kind] : P.phase2[kind]) : P.phase[kind];
-        T.epi8 = (!T.fuse_update && PT.mean_kblocks < static_cast<double>(g_epi8_below)) ? 1 : 0;
+        T.epi8 = (!T.fuse_update && PT.mean_kblocks < static_cast<double>(tu.epi8_below)) ? 1 : 0;
         T.tiles = static_cast<const uint2*>(PT.tiles.p);
         T.cta_begin = static_cast<const int32_t*>(PT.cta_begin.p);
         st = timed_launch(ctx, DMUON_KERNEL_NS_GRAM + kind, s, [&] {

@@ -175,6 +175,10 @@ class OwnerStep:
     def profile_read(self):
         return capi.dmuon_profile_read(self.ctx)
 
+    def set_tuning(self, key, value):
+        """One tuning key of this context (dmuon_context_set_tuning)."""
+        capi.dmuon_context_set_tuning(self.ctx, key, value)
+
     def host_timeline(self):
         """Timeline of the last step_host call made while profiling."""
         return capi.dmuon_profile_host_timeline(self.ctx)

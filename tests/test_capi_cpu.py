@@ -343,3 +343,29 @@ def test_noalloc_validation_without_gpu(mos):
     d = desc((8, 8))
     d.momentum = d.master  # written memory shared
     assert status(d)[0] == capi.DMUON_ERR_INVALID_ARG
+
+
+def test_context_tuning_is_per_context_without_gpu(mos):
+    """A context copies the process-wide defaults when created; changing the
+    defaults later or another context's copy leaves it alone (no GPU: the
+    setters are host-only)."""
+    capi = mos.capi
+    a = mos.dmuon_context_create(0)
+    try:
+        mos.dmuon_set_tuning(12, 7)  # default for contexts created from now on
+        b = mos.dmuon_context_create(0)
+        try:
+            mos.dmuon_context_set_tuning(a, 8, 0)
+            mos.dmuon_context_set_tuning(b, 8, 1000)
+            for key, value in ((1, 0), (13, 1), (8, -1), (9, 0)):
+                with pytest.raises(mos.DmuonError) as e:
+                    mos.dmuon_context_set_tuning(a, key, value)
+                assert e.value.status == capi.DMUON_ERR_INVALID_ARG
+            with pytest.raises(mos.DmuonError) as e:
+                mos.dmuon_context_set_tuning(None, 8, 0)
+            assert e.value.status == capi.DMUON_ERR_INVALID_ARG
+        finally:
+            mos.dmuon_context_destroy(b)
+    finally:
+        mos.dmuon_set_tuning(12, 128)
+        mos.dmuon_context_destroy(a)

@@ -334,6 +334,36 @@ def test_wide_tiles_bit_identical_to_narrow(cuda_lib):
         assert torch.equal(a_, b_)
 
 
+def test_two_contexts_with_their_own_tiling_policy(cuda_lib):
+    """Tuning is per context: one context on 256 x 512 tiles wherever they
+    fit and one on 256 x 256 tiles only, stepped alternately in one process,
+    give the same bits (and a context created afterwards has the defaults)."""
+    shapes = [(520, 520), (300, 700), (1024, 1536)]
+    g = torch.Generator().manual_seed(12)
+    W = [torch.randn(s, generator=g) * 0.02 for s in shapes]
+    G = [[torch.randn(s, generator=g).to(torch.bfloat16) for s in shapes] for _ in range(2)]
+    sides = []
+    for wide in (1, 0):
+        st = cuda_lib.OwnerStep(0)
+        st.set_tuning(12, wide)
+        t = {"W": [w.cuda() for w in W], "B": [torch.zeros(s, device="cuda") for s in shapes],
+             "G": [torch.empty(s, device="cuda", dtype=torch.bfloat16) for s in shapes],
+             "P": [torch.empty(s, device="cuda", dtype=torch.bfloat16) for s in shapes], "st": st}
+        st.set_muon(t["W"], t["B"], t["G"], t["P"])
+        sides.append(t)
+    for k in range(2):
+        for t in sides:
+            for d, h in zip(t["G"], G[k]):
+                d.copy_(h)
+            t["st"].muon_step(0.02, 0.95, 0.01, 5, A, B, C)
+    for t in sides:
+        t["st"].sync()
+    for x, y in zip(sides[0]["W"] + sides[0]["P"], sides[1]["W"] + sides[1]["P"]):
+        assert torch.equal(x, y)
+    for t in sides:
+        t["st"].close()
+
+
 # ------------------------------------------------------------- degenerate shapes
 
 EDGE_SHAPES = [(1, 4096), (4096, 1), (1, 1), (2, 3), (17, 1000), (1000, 17), (7, 7), (1, 2, 3), (300, 1),
