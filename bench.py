@@ -469,6 +469,7 @@ def run_ours(args, wl, rank, world, local_rank):
                             "compute_waiting_for_h2d": sum(max(0.0, g[0] - (tl["groups"][i - 1][1] if i else 0.0))
                                                            for i, g in enumerate(tl["groups"]))},
             "groups": len(tl["groups"]),
+            "per_group_ms": [[round(x, 2) for x in g] for g in tl["groups"]],
         }
 
     if rank != 0:

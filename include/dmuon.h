@@ -329,7 +329,10 @@ typedef struct dmuon_adamw_hparams {
  * group's gradients travel while earlier groups compute and each group's parameters
  * travel while later groups compute, on two copy streams the context owns,
  * so the host link is busy only at the ends of the step.  The AdamW tensors
- * travel and step right after the first Muon group.  Results are bit-identical
+ * travel and step right after the first Muon group.  Parameter copies start
+ * once every gradient copy has landed (where the link's two directions
+ * share a bottleneck, earlier ones would slow the gradient copies the
+ * compute waits for).  Results are bit-identical
  * to the device entry points on the same inputs.
  *
  *   mats, mat_io  n_mats Muon tensors and their host buffers

@@ -174,6 +174,8 @@ def test_step_host_timeline_is_ordered(small_host_groups):
         assert 0.0 <= h2d <= tl["h2d_done"] + 1e-3
         assert comp >= max(h2d, prev_compute) - 1e-3
         assert d2h >= comp - 1e-3 and d2h <= tl["end"] + 1e-3
+        # Parameter copies wait for the last gradient copy.
+        assert d2h >= tl["h2d_done"] - 1e-3
         prev_compute = comp
     # Without profiling nothing new is recorded: the last timeline stays.
     step.step_host(HP, dict(adam, step=2), n_groups=3)
