@@ -163,6 +163,46 @@ def test_ns_emulated_bf16_close_to_exact():
     assert np.all(omuon.bf16_round(emu) == emu)
 
 
+def _bf16_via_torch(v):
+    """fp64 scalar -> float32 -> bfloat16 (round to nearest even each time),
+    by torch's casts: the rounding points the emulation claims."""
+    return float(torch.tensor(v, dtype=torch.float64).to(torch.float32).to(torch.bfloat16).to(torch.float64))
+
+
+@pytest.mark.parametrize("rows,cols", [(3, 4), (8, 16), (64, 96), (24, 7)])
+def test_ns_emulated_bf16_on_signed_partial_permutation(rows, cols):
+    """Rounding points of the bf16 emulation, pinned exactly.  For a signed
+    partial permutation P (one +-1 in each row of the short side, at
+    distinct positions), every iterate is a scalar times P: X = x P,
+    X X^T = x^2 I, so A, B and X' are scalars times I, I and P, and the
+    emulated iteration must equal the scalar recurrence
+    x0 = r(1/(sqrt(k)+eps)); alpha = r(x^2); beta = r(b alpha + c alpha^2);
+    x <- r(a x + beta x), with k = min(rows, cols) and r the
+    float32-then-bfloat16 rounding done by torch.  A dropped or misplaced
+    rounding of A, B, X or X0 changes the bits; (24, 7) takes the
+    transposed orientation."""
+    r = _rng(40 + rows)
+    k = min(rows, cols)
+    P = np.zeros((rows, cols))
+    pos = r.permutation(max(rows, cols))[:k]
+    signs = r.choice([-1.0, 1.0], size=k)
+    for i in range(k):
+        if rows <= cols:
+            P[i, pos[i]] = signs[i]
+        else:
+            P[pos[i], i] = signs[i]
+    emu = omuon.newton_schulz(P, A, B, C, 5, emulate_bf16=True)
+    x = _bf16_via_torch(1.0 / (math.sqrt(k) + omuon.NS_EPS))
+    for _ in range(5):
+        alpha = _bf16_via_torch(x * x)
+        beta = _bf16_via_torch(B * alpha + C * (alpha * alpha))
+        x = _bf16_via_torch(A * x + beta * x)
+    assert np.array_equal(emu, x * P)
+    # The same input without emulation gives p^5(1/sqrt(k)) P, which differs.
+    exact = omuon.newton_schulz(P, A, B, C, 5)
+    assert not np.array_equal(emu, exact)
+
+
 # ----------------------------------------------------------------- momentum
 
 def test_momentum_matches_torch_sgd_nesterov():
