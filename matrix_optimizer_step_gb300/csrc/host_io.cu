@@ -260,7 +260,6 @@ int dmuon_step_host(dmuon_context* ctx, const dmuon_matrix* mats, const dmuon_ho
   DM_CUDA(cudaStreamWaitEvent(ctx->d2h, ev(kStart), 0));
   // Whatever happens below, `stream` ends up ordered after both copy streams.
   auto join = [&](int status) {
-    mark(1, ctx->h2d);
     mark(2, ctx->d2h);
     if (tl && status == DMUON_OK) ctx->tl_groups = G;
     if (cudaEventRecord(ev(kEndH2d), ctx->h2d) != cudaSuccess || cudaEventRecord(ev(kEndD2h), ctx->d2h) != cudaSuccess ||
@@ -289,6 +288,10 @@ int dmuon_step_host(dmuon_context* ctx, const dmuon_matrix* mats, const dmuon_ho
   // early parameter copies would slow the gradient copies that the later
   // groups' compute is waiting for; where they do not, the early groups'
   // parameter copies are not on the critical path anyway.
+  // (The timeline's "all gradients in" mark goes here too, right behind the
+  // last gradient copy: recorded later, on an idle stream, it would carry
+  // the time the host finished enqueueing instead.)
+  mark(1, ctx->h2d);
   if (cudaEventRecord(ev(kH2dAll), ctx->h2d) != cudaSuccess || cudaStreamWaitEvent(ctx->d2h, ev(kH2dAll), 0) != cudaSuccess)
     return join(cuda_fail(cudaGetLastError(), "step_host"));
   auto adam = [&]() {

@@ -426,6 +426,13 @@ static cudaError_t launch_variant3(const NsLaunch& L, int n_pairs, cudaStream_t 
 template <int STAGES>
 static cudaError_t launch_variant(const NsLaunch& L, int n_pairs, cudaStream_t st) {
   if (L.fuse_update) return launch_variant3<STAGES, true, 4>(L, n_pairs, st);
+  // Short main loops (8 epilogue warps) are bound by the epilogue drain: a
+  // launch without aux takes the pipelined drain there (GPT-2 and
+  // many-small sets -2 to -3 %).  Long main loops keep the plain drain (the
+  // overlapped epilogues' faster stores slowed the operand copies: +1 ms on
+  // the Llama-3-8B Combine).
+  const bool no_aux = L.kind == kGram || (L.kind == kCombine && L.a == 0.f);
+  if (L.epi8 && no_aux && L.tri) return launch_variant3<STAGES, false, 8, false, true>(L, n_pairs, st);
   return L.epi8 ? launch_variant3<STAGES, false, 8>(L, n_pairs, st) : launch_variant3<STAGES, false, 4>(L, n_pairs, st);
 }
 

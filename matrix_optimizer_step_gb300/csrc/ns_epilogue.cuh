@@ -382,10 +382,11 @@ namespace dmuon {
 // Combine once a*X is folded into the polynomial matrix), with the TMEM
 // drain software-pipelined: the load of chunk cc+1 is in flight while chunk
 // cc is scaled, packed and staged, so the TMEM latency is paid once per tile
-// instead of once per chunk.  Used by the 256 x 512 tiles, whose epilogue is
-// not hidden behind another tile's main loop (their two accumulators fill
-// all of TMEM).  Same arithmetic as ns_epilogue_tile_staged with beta = 0,
-// so the results are bit-identical.
+// instead of once per chunk.  Used where the epilogue is not hidden behind
+// another tile's main loop: the 256 x 512 tiles (their two accumulators fill
+// all of TMEM) and launches with main loops as short as the drain (8
+// epilogue warps).  Same arithmetic as ns_epilogue_tile_staged with
+// beta = 0, so the results are bit-identical.
 __device__ __forceinline__ void ns_epilogue_tile_staged_pipe(const NsLaunch& L, const NsProblem& P, int m0, int n0,
                                                              int row_in_tile, uint32_t t_lane, uint32_t stage_smem,
                                                              uint32_t& box_count, int c_begin, int c_end) {
