@@ -105,6 +105,49 @@ def test_noalloc_matches_oracle_on_two_calls(cuda_lib, shape, fp32_ns):
         mos.dmuon_context_destroy(ctx)
 
 
+@pytest.mark.parametrize("shape,ns_steps", [((1, 300), 5), ((130, 1), 5), ((7, 7), 5), ((96, 160), 0),
+                                            ((2, 20, 33), 0), ((1, 1), 3)])
+def test_noalloc_edge_shapes_and_no_iterations(cuda_lib, shape, ns_steps):
+    """Degenerate shapes (one row, one column, tiny) and ns_steps = 0 (the
+    update then applies the normalised momentum direction): the same bits as
+    dmuon_muon_step where both run the same kernels (min(m, n) < 64: the
+    fp32 kernels; no iteration: momentum, norm and update only), and the
+    oracle within the parity tolerances."""
+    mos = cuda_lib
+    capi = mos.capi
+    dev = torch.device("cuda")
+    g = torch.Generator().manual_seed(7)
+    W = torch.randn(shape, generator=g) * 0.02
+    grad = torch.randn(shape, generator=g).to(torch.bfloat16)
+    lr, mu, wd = 0.02, 0.95, 0.01
+    sides = []
+    for _ in range(2):
+        sides.append({"W": W.to(dev), "buf": torch.zeros(shape, device=dev), "g": grad.to(dev),
+                      "p": torch.empty(shape, device=dev, dtype=torch.bfloat16)})
+    ctx = mos.dmuon_context_create(0)
+    try:
+        d = [capi.matrix_desc(s["W"], s["buf"], s["g"], s["p"]) for s in sides]
+        mos.dmuon_muon_step_noalloc(d[0], lr, mu, wd, ns_steps, A, B, C)
+        mos.dmuon_muon_step_noalloc_sync()
+        mos.dmuon_muon_step(ctx, [d[1]], lr, mu, wd, ns_steps, A, B, C)
+        mos.dmuon_sync(ctx)
+    finally:
+        mos.dmuon_context_destroy(ctx)
+    m, n = shape[-2], shape[-1]
+    if min(m, n) < 64 or ns_steps == 0:
+        assert torch.equal(sides[0]["W"], sides[1]["W"]) and torch.equal(sides[0]["p"], sides[1]["p"])
+    W0 = W.double().numpy()
+    ref = omuon.muon_step(W0, np.zeros(shape), grad.double().numpy(), _f(lr), _f(mu), _f(wd), ns_steps,
+                          _f(A), _f(B), _f(C))
+    O = ((W0 * (1 - _f(lr) * _f(wd)) - sides[0]["W"].double().cpu().numpy())
+         / (_f(lr) * omuon.shape_scale(m, n))).reshape(-1, m, n)
+    # bf16 classes hold X0 in bf16 even with no iteration (2e-2); fp32 classes 1e-4.
+    tol = 1e-4 if min(m, n) < 64 else 2e-2
+    for k in range(O.shape[0]):
+        assert _frob(O[k], ref["O"].reshape(-1, m, n)[k]) <= tol, (shape, ns_steps, k)
+    assert torch.equal(sides[0]["p"], sides[0]["W"].to(torch.bfloat16))
+
+
 def test_noalloc_reports_a_wait_that_ran_out(cuda_lib):
     """A bounded wait given a barrier nothing completes records its site in
     the static array's error word; the sync query reports it once, clears
