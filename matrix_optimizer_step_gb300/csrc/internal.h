@@ -38,6 +38,11 @@ struct SliceDesc {
   int32_t chunk_begin;    // first chunk of this slice in the chunk table
   int32_t chunk_end;
   int32_t x_f32;          // 1: this slice's NS workspace is fp32 (fp32 CUDA-core path)
+  // Fused update with TMA stores: tensor maps (in NsLaunch::cmaps) of the
+  // slice's tensor's master (fp32, 32 x 32 boxes) and bf16 parameter
+  // (64 x 32 boxes, -1 = no parameter), and the slice's index within its
+  // tensor (the maps' third coordinate).
+  int32_t map_w, map_p, z_t;
 };
 
 // A contiguous run of one slice's elements (row-major element index of the
@@ -152,6 +157,9 @@ struct NsLaunch {
   int32_t wide;
   // CTA-pair kernel: ring depth of the 256 x 256 tiles (4 or 5).
   int32_t stages;
+  // Fused update: tensor maps of the callers' masters and parameters
+  // (SliceDesc::map_w / map_p index them).
+  const CUtensorMap* cmaps;
 };
 
 // ---- launch wrappers (each returns the cudaError_t of its launch) ----

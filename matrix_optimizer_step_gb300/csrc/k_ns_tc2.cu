@@ -76,12 +76,18 @@ constexpr int threads_of() {
   return (3 + EPI) * 32;
 }
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kStagingPerWarp = 2 * 4096;  // 2 boxes of 32 x 64 bf16
-template <int STAGES, int EPI, bool WIDE = false>
+// Epilogue staging per warp: 2 boxes of 32 x 64 bf16; the fused update
+// stages 2 fp32 boxes of 32 x 32 (W) and 2 bf16 boxes of 32 x 64 (param).
+template <bool FUSE>
+__host__ __device__ constexpr uint32_t staging_per_warp() {
+  return FUSE ? 4 * 4096 : 2 * 4096;
+}
+template <int STAGES, int EPI, bool WIDE = false, bool FUSE = false>
 constexpr size_t smem_bytes() {
-  return 1024 + STAGES * stage_bytes<WIDE>() + EPI * kStagingPerWarp + (2 * STAGES + 5) * 8 + 16;
+  return 1024 + STAGES * stage_bytes<WIDE>() + EPI * staging_per_warp<FUSE>() + (2 * STAGES + 5) * 8 + 16;
 }
 static_assert(smem_bytes<5, 8>() <= 227 * 1024, "shared memory budget");
+static_assert(smem_bytes<5, 4, false, true>() <= 227 * 1024, "shared memory budget (fused update)");
 // 3 stages of 48 KiB: a fourth does not fit beside 8 warps' staging boxes.
 static_assert(smem_bytes<3, 8, true>() <= 227 * 1024, "shared memory budget (wide)");
 // Every CTA allocates all 512 TMEM columns, so two CTAs must never share an
@@ -150,7 +156,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_of<EPI>(), 1
                                              ~static_cast<uintptr_t>(1023));
   const uint32_t ring = smem_u32(smem);
   const uint32_t staging = ring + STAGES * STAGE_BYTES;  // 1 KiB aligned (swizzled TMA source)
-  uint64_t* bar_mem = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES + EPI * kStagingPerWarp);
+  constexpr uint32_t kStaging = staging_per_warp<FUSE>();
+  uint64_t* bar_mem = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES + EPI * kStaging);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_mem + kNumBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -346,7 +353,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_of<EPI>(), 1
     const int quarter = warp & 3;
     const int half = (warp - 2) >> 2;
     const int row_in_tile = 128 * static_cast<int>(rank) + quarter * 32 + lane;
-    const uint32_t my_staging = staging + static_cast<uint32_t>(warp - 2) * kStagingPerWarp;
+    const uint32_t my_staging = staging + static_cast<uint32_t>(warp - 2) * kStaging;
     uint32_t box_count = 0;
     int use = 0;  // accumulator slot uses so far, as counted by the MMA issuer
     for (int t = t_begin; t < t_end; ++t) {
@@ -369,7 +376,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_of<EPI>(), 1
       const uint32_t t_lane =
           tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * TILE);
       if (FUSE)
-        ns_epilogue_tile<true>(L, P, tm * TILE, sub_tn * TILE, row_in_tile, t_lane, false);
+        ns_epilogue_tile_fused_tma(L, P, tm * TILE, sub_tn * TILE, row_in_tile, t_lane, my_staging);
       else if (PIPE)
         ns_epilogue_tile_staged_pipe(L, P, tm * TILE, sub_tn * TILE, row_in_tile, t_lane, my_staging, box_count,
                                      c_begin, c_end);
@@ -408,7 +415,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_of<EPI>(), 1
 template <int STAGES, bool FUSE, int EPI, bool WIDE = false, bool PIPE = false>
 static cudaError_t launch_variant3(const NsLaunch& L, int n_pairs, cudaStream_t st) {
   static unsigned long long attr_mask = 0;
-  constexpr size_t smem = smem_bytes<STAGES, EPI, WIDE>();
+  constexpr size_t smem = smem_bytes<STAGES, EPI, WIDE, FUSE>();
   if (attr_needed_on_current_device(&attr_mask)) {
     cudaError_t e = cudaFuncSetAttribute(ns_tc2_kernel<STAGES, FUSE, EPI, WIDE, PIPE>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));

@@ -463,3 +463,130 @@ __device__ __forceinline__ void ns_epilogue_tile_staged_pipe(const NsLaunch& L, 
 }
 
 }  // namespace dmuon
+
+namespace dmuon {
+
+// The last Combine's fused update on the CTA-pair kernel, with the results
+// written by TMA tile stores: per 32-column chunk a warp computes
+// W' = W*(1 - lr*wd) - lr*scale*X for its 32 rows (W read row by row, as in
+// ns_epilogue_tile<true>), stages W' as a 32 x 32 fp32 box and the bf16
+// parameter as half of a 32 x 64 bf16 box in swizzled shared memory (16-byte
+// piece j of row r at r*128 + ((j ^ (r & 7)) * 16)), and lane 0 stores the
+// boxes with cp.async.bulk.tensor through the slice's maps (S.map_w,
+// S.map_p in L.cmaps; rows and columns past the tensor's edge are clipped
+// by the hardware).  Per warp: W boxes alternate between two 4 KiB buffers
+// at stage_smem and stage_smem + 4096, parameter boxes between two at
+// stage_smem + 8192 and + 12288; before writing a chunk, lane 0 waits until
+// at most the previous chunk's stores are still reading shared memory.
+// Same arithmetic as ns_epilogue_tile<true>, so the results are
+// bit-identical to it.
+__device__ __forceinline__ void ns_epilogue_tile_fused_tma(const NsLaunch& L, const NsProblem& P, int m0, int n0,
+                                                           int row_in_tile, uint32_t t_lane, uint32_t stage_smem) {
+  constexpr int BN = 256;
+  const int lane = threadIdx.x & 31;
+  float g = 1.f;
+  if (L.gscale && L.gpow > 0) {
+    const float s = L.gscale[P.slice];
+    g = (L.gpow == 2) ? s * s : s;
+  }
+  const float alpha = g, beta = g * L.a;
+  const int row = m0 + row_in_tile;
+  const bool row_ok = row < P.M;
+  const int warp_row0 = row - lane;
+  if (warp_row0 >= P.M) return;  // no row of this warp is in the output
+  const SliceDesc& S = L.slices[P.slice];
+  const float* w_row = S.master + static_cast<int64_t>(row) * S.n;
+  const float decay = 1.0f - L.lr * L.wd;
+  const float step = L.lr * S.shape_scale;
+  const bool w_vec = S.vec_ok != 0;
+  const CUtensorMap* map_w = L.cmaps + S.map_w;
+  const CUtensorMap* map_p = S.map_p >= 0 ? L.cmaps + S.map_p : nullptr;
+  const int z = S.z_t;
+  const uint16_t* aux_row = reinterpret_cast<const uint16_t*>(P.aux) + static_cast<int64_t>(row) * P.ld_aux;
+  const uint16_t* auxlo_row = P.aux_lo ? P.aux_lo + static_cast<int64_t>(row) * P.ld_aux : nullptr;
+  const bool need_aux = beta != 0.f && row_ok;
+  auto load_aux = [&](int cc, uint4 (&q)[8]) {
+    const int c0 = n0 + cc * 32;
+    if (!need_aux || c0 + 32 > P.N) return;
+    load_aux_chunk(aux_row, auxlo_row, c0, q);
+  };
+  const int n_chunks = min(BN / 32, (P.N - n0 + 31) / 32);
+  const uint32_t swz = static_cast<uint32_t>(lane) * 128u;
+  uint4 aux_next[8];
+  load_aux(0, aux_next);
+#pragma unroll 1
+  for (int cc = 0; cc < n_chunks; ++cc) {
+    const int col0 = n0 + cc * 32;
+    uint4 aux_cur[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) aux_cur[i] = aux_next[i];
+    if (cc + 1 < n_chunks) load_aux(cc + 1, aux_next);
+    __syncwarp();
+    uint32_t r[32];
+    tmem_ld_32x32b_x32(t_lane + static_cast<uint32_t>(cc * 32), r);
+    const bool full_chunk = (col0 + 32 <= P.N);
+    float auxf[32];
+    if (need_aux && full_chunk) {
+      unpack_aux_chunk(aux_cur, auxlo_row != nullptr, auxf);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const int c = col0 + j;
+        auxf[j] = (need_aux && c < P.N)
+                      ? bf16_bits_to_f32(aux_row[c]) + (auxlo_row ? bf16_bits_to_f32(auxlo_row[c]) : 0.f)
+                      : 0.f;
+      }
+    }
+    float w[32];
+    if (row_ok && full_chunk && w_vec) {
+      const float4* src = reinterpret_cast<const float4*>(w_row + col0);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float4 q = src[i];
+        w[4 * i] = q.x; w[4 * i + 1] = q.y; w[4 * i + 2] = q.z; w[4 * i + 3] = q.w;
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) w[j] = (row_ok && col0 + j < P.N) ? w_row[col0 + j] : 0.f;
+    }
+    tmem_ld_wait_regs(r);
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      float v = alpha * __uint_as_float(r[j]);
+      if (beta != 0.f) v = fmaf(beta, auxf[j], v);
+      w[j] = fmaf(-step, v, w[j] * decay);
+    }
+    // Buffers of this chunk: free once at most the previous chunk's stores
+    // are still reading shared memory.
+    if (lane == 0) bulk_wait_group_read<1>();
+    __syncwarp();
+    const uint32_t wbuf = stage_smem + static_cast<uint32_t>(cc & 1) * 4096u;
+    const uint32_t pbuf = stage_smem + 8192u + static_cast<uint32_t>((cc >> 1) & 1) * 4096u;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const uint32_t off = swz + ((static_cast<uint32_t>(j) ^ static_cast<uint32_t>(lane & 7)) << 4);
+      st_shared_v4(wbuf + off, __float_as_uint(w[4 * j]), __float_as_uint(w[4 * j + 1]),
+                   __float_as_uint(w[4 * j + 2]), __float_as_uint(w[4 * j + 3]));
+    }
+    if (map_p) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t j = static_cast<uint32_t>(4 * (cc & 1) + i);
+        const uint32_t off = swz + ((j ^ static_cast<uint32_t>(lane & 7)) << 4);
+        st_shared_v4(pbuf + off, pack_bf16x2(w[8 * i], w[8 * i + 1]), pack_bf16x2(w[8 * i + 2], w[8 * i + 3]),
+                     pack_bf16x2(w[8 * i + 4], w[8 * i + 5]), pack_bf16x2(w[8 * i + 6], w[8 * i + 7]));
+      }
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_3d(map_w, wbuf, col0, warp_row0, z);
+      // A parameter box holds two chunks; the last chunk of a ragged tile
+      // stores its half alone (the other half lies past the edge).
+      if (map_p && ((cc & 1) || cc + 1 == n_chunks)) tma_store_3d(map_p, pbuf, n0 + 64 * (cc >> 1), warp_row0, z);
+      bulk_commit_group();
+    }
+  }
+}
+
+}  // namespace dmuon

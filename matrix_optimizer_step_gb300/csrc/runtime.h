@@ -268,10 +268,23 @@ struct MuonSlot {
   MuonPlan plan;
   StagedTable table;
   std::vector<uint8_t> checked;
+  // Tensor maps of the callers' masters and parameters for the fused
+  // update's TMA stores, rebuilt when the descriptor array changes.
+  StagedTable cmaps;
+  std::vector<uint8_t> cmaps_key;
+  std::vector<CUtensorMap> cmaps_host;
+  std::vector<int32_t> map_w, map_p;  // per tensor of the call, -1 = not storable by TMA
+  bool all_tma = false;               // every bf16-class tensor has its maps
   void release() {
     plan.release();
     table.release();
     checked.clear();
+    cmaps.release();
+    cmaps_key.clear();
+    cmaps_host.clear();
+    map_w.clear();
+    map_p.clear();
+    all_tma = false;
   }
 };
 

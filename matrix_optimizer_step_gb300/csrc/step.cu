@@ -27,11 +27,81 @@ int prepare_slot(dmuon_context* ctx, MuonSlot& S, const dmuon_matrix* mats, int 
   return st;
 }
 
+// Tensor maps of the callers' fp32 masters (32 x 32 boxes) and bf16
+// parameters (64 x 32 boxes) for the fused update's TMA stores, per tensor
+// of a bf16 class, rebuilt only when the descriptor array changes.  A TMA
+// store needs a 16-byte-aligned base and rows whose byte length is a
+// multiple of 16 (n % 4 == 0 for the master, n % 8 == 0 for the parameter);
+// a tensor that misses either gets no maps, and then no launch fuses the
+// update (the last Combine stores X and the streaming pass updates W).
+int build_caller_maps(MuonSlot& S, const dmuon_matrix* mats, int n, cudaStream_t s) {
+  std::vector<uint8_t> key;
+  keep_bytes(key, mats, n);
+  if (key == S.cmaps_key && !S.cmaps_host.empty()) return DMUON_OK;
+  const MuonPlan& P = S.plan;
+  std::vector<char> bf16_tensor(static_cast<size_t>(n), 0);
+  for (const SliceRef& R : P.slices)
+    if (!P.classes[static_cast<size_t>(R.cls)].f32) bf16_tensor[static_cast<size_t>(R.mat)] = 1;
+  S.cmaps_host.clear();
+  S.map_w.assign(static_cast<size_t>(n), -1);
+  S.map_p.assign(static_cast<size_t>(n), -1);
+  S.all_tma = true;
+  EncodeTiledFn enc = get_encode_fn();
+  for (int i = 0; i < n; ++i) {
+    if (!bf16_tensor[static_cast<size_t>(i)]) continue;
+    const dmuon_matrix& M = mats[i];
+    const int64_t m = M.shape[M.rank - 2], nn = M.shape[M.rank - 1];
+    int64_t lead = 1;
+    for (int d = 0; d < M.rank - 2; ++d) lead *= M.shape[d];
+    const bool ok = enc && aligned16(M.master) && nn % 4 == 0 &&
+                    (!M.param_bf16 || (aligned16(M.param_bf16) && nn % 8 == 0));
+    if (!ok) {
+      S.all_tma = false;
+      continue;
+    }
+    cuuint64_t dims[3] = {(cuuint64_t)nn, (cuuint64_t)m, (cuuint64_t)lead};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUtensorMap mw;
+    cuuint64_t sw[2] = {(cuuint64_t)(nn * 4), (cuuint64_t)(m * nn * 4)};
+    cuuint32_t bw[3] = {32, 32, 1};
+    if (enc(&mw, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, M.master, dims, sw, bw, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) !=
+        CUDA_SUCCESS) {
+      S.all_tma = false;
+      continue;
+    }
+    S.map_w[static_cast<size_t>(i)] = static_cast<int32_t>(S.cmaps_host.size());
+    S.cmaps_host.push_back(mw);
+    if (M.param_bf16) {
+      CUtensorMap mp;
+      cuuint64_t spr[2] = {(cuuint64_t)(nn * 2), (cuuint64_t)(m * nn * 2)};
+      cuuint32_t bp[3] = {64, 32, 1};
+      if (enc(&mp, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, M.param_bf16, dims, spr, bp, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS) {
+        S.map_w[static_cast<size_t>(i)] = -1;
+        S.cmaps_host.pop_back();
+        S.all_tma = false;
+        continue;
+      }
+      S.map_p[static_cast<size_t>(i)] = static_cast<int32_t>(S.cmaps_host.size());
+      S.cmaps_host.push_back(mp);
+    }
+  }
+  if (S.cmaps_host.empty()) S.cmaps_host.resize(1);  // keep a valid (unused) table
+  int st = S.cmaps.put(S.cmaps_host.data(), S.cmaps_host.size() * sizeof(CUtensorMap), s);
+  if (st != DMUON_OK) return st;
+  S.cmaps_key.swap(key);
+  return DMUON_OK;
+}
+
 // Stage 1 of a Muon step on a prepared slot: the per-call pointer table,
 // uploaded on stream s.
 int muon_stage_table(dmuon_context* ctx, MuonSlot& S, const dmuon_matrix* mats, int n, int32_t ns_steps,
                      cudaStream_t s) {
   int st = check_matrices_reachable(ctx, S.checked, mats, n);
+  if (st != DMUON_OK) return st;
+  st = build_caller_maps(S, mats, n, s);
   if (st != DMUON_OK) return st;
   MuonPlan& P = S.plan;
   uint8_t* ws = static_cast<uint8_t*>(ctx->ws.p);
@@ -62,6 +132,9 @@ int muon_stage_table(dmuon_context* ctx, MuonSlot& S, const dmuon_matrix* mats, 
     D.shape_scale = static_cast<float>(std::sqrt(std::max(1.0, double(C.m) / double(C.n))));
     D.chunk_begin = P.slice_chunk_begin[i];
     D.chunk_end = P.slice_chunk_end[i];
+    D.map_w = S.map_w[static_cast<size_t>(R.mat)];
+    D.map_p = S.map_p[static_cast<size_t>(R.mat)];
+    D.z_t = static_cast<int32_t>(R.elem_offset / (static_cast<int64_t>(C.m) * C.n));
   }
   return S.table.put(table.data(), table.size() * sizeof(SliceDesc), s);
 }
@@ -101,7 +174,7 @@ int muon_launch_ns(dmuon_context* ctx, MuonSlot& S, float lr, float wd, int32_t 
   const Tuning& tu = ctx->tune;
   const bool pairs = tu.ns_pairs != 0;
   const PhaseTiles& last_combine = pairs ? P.phase2[kCombine] : P.phase[kCombine];
-  const bool fuse_last = last_combine.mean_kblocks >= static_cast<double>(tu.epi8_below);
+  const bool fuse_last = last_combine.mean_kblocks >= static_cast<double>(tu.epi8_below) && S.all_tma;
   for (int it = 0; it < ns_steps; ++it) {
     const int variant = it < 2 ? 2 + it : (it & 1);
     for (int kind = kGram; kind <= kCombine; ++kind) {
@@ -128,6 +201,7 @@ int muon_launch_ns(dmuon_context* ctx, MuonSlot& S, float lr, float wd, int32_t 
           // The last Combine applies the update itself (no X store, no update pass).
           T.fuse_update = 1;
           T.slices = d_slices;
+          T.cmaps = static_cast<const CUtensorMap*>(S.cmaps.dev.p);
           T.lr = lr;
           T.wd = wd;
         }

@@ -307,6 +307,44 @@ def test_pair_kernel_tuning_variants(cuda_lib, settings):
         assert max(r["O_slices"]) <= bf16_tol(r["shape"]), r
 
 
+FUSED_SHAPES = [(520, 520), (200, 328), (1000, 136), (136, 1000), (2, 300, 600), (3, 64, 96), (1024, 2048),
+                (2048, 1024), (8, 4096)]
+
+
+@pytest.mark.parametrize("settings", [{8: 0}, {8: 0, 7: 0}])
+def test_fused_update_with_tma_stores_on_ragged_tiles(cuda_lib, settings):
+    """The last Combine applies the update in its epilogue and writes W and
+    the bf16 parameter with TMA tile stores (every tensor here has rows of a
+    multiple of 16 bytes); tiles cut by the tensors' edges rely on the
+    stores' clipping.  Key 8 = 0 fuses every step's last Combine; with key 7
+    = 0 the fused epilogue also reads X as aux.  Against the oracle."""
+    try:
+        for key, value in settings.items():
+            cuda_lib.dmuon_set_tuning(key, value)
+        res = run_muon(cuda_lib, FUSED_SHAPES, seed=51 + sum(settings), steps=2)
+    finally:
+        for key in settings:
+            cuda_lib.dmuon_set_tuning(key, TUNING_DEFAULTS[key])
+    for errs in res:
+        for r in errs:
+            assert r["buf"] <= 1e-6 and r["param_exact"], r
+            assert max(r["O_slices"]) <= bf16_tol(r["shape"]), r
+
+
+def test_unstorable_tensor_falls_back_to_the_update_pass(cuda_lib):
+    """A call with a tensor whose rows are not a multiple of 16 bytes (n = 130)
+    does not fuse the update (the last Combine stores X and the streaming pass
+    updates W); the results stay within the tolerances."""
+    cuda_lib.dmuon_set_tuning(8, 0)
+    try:
+        res = run_muon(cuda_lib, [(1024, 130), (512, 1024)], seed=53)[0]
+    finally:
+        cuda_lib.dmuon_set_tuning(8, TUNING_DEFAULTS[8])
+    for r in res:
+        assert r["buf"] <= 1e-6 and r["param_exact"], r
+        assert max(r["O_slices"]) <= bf16_tol(r["shape"]), r
+
+
 def test_wide_tiles_bit_identical_to_narrow(cuda_lib):
     """A 256 x 512 tile accumulates each output element over the same
     k-steps in the same order as two 256 x 256 tiles, so a step on wide
