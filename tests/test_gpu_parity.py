@@ -331,6 +331,35 @@ def test_fused_update_with_tma_stores_on_ragged_tiles(cuda_lib, settings):
             assert max(r["O_slices"]) <= bf16_tol(r["shape"]), r
 
 
+def test_fused_update_without_bf16_parameter(cuda_lib):
+    """param_bf16 = NULL: the fused update stores W' only (no parameter map);
+    W against the oracle, on ragged tiles, rank-3 included."""
+    shapes = [(520, 520), (2, 300, 600), (1000, 136)]
+    g = torch.Generator().manual_seed(61)
+    W = [torch.randn(s, generator=g) * 0.02 for s in shapes]
+    G = [torch.randn(s, generator=g).to(torch.bfloat16) for s in shapes]
+    Wd = [w.cuda() for w in W]
+    Bd = [torch.zeros(s, device="cuda") for s in shapes]
+    Gd = [x.cuda() for x in G]
+    cuda_lib.dmuon_set_tuning(8, 0)
+    try:
+        st = cuda_lib.OwnerStep(0)
+    finally:
+        cuda_lib.dmuon_set_tuning(8, TUNING_DEFAULTS[8])
+    st.set_muon(Wd, Bd, Gd, None)
+    st.muon_step(0.02, 0.95, 0.01, 5, A, B, C)
+    st.sync()
+    st.close()
+    for i, s in enumerate(shapes):
+        m, n = s[-2], s[-1]
+        ref = omuon.muon_step(W[i].double().numpy(), np.zeros(s), G[i].double().numpy(), _f(0.02), _f(0.95),
+                              _f(0.01), 5, _f(A), _f(B), _f(C))
+        O = ((W[i].double().numpy() * (1 - _f(0.02) * _f(0.01)) - Wd[i].double().cpu().numpy())
+             / (_f(0.02) * omuon.shape_scale(m, n))).reshape(-1, m, n)
+        for k in range(O.shape[0]):
+            assert _frob(O[k], ref["O"].reshape(-1, m, n)[k]) <= 2e-2, (s, k)
+
+
 def test_unstorable_tensor_falls_back_to_the_update_pass(cuda_lib):
     """A call with a tensor whose rows are not a multiple of 16 bytes (n = 130)
     does not fuse the update (the last Combine stores X and the streaming pass
