@@ -212,3 +212,45 @@ def test_owner_partition_balances_the_llama_set():
         assert max(load) <= mean + top
         # 224 tensors of 7 shapes: LPT evens the owners out to well under 1 %.
         assert max(load) <= 1.01 * mean, (world, max(load) / mean)
+
+
+def test_nccl_branch_issues_the_pages_collectives(monkeypatch):
+    """The NCCL branch (which needs one GPU per rank, so it cannot run here)
+    checked by recording its calls as rank 1 of 2: a mean reduce of each
+    owner's contiguous gradient range to that owner, an in-place mean
+    reduce_scatter of the sharded gradients onto this rank's piece, a
+    broadcast of each owner's parameter range from it, and an in-place
+    all_gather of the pieces; every call on a view of the flat buffers."""
+    from matrix_optimizer_step_gb300.owner_dist import DistributedOwnerStep, OwnerLayout
+
+    calls = []
+    monkeypatch.setattr(dist, "get_world_size", lambda group=None: 2)
+    monkeypatch.setattr(dist, "get_rank", lambda group=None: 1)
+    monkeypatch.setattr(dist, "get_backend", lambda group=None: "nccl")
+    monkeypatch.setattr(dist, "reduce", lambda t, dst, op, group=None: calls.append(("reduce", t, dst, op)))
+    monkeypatch.setattr(dist, "broadcast", lambda t, src, group=None: calls.append(("broadcast", t, src, None)))
+    monkeypatch.setattr(dist, "reduce_scatter_tensor",
+                        lambda out, inp, op, group=None: calls.append(("reduce_scatter", (out, inp), None, op)))
+    monkeypatch.setattr(dist, "all_gather_into_tensor",
+                        lambda out, inp, group=None: calls.append(("all_gather", (out, inp), None, None)))
+    L = OwnerLayout.build(MUON, ADAMW, SHARDED, 2)
+    ds = DistributedOwnerStep(L, device="cpu", grad_dtype=torch.float32, stepper=OracleStepper())
+    ds.reduce_grads()
+    ds.publish_params()
+    elt = ds.grad_flat.element_size()
+    kinds = [c[0] for c in calls]
+    assert kinds == ["reduce", "reduce", "reduce_scatter", "broadcast", "broadcast", "all_gather"]
+    for r in range(2):
+        a, b = L.owner_range[r]
+        _, t, dst, op = calls[r]
+        assert dst == r and op == dist.ReduceOp.AVG
+        assert t.data_ptr() == ds.grad_flat.data_ptr() + a * elt and t.numel() == b - a
+        _, t, src, _ = calls[3 + r]
+        assert src == r
+        assert t.data_ptr() == ds.param_flat.data_ptr() + a * ds.param_flat.element_size() and t.numel() == b - a
+    (out, inp), op = calls[2][1], calls[2][3]
+    assert op == dist.ReduceOp.AVG and inp.data_ptr() == ds.sp_grad_flat.data_ptr()
+    assert out.data_ptr() == ds.sp_grad_flat.data_ptr() + 1 * L.piece * elt and out.numel() == L.piece
+    out, inp = calls[5][1]
+    assert out.data_ptr() == ds.sp_param_flat.data_ptr() and out.numel() == 2 * L.piece
+    assert inp.data_ptr() == ds.sp_param_flat.data_ptr() + L.piece * ds.sp_param_flat.element_size()
