@@ -388,7 +388,8 @@ DMUON_API int dmuon_selftest_wait_timeout(dmuon_context* ctx, int32_t timeout_us
  *   key 2: tensor-core kernel of the Newton-Schulz phases (1 = CTA pairs,
  *          cta_group::2, on 256 x 256 tiles and, per key 12, 256 x 512
  *          ones, the default; 0 = one CTA per 128 x 256 tile).
- *   key 3: pipeline depth of the CTA-pair kernel (4 or 5 stages; default 4).
+ *   key 3: pipeline depth of the CTA-pair kernel (4 or 5 stages; default 4;
+ *          the last Combine with the fused update always runs 4).
  *   key 4: tile order inside a problem (1 = longer tile dimension outer, the
  *          default; 0 = rows outer).  Takes effect at the next plan build.
  *   key 6: CTA-pair kernel keeps symmetric products as upper blocks only and

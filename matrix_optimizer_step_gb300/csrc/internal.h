@@ -155,7 +155,8 @@ struct NsLaunch {
   // CTA-pair kernel: the tile list holds 256 x 512 tiles (kTileWideBit);
   // needs tri, excludes fuse_update.
   int32_t wide;
-  // CTA-pair kernel: ring depth of the 256 x 256 tiles (4 or 5).
+  // CTA-pair kernel: ring depth of the 256 x 256 tiles (4 or 5; a launch
+  // with fuse_update always runs 4).
   int32_t stages;
   // Fused update: tensor maps of the callers' masters and parameters
   // (SliceDesc::map_w / map_p index them).

@@ -69,25 +69,35 @@ constexpr uint32_t MN_BOX_BYTES = 64 * 64 * 2;        // 8 KiB
 // fast, which pays where the main loop is short (K of a few k-blocks: small
 // matrices), but their global loads then compete with the operand copies
 // for each SM's memory bandwidth, which slows long main loops; the host
-// picks per launch.  The fused update always runs with 4 (its register
-// needs leave no room for more threads).
+// picks per launch.  The fused update always runs with 4 (its staging boxes
+// and registers leave no room for more warps).
 template <int EPI>
 constexpr int threads_of() {
   return (3 + EPI) * 32;
 }
 constexpr uint32_t kTmemCols = 512;
 // Epilogue staging per warp: 2 boxes of 32 x 64 bf16; the fused update
-// stages 2 fp32 boxes of 32 x 32 (W) and 2 bf16 boxes of 32 x 64 (param).
+// stages kFusedWBoxes fp32 boxes of 32 x 32 (W, loaded and stored by TMA)
+// and 2 bf16 boxes of 32 x 64 (param).
 template <bool FUSE>
 __host__ __device__ constexpr uint32_t staging_per_warp() {
-  return FUSE ? 4 * 4096 : 2 * 4096;
+  return FUSE ? (kFusedWBoxes + 2) * 4096 : 2 * 4096;
+}
+// mbarriers: full/empty per ring stage, 2 accumulator full/empty pairs, the
+// drain barrier, and (fused update) one per W box buffer of each epilogue warp.
+template <int STAGES, int EPI, bool FUSE>
+__host__ __device__ constexpr int num_bars() {
+  return 2 * STAGES + 2 + 2 + 1 + (FUSE ? kFusedWBoxes * EPI : 0);
 }
 template <int STAGES, int EPI, bool WIDE = false, bool FUSE = false>
 constexpr size_t smem_bytes() {
-  return 1024 + STAGES * stage_bytes<WIDE>() + EPI * staging_per_warp<FUSE>() + (2 * STAGES + 5) * 8 + 16;
+  return 1024 + STAGES * stage_bytes<WIDE>() + EPI * staging_per_warp<FUSE>() + num_bars<STAGES, EPI, FUSE>() * 8 +
+         16;
 }
 static_assert(smem_bytes<5, 8>() <= 227 * 1024, "shared memory budget");
-static_assert(smem_bytes<5, 4, false, true>() <= 227 * 1024, "shared memory budget (fused update)");
+// The fused update runs with a 4-stage ring: a fifth stage does not fit
+// beside its W boxes.
+static_assert(smem_bytes<4, 4, false, true>() <= 227 * 1024, "shared memory budget (fused update)");
 // 3 stages of 48 KiB: a fourth does not fit beside 8 warps' staging boxes.
 static_assert(smem_bytes<3, 8, true>() <= 227 * 1024, "shared memory budget (wide)");
 // Every CTA allocates all 512 TMEM columns, so two CTAs must never share an
@@ -150,7 +160,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_of<EPI>(), 1
   static_assert(!PIPE || !FUSE, "pipelined drain: plain stores only");
   constexpr uint32_t STAGE_BYTES = stage_bytes<WIDE>();
   constexpr int kProducerBWarp = 2 + EPI;
-  constexpr int kNumBars = 2 * STAGES + 2 + 2 + 1;
+  constexpr int kNumBars = num_bars<STAGES, EPI, FUSE>();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -167,6 +177,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_of<EPI>(), 1
   auto tfull = [&](int a) { return bar0 + 8u * (2 * STAGES + a); };
   auto tempty = [&](int a) { return bar0 + 8u * (2 * STAGES + 2 + a); };
   const uint32_t drain = bar0 + 8u * (2 * STAGES + 4);
+  const uint32_t wbars = bar0 + 8u * (2 * STAGES + 5);  // fused update: kFusedWBoxes per epilogue warp
 
   const uint32_t rank = cluster_ctarank();
   const bool leader = rank == 0;
@@ -184,6 +195,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_of<EPI>(), 1
       mbar_init(tempty(a), 2 * EPI);  // every epilogue warp of both CTAs
     }
     mbar_init(drain, 1);
+    for (int i = 0; i < (FUSE ? kFusedWBoxes * EPI : 0); ++i) mbar_init(wbars + 8u * i, 1);
     *abort_flag = 0;
     fence_barrier_init();
     fence_proxy_async_smem();
@@ -355,6 +367,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_of<EPI>(), 1
     const int row_in_tile = 128 * static_cast<int>(rank) + quarter * 32 + lane;
     const uint32_t my_staging = staging + static_cast<uint32_t>(warp - 2) * kStaging;
     uint32_t box_count = 0;
+    const uint32_t my_wbars = wbars + 8u * static_cast<uint32_t>(kFusedWBoxes * (warp - 2));
+    uint32_t w_issued = 0, w_used = 0;  // fused update: W boxes requested / consumed
     int use = 0;  // accumulator slot uses so far, as counted by the MMA issuer
     for (int t = t_begin; t < t_end; ++t) {
       const uint2 tile = L.tiles[t];
@@ -371,13 +385,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_of<EPI>(), 1
       const int c_begin = (EPI == 8 && !wide) ? 4 * half : 0;
       const int c_end = (EPI == 8 && !wide) ? c_begin + 4 : 8;
       use += wide ? 2 : 1;
+      if (FUSE) fused_w_prefetch(L, P, tm * TILE, sub_tn * TILE, row_in_tile, my_staging, my_wbars, w_issued);
       if (!mbar_wait_bounded_cluster(tfull(acc), acc_phase, abort_flag, L.err, kErrTimeoutEpilogue)) break;
       tc_fence_after();
       const uint32_t t_lane =
           tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * TILE);
-      if (FUSE)
-        ns_epilogue_tile_fused_tma(L, P, tm * TILE, sub_tn * TILE, row_in_tile, t_lane, my_staging);
-      else if (PIPE)
+      if (FUSE) {
+        if (!ns_epilogue_tile_fused_tma(L, P, tm * TILE, sub_tn * TILE, row_in_tile, t_lane, my_staging, my_wbars,
+                                        w_issued, w_used, abort_flag))
+          break;
+      } else if (PIPE)
         ns_epilogue_tile_staged_pipe(L, P, tm * TILE, sub_tn * TILE, row_in_tile, t_lane, my_staging, box_count,
                                      c_begin, c_end);
       else
@@ -396,6 +413,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_of<EPI>(), 1
             mbar_arrive_cluster(mapa_shared(tempty(acc), 0));
         }
       }
+    }
+    if (FUSE) {
+      // After an abort, W boxes may still be on their way into shared
+      // memory: wait (bounded) for each before the block exits.
+      volatile int no_abort = 0;
+      for (uint32_t g = w_used; g < w_issued; ++g)
+        mbar_wait_bounded(my_wbars + 8u * (g % kFusedWBoxes), (g / kFusedWBoxes) & 1u, &no_abort, nullptr, 0);
     }
     if (lane == 0) bulk_wait_group<0>();  // staged TMA stores complete
     __syncwarp();
@@ -426,13 +450,14 @@ static cudaError_t launch_variant3(const NsLaunch& L, int n_pairs, cudaStream_t 
   return cudaGetLastError();
 }
 
-// The fused update keeps 4 epilogue warps: it runs on long main loops only
-// (short ones store X and update in a separate pass), where more concurrent
-// W traffic slows the operand copies (measured +5 ms per Llama-3-8B step
-// with 8 warps and an aux-free epilogue).
+// The fused update keeps 4 epilogue warps and a 4-stage ring: it runs on
+// long main loops only (short ones store X and update in a separate pass),
+// where more concurrent W traffic slows the operand copies (measured +5 ms
+// per Llama-3-8B step with 8 warps and an aux-free epilogue), and its W
+// boxes leave no shared memory for a fifth stage.
 template <int STAGES>
 static cudaError_t launch_variant(const NsLaunch& L, int n_pairs, cudaStream_t st) {
-  if (L.fuse_update) return launch_variant3<STAGES, true, 4>(L, n_pairs, st);
+  if (L.fuse_update) return launch_variant3<4, true, 4>(L, n_pairs, st);
   // Short main loops (8 epilogue warps) are bound by the epilogue drain: a
   // launch without aux takes the pipelined drain there (GPT-2 and
   // many-small sets -2 to -3 %).  Long main loops keep the plain drain (the

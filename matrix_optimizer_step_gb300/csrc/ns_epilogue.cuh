@@ -466,23 +466,83 @@ __device__ __forceinline__ void ns_epilogue_tile_staged_pipe(const NsLaunch& L, 
 
 namespace dmuon {
 
-// The last Combine's fused update on the CTA-pair kernel, with the results
-// written by TMA tile stores: per 32-column chunk a warp computes
-// W' = W*(1 - lr*wd) - lr*scale*X for its 32 rows (W read row by row, as in
-// ns_epilogue_tile<true>), stages W' as a 32 x 32 fp32 box and the bf16
-// parameter as half of a 32 x 64 bf16 box in swizzled shared memory (16-byte
-// piece j of row r at r*128 + ((j ^ (r & 7)) * 16)), and lane 0 stores the
-// boxes with cp.async.bulk.tensor through the slice's maps (S.map_w,
-// S.map_p in L.cmaps; rows and columns past the tensor's edge are clipped
-// by the hardware).  Per warp: W boxes alternate between two 4 KiB buffers
-// at stage_smem and stage_smem + 4096, parameter boxes between two at
-// stage_smem + 8192 and + 12288; before writing a chunk, lane 0 waits until
-// at most the previous chunk's stores are still reading shared memory.
+// The last Combine's fused update on the CTA-pair kernel, with W read and
+// the results written by TMA tile copies.  Per 32-column chunk a warp loads
+// the 32 x 32 fp32 box of W under its rows (cp.async.bulk.tensor through the
+// slice's map S.map_w in L.cmaps, 128-byte swizzle: 16-byte piece j of row r
+// at r*128 + ((j ^ (r & 7)) * 16); parts past the tensor's edge read as
+// zero), computes W' = W*(1 - lr*wd) - lr*scale*X in place in that box and
+// the bf16 parameter into half of a 32 x 64 bf16 box, and lane 0 stores both
+// boxes (rows and columns past the edge clipped by the hardware).
+//
+// Per warp: W boxes rotate through kFusedWBoxes 4 KiB buffers at
+// stage_smem, each with its own mbarrier (wbar0 + 8*i) that the load
+// completes; parameter boxes alternate between two buffers after them.  A
+// warp counts the W boxes it has requested (w_issued) and consumed
+// (w_used) over all its tiles: box g goes to buffer g % kFusedWBoxes and
+// is the (g / kFusedWBoxes)-th completion of that buffer's barrier.
+// fused_w_prefetch requests a tile's first two boxes before the epilogue
+// waits for the tile's accumulator (the main loop hides them); the chunk
+// loop requests box cc + 2 after storing chunk cc, once the store of chunk
+// cc - 1 (the buffer's previous user) has finished reading it.
 // Same arithmetic as ns_epilogue_tile<true>, so the results are
 // bit-identical to it.
-__device__ __forceinline__ void ns_epilogue_tile_fused_tma(const NsLaunch& L, const NsProblem& P, int m0, int n0,
-                                                           int row_in_tile, uint32_t t_lane, uint32_t stage_smem) {
-  constexpr int BN = 256;
+constexpr int kFusedWBoxes = 3;
+
+__device__ __forceinline__ void ld_shared_v4(uint32_t addr, float (&v)[4]) {
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3])
+               : "r"(addr)
+               : "memory");
+}
+
+struct FusedTile {
+  const CUtensorMap* map_w;
+  int warp_row0, z, n_chunks;
+  bool any_row;  // some row of this warp lies in the output
+};
+
+__device__ __forceinline__ FusedTile fused_tile(const NsLaunch& L, const NsProblem& P, int n0, int row) {
+  const int lane = threadIdx.x & 31;
+  const SliceDesc& S = L.slices[P.slice];
+  FusedTile f;
+  f.map_w = L.cmaps + S.map_w;
+  f.warp_row0 = row - lane;
+  f.z = S.z_t;
+  f.n_chunks = min(8, (P.N - n0 + 31) / 32);
+  f.any_row = f.warp_row0 < P.M;
+  return f;
+}
+
+// Lane 0 requests W box `g` (chunk cc of the tile) into its buffer.
+__device__ __forceinline__ void fused_w_request(const FusedTile& f, int n0, int cc, uint32_t g, uint32_t stage_smem,
+                                                uint32_t wbar0) {
+  const uint32_t b = g % kFusedWBoxes;
+  mbar_expect_tx(wbar0 + 8u * b, 4096u);
+  tma_load_3d(stage_smem + b * 4096u, f.map_w, wbar0 + 8u * b, n0 + 32 * cc, f.warp_row0, f.z);
+}
+
+// A tile's first two W boxes, requested before its accumulator is ready.
+__device__ __forceinline__ void fused_w_prefetch(const NsLaunch& L, const NsProblem& P, int m0, int n0,
+                                                 int row_in_tile, uint32_t stage_smem, uint32_t wbar0,
+                                                 uint32_t& w_issued) {
+  const FusedTile f = fused_tile(L, P, n0, m0 + row_in_tile);
+  if (!f.any_row) return;
+  const int first = min(2, f.n_chunks);
+  if ((threadIdx.x & 31) == 0) {
+    // Their buffers' previous users are boxes w_issued - 3 and - 2: at most
+    // the last store (box w_issued - 1) may still be reading.
+    bulk_wait_group_read<1>();
+    for (int cc = 0; cc < first; ++cc) fused_w_request(f, n0, cc, w_issued + cc, stage_smem, wbar0);
+  }
+  w_issued += first;
+}
+
+// Returns false when a wait for a W box ran out (the block is aborting).
+__device__ __forceinline__ bool ns_epilogue_tile_fused_tma(const NsLaunch& L, const NsProblem& P, int m0, int n0,
+                                                           int row_in_tile, uint32_t t_lane, uint32_t stage_smem,
+                                                           uint32_t wbar0, uint32_t& w_issued, uint32_t& w_used,
+                                                           volatile int* abort_flag) {
   const int lane = threadIdx.x & 31;
   float g = 1.f;
   if (L.gscale && L.gpow > 0) {
@@ -492,16 +552,12 @@ __device__ __forceinline__ void ns_epilogue_tile_fused_tma(const NsLaunch& L, co
   const float alpha = g, beta = g * L.a;
   const int row = m0 + row_in_tile;
   const bool row_ok = row < P.M;
-  const int warp_row0 = row - lane;
-  if (warp_row0 >= P.M) return;  // no row of this warp is in the output
+  const FusedTile f = fused_tile(L, P, n0, row);
+  if (!f.any_row) return true;  // no row of this warp is in the output
   const SliceDesc& S = L.slices[P.slice];
-  const float* w_row = S.master + static_cast<int64_t>(row) * S.n;
   const float decay = 1.0f - L.lr * L.wd;
   const float step = L.lr * S.shape_scale;
-  const bool w_vec = S.vec_ok != 0;
-  const CUtensorMap* map_w = L.cmaps + S.map_w;
   const CUtensorMap* map_p = S.map_p >= 0 ? L.cmaps + S.map_p : nullptr;
-  const int z = S.z_t;
   const uint16_t* aux_row = reinterpret_cast<const uint16_t*>(P.aux) + static_cast<int64_t>(row) * P.ld_aux;
   const uint16_t* auxlo_row = P.aux_lo ? P.aux_lo + static_cast<int64_t>(row) * P.ld_aux : nullptr;
   const bool need_aux = beta != 0.f && row_ok;
@@ -510,8 +566,9 @@ __device__ __forceinline__ void ns_epilogue_tile_fused_tma(const NsLaunch& L, co
     if (!need_aux || c0 + 32 > P.N) return;
     load_aux_chunk(aux_row, auxlo_row, c0, q);
   };
-  const int n_chunks = min(BN / 32, (P.N - n0 + 31) / 32);
+  const int n_chunks = f.n_chunks;
   const uint32_t swz = static_cast<uint32_t>(lane) * 128u;
+  const uint32_t pbase = stage_smem + static_cast<uint32_t>(kFusedWBoxes) * 4096u;
   uint4 aux_next[8];
   load_aux(0, aux_next);
 #pragma unroll 1
@@ -537,31 +594,33 @@ __device__ __forceinline__ void ns_epilogue_tile_fused_tma(const NsLaunch& L, co
                       : 0.f;
       }
     }
-    float w[32];
-    if (row_ok && full_chunk && w_vec) {
-      const float4* src = reinterpret_cast<const float4*>(w_row + col0);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float4 q = src[i];
-        w[4 * i] = q.x; w[4 * i + 1] = q.y; w[4 * i + 2] = q.z; w[4 * i + 3] = q.w;
-      }
-    } else {
-#pragma unroll
-      for (int j = 0; j < 32; ++j) w[j] = (row_ok && col0 + j < P.N) ? w_row[col0 + j] : 0.f;
-    }
+    const uint32_t gbox = w_used + static_cast<uint32_t>(cc);
+    const uint32_t wbuf = stage_smem + (gbox % kFusedWBoxes) * 4096u;
+    const bool w_ready = mbar_wait_bounded(wbar0 + 8u * (gbox % kFusedWBoxes), (gbox / kFusedWBoxes) & 1u,
+                                           abort_flag, L.err, kErrTimeoutEpilogue);
     tmem_ld_wait_regs(r);
+    if (!w_ready) {
+      w_used += static_cast<uint32_t>(cc);
+      return false;
+    }
+    float w[32];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      float q[4];
+      ld_shared_v4(wbuf + swz + ((static_cast<uint32_t>(j) ^ static_cast<uint32_t>(lane & 7)) << 4), q);
+      w[4 * j] = q[0]; w[4 * j + 1] = q[1]; w[4 * j + 2] = q[2]; w[4 * j + 3] = q[3];
+    }
 #pragma unroll
     for (int j = 0; j < 32; ++j) {
       float v = alpha * __uint_as_float(r[j]);
       if (beta != 0.f) v = fmaf(beta, auxf[j], v);
       w[j] = fmaf(-step, v, w[j] * decay);
     }
-    // Buffers of this chunk: free once at most the previous chunk's stores
-    // are still reading shared memory.
-    if (lane == 0) bulk_wait_group_read<1>();
+    // The parameter buffer of this chunk: free once at most the previous
+    // chunk's stores are still reading shared memory.
+    if (lane == 0 && map_p) bulk_wait_group_read<1>();
     __syncwarp();
-    const uint32_t wbuf = stage_smem + static_cast<uint32_t>(cc & 1) * 4096u;
-    const uint32_t pbuf = stage_smem + 8192u + static_cast<uint32_t>((cc >> 1) & 1) * 4096u;
+    const uint32_t pbuf = pbase + static_cast<uint32_t>((cc >> 1) & 1) * 4096u;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const uint32_t off = swz + ((static_cast<uint32_t>(j) ^ static_cast<uint32_t>(lane & 7)) << 4);
@@ -580,13 +639,23 @@ __device__ __forceinline__ void ns_epilogue_tile_fused_tma(const NsLaunch& L, co
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) {
-      tma_store_3d(map_w, wbuf, col0, warp_row0, z);
+      tma_store_3d(f.map_w, wbuf, col0, f.warp_row0, f.z);
       // A parameter box holds two chunks; the last chunk of a ragged tile
       // stores its half alone (the other half lies past the edge).
-      if (map_p && ((cc & 1) || cc + 1 == n_chunks)) tma_store_3d(map_p, pbuf, n0 + 64 * (cc >> 1), warp_row0, z);
+      if (map_p && ((cc & 1) || cc + 1 == n_chunks))
+        tma_store_3d(map_p, pbuf, n0 + 64 * (cc >> 1), f.warp_row0, f.z);
       bulk_commit_group();
+      if (cc + 2 < n_chunks) {
+        // Box cc + 2 reuses the buffer of chunk cc - 1: wait until at most
+        // this chunk's stores are still reading.
+        bulk_wait_group_read<1>();
+        fused_w_request(f, n0, cc + 2, gbox + 2u, stage_smem, wbar0);
+      }
     }
+    if (cc + 2 < n_chunks) ++w_issued;
   }
+  w_used += static_cast<uint32_t>(n_chunks);
+  return true;
 }
 
 }  // namespace dmuon

@@ -307,17 +307,21 @@ def test_pair_kernel_tuning_variants(cuda_lib, settings):
         assert max(r["O_slices"]) <= bf16_tol(r["shape"]), r
 
 
+# (40, 264, 264) adds 160 tiles cut 8 rows / columns past a 256-block: more
+# tiles than CTA pairs, so every pair's epilogue warps carry their W box ring
+# across several tiles, some of which hold none of their rows.
 FUSED_SHAPES = [(520, 520), (200, 328), (1000, 136), (136, 1000), (2, 300, 600), (3, 64, 96), (1024, 2048),
-                (2048, 1024), (8, 4096)]
+                (2048, 1024), (8, 4096), (40, 264, 264)]
 
 
 @pytest.mark.parametrize("settings", [{8: 0}, {8: 0, 7: 0}])
 def test_fused_update_with_tma_stores_on_ragged_tiles(cuda_lib, settings):
-    """The last Combine applies the update in its epilogue and writes W and
-    the bf16 parameter with TMA tile stores (every tensor here has rows of a
-    multiple of 16 bytes); tiles cut by the tensors' edges rely on the
-    stores' clipping.  Key 8 = 0 fuses every step's last Combine; with key 7
-    = 0 the fused epilogue also reads X as aux.  Against the oracle."""
+    """The last Combine applies the update in its epilogue: it reads W and
+    writes W and the bf16 parameter with TMA tile copies (every tensor here
+    has rows of a multiple of 16 bytes); tiles cut by the tensors' edges rely
+    on the loads' zero fill and the stores' clipping.  Key 8 = 0 fuses every
+    step's last Combine; with key 7 = 0 the fused epilogue also reads X as
+    aux.  Against the oracle."""
     try:
         for key, value in settings.items():
             cuda_lib.dmuon_set_tuning(key, value)
