@@ -376,8 +376,18 @@ class DistributedOwnerStep:
             self.comm.all_gather_pieces(self.sp_param_flat, L.piece)
 
     def step(self, muon, adamw=None, stream=None):
+        """reduce -> owner step -> publish.  The collectives are ordered on
+        torch's current stream; a ``stream`` (torch.cuda.Stream) other than
+        that one runs the owner step after the reduce and before the
+        broadcast.  A raw stream handle must be the current stream."""
         self.reduce_grads()
-        self.local_step(muon, adamw, stream=stream)
+        if isinstance(stream, torch.cuda.Stream):
+            cur = torch.cuda.current_stream(self.device)
+            stream.wait_stream(cur)
+            self.local_step(muon, adamw, stream=stream)
+            cur.wait_stream(stream)
+        else:
+            self.local_step(muon, adamw, stream=stream)
         self.publish_params()
 
     def close(self):
