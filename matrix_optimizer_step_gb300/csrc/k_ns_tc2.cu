@@ -450,11 +450,10 @@ static cudaError_t launch_variant3(const NsLaunch& L, int n_pairs, cudaStream_t 
   return cudaGetLastError();
 }
 
-// The fused update keeps 4 epilogue warps and a 4-stage ring: it runs on
-// long main loops only (short ones store X and update in a separate pass),
-// where more concurrent W traffic slows the operand copies (measured +5 ms
+// The fused update keeps 4 epilogue warps and a 4-stage ring: on long main
+// loops more concurrent W traffic slows the operand copies (measured +5 ms
 // per Llama-3-8B step with 8 warps and an aux-free epilogue), and its W
-// boxes leave no shared memory for a fifth stage.
+// boxes leave no shared memory for more warps' staging or a fifth stage.
 template <int STAGES>
 static cudaError_t launch_variant(const NsLaunch& L, int n_pairs, cudaStream_t st) {
   if (L.fuse_update) return launch_variant3<4, true, 4>(L, n_pairs, st);

@@ -167,14 +167,18 @@ int muon_launch_ns(dmuon_context* ctx, MuonSlot& S, float lr, float wd, int32_t 
   float* inv_norm = static_cast<float*>(P.inv_norm.p);
   const int n_chunks = static_cast<int>(P.chunks.size());
   int st = DMUON_OK;
-  // The last Combine applies the update in its epilogue, except where its
-  // tiles' main loops are short: there the epilogue sets the pace, and a
-  // plain X store by 8 epilogue warps followed by the streaming update pass
-  // is faster (GPT-2 set: 380 us fused against 120 + ~160 us).
+  // The last Combine applies the update in its epilogue when every tensor
+  // has TMA maps.  On the CTA-pair kernel (W in, W' and the parameter out by
+  // TMA tile copies) that pays at any main-loop length: GPT-2 set 1.90 ->
+  // 1.85 ms, many-small set 43.3 -> 42.7 ms per step against a plain X store
+  // by 8 epilogue warps plus the streaming update pass.  The one-CTA
+  // kernel's fused epilogue moves W row by row; there launches with short
+  // main loops keep the separate pass (GPT-2 set: 380 us fused against
+  // 120 + ~160 us).
   const Tuning& tu = ctx->tune;
   const bool pairs = tu.ns_pairs != 0;
-  const PhaseTiles& last_combine = pairs ? P.phase2[kCombine] : P.phase[kCombine];
-  const bool fuse_last = last_combine.mean_kblocks >= static_cast<double>(tu.epi8_below) && S.all_tma;
+  const bool fuse_last =
+      S.all_tma && (pairs || P.phase[kCombine].mean_kblocks >= static_cast<double>(tu.epi8_below));
   for (int it = 0; it < ns_steps; ++it) {
     const int variant = it < 2 ? 2 + it : (it & 1);
     for (int kind = kGram; kind <= kCombine; ++kind) {

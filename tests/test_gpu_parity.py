@@ -288,13 +288,12 @@ TUNING_DEFAULTS = {3: 4, 4: 1, 6: 1, 7: 1, 8: 32, 12: 128}
 @pytest.mark.parametrize("settings", [{3: 5}, {4: 0}, {6: 0}, {7: 0}, {8: 0}, {8: 1000000}, {8: 0, 7: 0},
                                       {12: 1}, {12: 1, 7: 0}, {12: 1, 8: 1000000}, {12: 1, 4: 0}, {12: 0}])
 def test_pair_kernel_tuning_variants(cuda_lib, settings):
-    """5-stage ring, rows-outer tile order, mirrored symmetric outputs, a*X
-    added in every Combine epilogue, 4 or 8 epilogue warps in every launch,
-    the update fused into every step's last Combine (key 8 = 0), with and
-    without an aux operand there, 256 x 512 tiles in every launch they fit
-    (key 12 = 1; with aux, unfused last Combine, rows-outer order) or in
-    none (key 12 = 0): each selectable variant of the CTA-pair kernel
-    against the oracle."""
+    """5-stage ring (the fused last Combine keeps 4), rows-outer tile order,
+    mirrored symmetric outputs, a*X added in every Combine epilogue (so the
+    fused last Combine reads X as aux), 4 or 8 epilogue warps in every other
+    launch, 256 x 512 tiles in every launch they fit (key 12 = 1; with aux,
+    with 8 warps, rows-outer order) or in none (key 12 = 0): each selectable
+    variant of the CTA-pair kernel against the oracle."""
     try:
         for key, value in settings.items():
             cuda_lib.dmuon_set_tuning(key, value)
@@ -319,9 +318,9 @@ def test_fused_update_with_tma_stores_on_ragged_tiles(cuda_lib, settings):
     """The last Combine applies the update in its epilogue: it reads W and
     writes W and the bf16 parameter with TMA tile copies (every tensor here
     has rows of a multiple of 16 bytes); tiles cut by the tensors' edges rely
-    on the loads' zero fill and the stores' clipping.  Key 8 = 0 fuses every
-    step's last Combine; with key 7 = 0 the fused epilogue also reads X as
-    aux.  Against the oracle."""
+    on the loads' zero fill and the stores' clipping.  Key 8 = 0 runs the
+    other launches with 4 epilogue warps; with key 7 = 0 the fused epilogue
+    also reads X as aux.  Against the oracle."""
     try:
         for key, value in settings.items():
             cuda_lib.dmuon_set_tuning(key, value)
@@ -345,11 +344,7 @@ def test_fused_update_without_bf16_parameter(cuda_lib):
     Wd = [w.cuda() for w in W]
     Bd = [torch.zeros(s, device="cuda") for s in shapes]
     Gd = [x.cuda() for x in G]
-    cuda_lib.dmuon_set_tuning(8, 0)
-    try:
-        st = cuda_lib.OwnerStep(0)
-    finally:
-        cuda_lib.dmuon_set_tuning(8, TUNING_DEFAULTS[8])
+    st = cuda_lib.OwnerStep(0)
     st.set_muon(Wd, Bd, Gd, None)
     st.muon_step(0.02, 0.95, 0.01, 5, A, B, C)
     st.sync()
@@ -368,11 +363,7 @@ def test_unstorable_tensor_falls_back_to_the_update_pass(cuda_lib):
     """A call with a tensor whose rows are not a multiple of 16 bytes (n = 130)
     does not fuse the update (the last Combine stores X and the streaming pass
     updates W); the results stay within the tolerances."""
-    cuda_lib.dmuon_set_tuning(8, 0)
-    try:
-        res = run_muon(cuda_lib, [(1024, 130), (512, 1024)], seed=53)[0]
-    finally:
-        cuda_lib.dmuon_set_tuning(8, TUNING_DEFAULTS[8])
+    res = run_muon(cuda_lib, [(1024, 130), (512, 1024)], seed=53)[0]
     for r in res:
         assert r["buf"] <= 1e-6 and r["param_exact"], r
         assert max(r["O_slices"]) <= bf16_tol(r["shape"]), r
