@@ -133,9 +133,11 @@ DMUON_API int dmuon_lpt_assign_layered(const int64_t* sizes, const int32_t* laye
  * Tensors whose rows are a multiple of 16 bytes (n % 4 == 0, and n % 8 == 0
  * when param_bf16 is given) with 16-byte-aligned master and param_bf16
  * let the step apply the update inside its last Newton-Schulz product (TMA
- * tile stores to those buffers); a call with any other bf16-path tensor
- * applies it in a separate pass, which rounds the last iterate to bf16
- * first (results stay within the same tolerances).
+ * tile copies from and to those buffers); a call with any other bf16-path
+ * tensor applies it in a separate pass for all its tensors, which rounds the
+ * last iterate to bf16 first (results stay within the same tolerances).
+ * The choice is made over the whole call, so splitting a call into groups
+ * (tuning keys 9 and 11, dmuon_step_host) never changes a result.
  * Reachable means memory of the context's device, managed memory, or
  * page-locked host memory mapped into the device's address space
  * (cudaHostAlloc / cudaHostRegister with mapping): the kernels then read

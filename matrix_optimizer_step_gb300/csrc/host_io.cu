@@ -303,11 +303,18 @@ int dmuon_step_host(dmuon_context* ctx, const dmuon_matrix* mats, const dmuon_ho
       return cuda_fail(cudaGetLastError(), "step_host");
     return enqueue_runs(H.a_out, cudaMemcpyDeviceToHost, ctx->d2h);
   };
+  // The update fuses in every group or in none, as in one dmuon_muon_step
+  // over all tensors, so the grouping never changes a result.
+  bool call_tma = true;
+  for (int g = 0; g < G; ++g) {
+    const int b = groups[static_cast<size_t>(g)].first, e = groups[static_cast<size_t>(g)].second;
+    call_tma = call_tma && plan_tma_copyable(slot[static_cast<size_t>(g)]->plan, mats + b, e - b);
+  }
   for (int g = 0; g < G; ++g) {
     const int b = groups[static_cast<size_t>(g)].first, e = groups[static_cast<size_t>(g)].second;
     if (cudaStreamWaitEvent(s, ev_in(g), 0) != cudaSuccess) return join(cuda_fail(cudaGetLastError(), "step_host"));
     st = muon_step_impl(ctx, *slot[static_cast<size_t>(g)], mats + b, e - b, muon->lr, muon->momentum, muon->wd,
-                        muon->ns_steps, muon->a, muon->b, muon->c, muon->flags, s);
+                        muon->ns_steps, muon->a, muon->b, muon->c, muon->flags, s, call_tma);
     if (st != DMUON_OK) return join(st);
     if (cudaEventRecord(ev_done(g), s) != cudaSuccess || cudaStreamWaitEvent(ctx->d2h, ev_done(g), 0) != cudaSuccess)
       return join(cuda_fail(cudaGetLastError(), "step_host"));

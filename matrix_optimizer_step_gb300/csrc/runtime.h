@@ -415,11 +415,16 @@ int prepare_slot(dmuon_context* ctx, MuonSlot& S, const dmuon_matrix* mats, int 
 int muon_stage_table(dmuon_context* ctx, MuonSlot& S, const dmuon_matrix* mats, int n, int32_t ns_steps,
                      cudaStream_t s);
 int muon_launch_front(dmuon_context* ctx, MuonSlot& S, float momentum, uint32_t flags, cudaStream_t s);
+// call_tma: every tensor of the whole call (all groups of a grouped call)
+// can take the fused update's TMA copies; false keeps every group unfused.
 int muon_launch_ns(dmuon_context* ctx, MuonSlot& S, float lr, float wd, int32_t ns_steps, float a, float b,
-                   float c, cudaStream_t s);
+                   float c, cudaStream_t s, bool call_tma = true);
 int muon_step_impl(dmuon_context* ctx, MuonSlot& S, const dmuon_matrix* mats, int n, float lr,
                    float momentum, float wd, int32_t ns_steps, float a, float b, float c,
-                   uint32_t flags, cudaStream_t s);
+                   uint32_t flags, cudaStream_t s, bool call_tma = true);
+// Whether every bf16-class tensor of plan P (over mats[0..n)) can take the
+// fused update's TMA copies.
+bool plan_tma_copyable(const MuonPlan& P, const dmuon_matrix* mats, int n);
 int64_t matrix_elems(const dmuon_matrix& M);
 int muon_step_overlapped(dmuon_context* ctx, const dmuon_matrix* mats, int n, int groups, float lr,
                          float momentum, float wd, int32_t ns_steps, float a, float b, float c,

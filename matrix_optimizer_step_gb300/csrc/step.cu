@@ -27,21 +27,42 @@ int prepare_slot(dmuon_context* ctx, MuonSlot& S, const dmuon_matrix* mats, int 
   return st;
 }
 
+// Tensors of a bf16 class in plan P (the ones the tensor-core path steps).
+std::vector<char> bf16_tensors(const MuonPlan& P, int n) {
+  std::vector<char> f(static_cast<size_t>(n), 0);
+  for (const SliceRef& R : P.slices)
+    if (!P.classes[static_cast<size_t>(R.cls)].f32) f[static_cast<size_t>(R.mat)] = 1;
+  return f;
+}
+
+// A TMA copy needs a 16-byte-aligned base and rows whose byte length is a
+// multiple of 16: n % 4 == 0 for the fp32 master, n % 8 == 0 for the bf16
+// parameter.
+bool tma_copyable(const dmuon_matrix& M) {
+  const int64_t nn = M.shape[M.rank - 1];
+  return aligned16(M.master) && nn % 4 == 0 && (!M.param_bf16 || (aligned16(M.param_bf16) && nn % 8 == 0));
+}
+
+bool plan_tma_copyable(const MuonPlan& P, const dmuon_matrix* mats, int n) {
+  const std::vector<char> f = bf16_tensors(P, n);
+  for (int i = 0; i < n; ++i)
+    if (f[static_cast<size_t>(i)] && !tma_copyable(mats[i])) return false;
+  return true;
+}
+
 // Tensor maps of the callers' fp32 masters (32 x 32 boxes) and bf16
-// parameters (64 x 32 boxes) for the fused update's TMA stores, per tensor
-// of a bf16 class, rebuilt only when the descriptor array changes.  A TMA
-// store needs a 16-byte-aligned base and rows whose byte length is a
-// multiple of 16 (n % 4 == 0 for the master, n % 8 == 0 for the parameter);
-// a tensor that misses either gets no maps, and then no launch fuses the
-// update (the last Combine stores X and the streaming pass updates W).
+// parameters (64 x 32 boxes) for the fused update's TMA copies, per tensor
+// of a bf16 class, rebuilt only when the descriptor array or the tensors'
+// classes change.  A tensor that is not tma_copyable gets no maps, and then
+// no launch of the call fuses the update (the last Combine stores X and the
+// streaming pass updates W).
 int build_caller_maps(MuonSlot& S, const dmuon_matrix* mats, int n, cudaStream_t s) {
+  const MuonPlan& P = S.plan;
+  const std::vector<char> bf16_tensor = bf16_tensors(P, n);
   std::vector<uint8_t> key;
   keep_bytes(key, mats, n);
+  key.insert(key.end(), bf16_tensor.begin(), bf16_tensor.end());
   if (key == S.cmaps_key && !S.cmaps_host.empty()) return DMUON_OK;
-  const MuonPlan& P = S.plan;
-  std::vector<char> bf16_tensor(static_cast<size_t>(n), 0);
-  for (const SliceRef& R : P.slices)
-    if (!P.classes[static_cast<size_t>(R.cls)].f32) bf16_tensor[static_cast<size_t>(R.mat)] = 1;
   S.cmaps_host.clear();
   S.map_w.assign(static_cast<size_t>(n), -1);
   S.map_p.assign(static_cast<size_t>(n), -1);
@@ -53,9 +74,7 @@ int build_caller_maps(MuonSlot& S, const dmuon_matrix* mats, int n, cudaStream_t
     const int64_t m = M.shape[M.rank - 2], nn = M.shape[M.rank - 1];
     int64_t lead = 1;
     for (int d = 0; d < M.rank - 2; ++d) lead *= M.shape[d];
-    const bool ok = enc && aligned16(M.master) && nn % 4 == 0 &&
-                    (!M.param_bf16 || (aligned16(M.param_bf16) && nn % 8 == 0));
-    if (!ok) {
+    if (!enc || !tma_copyable(M)) {
       S.all_tma = false;
       continue;
     }
@@ -160,7 +179,7 @@ int muon_launch_front(dmuon_context* ctx, MuonSlot& S, float momentum, uint32_t 
 // Stage 3: the Newton-Schulz launches and the update (needs stage 2's
 // results, ordered before s).
 int muon_launch_ns(dmuon_context* ctx, MuonSlot& S, float lr, float wd, int32_t ns_steps, float a, float b,
-                   float c, cudaStream_t s) {
+                   float c, cudaStream_t s, bool call_tma) {
   MuonPlan& P = S.plan;
   const SliceDesc* d_slices = static_cast<const SliceDesc*>(S.table.dev.p);
   const Chunk* d_chunks = static_cast<const Chunk*>(P.chunks_dev.p);
@@ -168,17 +187,19 @@ int muon_launch_ns(dmuon_context* ctx, MuonSlot& S, float lr, float wd, int32_t 
   const int n_chunks = static_cast<int>(P.chunks.size());
   int st = DMUON_OK;
   // The last Combine applies the update in its epilogue when every tensor
-  // has TMA maps.  On the CTA-pair kernel (W in, W' and the parameter out by
-  // TMA tile copies) that pays at any main-loop length: GPT-2 set 1.90 ->
-  // 1.85 ms, many-small set 43.3 -> 42.7 ms per step against a plain X store
-  // by 8 epilogue warps plus the streaming update pass.  The one-CTA
-  // kernel's fused epilogue moves W row by row; there launches with short
-  // main loops keep the separate pass (GPT-2 set: 380 us fused against
-  // 120 + ~160 us).
+  // of the call has TMA maps (call_tma: the same decision for every group
+  // of a grouped call, so grouping never changes a result).  On the CTA-pair
+  // kernel (W in, W' and the parameter out by TMA tile copies) that pays at
+  // any main-loop length: GPT-2 set 1.90 -> 1.85 ms, many-small set 43.3 ->
+  // 42.7 ms per step against a plain X store by 8 epilogue warps plus the
+  // streaming update pass.  (The one-CTA kernel's fused epilogue moves W
+  // row by row and is slower than the separate pass on short main loops,
+  // GPT-2 set 380 against 120 + ~160 us, but a rule that looked at the
+  // call's main-loop lengths would differ between the groups of a grouped
+  // call.)
   const Tuning& tu = ctx->tune;
   const bool pairs = tu.ns_pairs != 0;
-  const bool fuse_last =
-      S.all_tma && (pairs || P.phase[kCombine].mean_kblocks >= static_cast<double>(tu.epi8_below));
+  const bool fuse_last = call_tma && S.all_tma;
   for (int it = 0; it < ns_steps; ++it) {
     const int variant = it < 2 ? 2 + it : (it & 1);
     for (int kind = kGram; kind <= kCombine; ++kind) {
@@ -253,14 +274,14 @@ int muon_launch_ns(dmuon_context* ctx, MuonSlot& S, float lr, float wd, int32_t 
 // every stage on stream s.
 int muon_step_impl(dmuon_context* ctx, MuonSlot& S, const dmuon_matrix* mats, int n, float lr,
                    float momentum, float wd, int32_t ns_steps, float a, float b, float c,
-                   uint32_t flags, cudaStream_t s) {
+                   uint32_t flags, cudaStream_t s, bool call_tma) {
   int st = prepare_slot(ctx, S, mats, n, (flags & DMUON_FLAG_FP32_NS) != 0);
   if (st != DMUON_OK) return st;
   st = muon_stage_table(ctx, S, mats, n, ns_steps, s);
   if (st != DMUON_OK) return st;
   st = muon_launch_front(ctx, S, momentum, flags, s);
   if (st != DMUON_OK) return st;
-  return muon_launch_ns(ctx, S, lr, wd, ns_steps, a, b, c, s);
+  return muon_launch_ns(ctx, S, lr, wd, ns_steps, a, b, c, s, call_tma);
 }
 
 int64_t matrix_elems(const dmuon_matrix& M) {
@@ -335,10 +356,13 @@ int muon_step_overlapped(dmuon_context* ctx, const dmuon_matrix* mats, int n, in
     if (cudaEventRecord(join, ctx->side) == cudaSuccess) cudaStreamWaitEvent(s, join, 0);
     return st;
   }
-  // Caller's stream: each group's Newton-Schulz once its momentum is done.
+  // Caller's stream: each group's Newton-Schulz once its momentum is done;
+  // the update fuses in every group or in none.
+  bool call_tma = true;
+  for (int g = 0; g < G; ++g) call_tma = call_tma && S[static_cast<size_t>(g)]->all_tma;
   for (int g = 0; g < G; ++g) {
     DM_CUDA(cudaStreamWaitEvent(s, ctx->side_events[2 + static_cast<size_t>(g)], 0));
-    st = muon_launch_ns(ctx, *S[static_cast<size_t>(g)], lr, wd, ns_steps, a, b, c, s);
+    st = muon_launch_ns(ctx, *S[static_cast<size_t>(g)], lr, wd, ns_steps, a, b, c, s, call_tma);
     if (st != DMUON_OK) return st;
   }
   return DMUON_OK;

@@ -359,6 +359,45 @@ def test_fused_update_without_bf16_parameter(cuda_lib):
             assert _frob(O[k], ref["O"].reshape(-1, m, n)[k]) <= 2e-2, (s, k)
 
 
+def test_same_descriptors_fp32_mode_then_bf16_mode(cuda_lib):
+    """One context steps the same descriptor array first in the fp32
+    validation mode (no tensor-core launch, so no TMA maps are needed) and
+    then in bf16 mode: the second call builds the maps the fused update
+    needs (the map cache is keyed by the descriptors and the tensors'
+    classes).  Both steps against the oracle."""
+    shapes = [(256, 512), (520, 264), (2, 128, 96)]
+    g = torch.Generator().manual_seed(71)
+    W = [torch.randn(s, generator=g) * 0.02 for s in shapes]
+    Wd = [w.cuda() for w in W]
+    Bd = [torch.zeros(s, device="cuda") for s in shapes]
+    Gd = [torch.empty(s, device="cuda", dtype=torch.bfloat16) for s in shapes]
+    Pd = [torch.empty(s, device="cuda", dtype=torch.bfloat16) for s in shapes]
+    st = cuda_lib.OwnerStep(0)
+    st.set_muon(Wd, Bd, Gd, Pd)
+    ref_B = [np.zeros(s) for s in shapes]
+    try:
+        for fp32_ns in (True, False):
+            G = [torch.randn(s, generator=g).to(torch.bfloat16) for s in shapes]
+            for d, h in zip(Gd, G):
+                d.copy_(h)
+            W_before = [w.double().cpu().numpy() for w in Wd]
+            st.muon_step(0.02, 0.95, 0.01, 5, A, B, C, fp32_ns=fp32_ns)
+            st.sync()
+            for i, s in enumerate(shapes):
+                m, n = s[-2], s[-1]
+                ref = omuon.muon_step(W_before[i], ref_B[i], G[i].double().numpy(), _f(0.02), _f(0.95), _f(0.01),
+                                      5, _f(A), _f(B), _f(C))
+                O = ((W_before[i] * (1 - _f(0.02) * _f(0.01)) - Wd[i].double().cpu().numpy())
+                     / (_f(0.02) * omuon.shape_scale(m, n))).reshape(-1, m, n)
+                tol = 1e-4 if fp32_ns else bf16_tol(s)
+                for k in range(O.shape[0]):
+                    assert _frob(O[k], ref["O"].reshape(-1, m, n)[k]) <= tol, (fp32_ns, s, k)
+                assert torch.equal(Pd[i], Wd[i].to(torch.bfloat16)), (fp32_ns, s)
+                ref_B[i] = Bd[i].double().cpu().numpy()
+    finally:
+        st.close()
+
+
 def test_unstorable_tensor_falls_back_to_the_update_pass(cuda_lib):
     """A call with a tensor whose rows are not a multiple of 16 bytes (n = 130)
     does not fuse the update (the last Combine stores X and the streaming pass
@@ -461,7 +500,10 @@ def test_many_tensors_one_call(cuda_lib):
 
 # ------------------------------------------- momentum overlapped with NS
 
-def test_overlapped_momentum_groups_bit_identical(cuda_lib):
+# The second list adds a tensor with rows of 130 floats (no TMA map): the
+# whole call then updates in the separate pass, in every group alike.
+@pytest.mark.parametrize("extra", [(), ((1000, 130),)])
+def test_overlapped_momentum_groups_bit_identical(cuda_lib, extra):
     """A large step is cut into groups whose momentum runs on a side stream
     beside the previous group's Newton-Schulz launches: every output must
     equal the one-group step bit for bit, for several group counts, over two
@@ -469,7 +511,7 @@ def test_overlapped_momentum_groups_bit_identical(cuda_lib):
     list forms up to 7 groups)."""
     dev = torch.device("cuda")
     shapes = [(1024, 4096), (4096, 1024), (2, 768, 3072), (1536, 1536), (3072, 768), (1024, 4096), (64, 4096),
-              (24, 2048)]
+              (24, 2048)] + list(extra)
     assert sum(int(np.prod(s)) for s in shapes) >= 16 << 20
     g = torch.Generator(device=dev).manual_seed(77)
     W0 = [torch.randn(s, generator=g, device=dev) * 0.02 for s in shapes]
