@@ -76,7 +76,7 @@ def build(verbose=False, force=False):
                 print(f"--- {os.path.basename(o)}\n{log}")
     if (not os.path.exists(LIB) or any(os.path.getmtime(o) > os.path.getmtime(LIB) for o in objs)):
         tmp = LIB + ".tmp"
-        cmd = [nvcc, "-shared"] + ARCH + ["-o", tmp] + objs + ["-lcuda" if False else "-ldl", "-lpthread", "-lrt"]
+        cmd = [nvcc, "-shared"] + ARCH + ["-o", tmp] + objs + ["-ldl", "-lpthread", "-lrt"]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed: {' '.join(cmd)}\n{r.stdout}\n{r.stderr}")
