@@ -402,6 +402,7 @@ __device__ __forceinline__ void ns_epilogue_tile_staged_pipe(const NsLaunch& L, 
   const int warp_row0 = row - lane;
   if (warp_row0 >= P.M) return;  // no row of this warp is in the output
   const CUtensorMap* map_out = L.maps + P.map_out;
+  const int pz = P.z;  // read once (the asm statements in the loop clobber memory)
   const bool has_lo = P.out_lo != nullptr;
   const CUtensorMap* map_out_lo = has_lo ? L.maps + P.map_out_lo : nullptr;
   const int n_boxes = (min(BN, P.N - n0) + 63) / 64;
@@ -449,8 +450,8 @@ __device__ __forceinline__ void ns_epilogue_tile_staged_pipe(const NsLaunch& L, 
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
-        tma_store_3d(map_out, buf, n0 + 64 * (cc >> 1), warp_row0, P.z);
-        if (has_lo) tma_store_3d(map_out_lo, buf + 4096u, n0 + 64 * (cc >> 1), warp_row0, P.z);
+        tma_store_3d(map_out, buf, n0 + 64 * (cc >> 1), warp_row0, pz);
+        if (has_lo) tma_store_3d(map_out_lo, buf + 4096u, n0 + 64 * (cc >> 1), warp_row0, pz);
         bulk_commit_group();
       }
       ++box_count;
@@ -550,6 +551,10 @@ __device__ __forceinline__ bool ns_epilogue_tile_fused_tma(const NsLaunch& L, co
     g = (L.gpow == 2) ? s * s : s;
   }
   const float alpha = g, beta = g * L.a;
+  // The problem's fields the chunk loop uses, read once: every inline-asm
+  // statement below clobbers memory, so a field read through P inside the
+  // loop would be fetched again after each of them.
+  const int PN = P.N;
   const int row = m0 + row_in_tile;
   const bool row_ok = row < P.M;
   const FusedTile f = fused_tile(L, P, n0, row);
@@ -563,35 +568,37 @@ __device__ __forceinline__ bool ns_epilogue_tile_fused_tma(const NsLaunch& L, co
   const bool need_aux = beta != 0.f && row_ok;
   auto load_aux = [&](int cc, uint4 (&q)[8]) {
     const int c0 = n0 + cc * 32;
-    if (!need_aux || c0 + 32 > P.N) return;
+    if (c0 + 32 > PN) return;
     load_aux_chunk(aux_row, auxlo_row, c0, q);
   };
   const int n_chunks = f.n_chunks;
   const uint32_t swz = static_cast<uint32_t>(lane) * 128u;
   const uint32_t pbase = stage_smem + static_cast<uint32_t>(kFusedWBoxes) * 4096u;
   uint4 aux_next[8];
-  load_aux(0, aux_next);
+  if (need_aux) load_aux(0, aux_next);
 #pragma unroll 1
   for (int cc = 0; cc < n_chunks; ++cc) {
     const int col0 = n0 + cc * 32;
     uint4 aux_cur[8];
+    float auxf[32];
+    if (need_aux) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) aux_cur[i] = aux_next[i];
-    if (cc + 1 < n_chunks) load_aux(cc + 1, aux_next);
+      for (int i = 0; i < 8; ++i) aux_cur[i] = aux_next[i];
+      if (cc + 1 < n_chunks) load_aux(cc + 1, aux_next);
+    }
     __syncwarp();
     uint32_t r[32];
     tmem_ld_32x32b_x32(t_lane + static_cast<uint32_t>(cc * 32), r);
-    const bool full_chunk = (col0 + 32 <= P.N);
-    float auxf[32];
-    if (need_aux && full_chunk) {
-      unpack_aux_chunk(aux_cur, auxlo_row != nullptr, auxf);
-    } else {
+    if (need_aux) {
+      if (col0 + 32 <= PN) {
+        unpack_aux_chunk(aux_cur, auxlo_row != nullptr, auxf);
+      } else {
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const int c = col0 + j;
-        auxf[j] = (need_aux && c < P.N)
-                      ? bf16_bits_to_f32(aux_row[c]) + (auxlo_row ? bf16_bits_to_f32(auxlo_row[c]) : 0.f)
-                      : 0.f;
+        for (int j = 0; j < 32; ++j) {
+          const int c = col0 + j;
+          auxf[j] = (c < PN) ? bf16_bits_to_f32(aux_row[c]) + (auxlo_row ? bf16_bits_to_f32(auxlo_row[c]) : 0.f)
+                             : 0.f;
+        }
       }
     }
     const uint32_t gbox = w_used + static_cast<uint32_t>(cc);
@@ -610,11 +617,15 @@ __device__ __forceinline__ bool ns_epilogue_tile_fused_tma(const NsLaunch& L, co
       ld_shared_v4(wbuf + swz + ((static_cast<uint32_t>(j) ^ static_cast<uint32_t>(lane & 7)) << 4), q);
       w[4 * j] = q[0]; w[4 * j + 1] = q[1]; w[4 * j + 2] = q[2]; w[4 * j + 3] = q[3];
     }
+    // Rows past the output's edge (need_aux false there) are clipped by the
+    // stores, so only the in-range rows' values matter.
+    if (need_aux) {
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      float v = alpha * __uint_as_float(r[j]);
-      if (beta != 0.f) v = fmaf(beta, auxf[j], v);
-      w[j] = fmaf(-step, v, w[j] * decay);
+      for (int j = 0; j < 32; ++j)
+        w[j] = fmaf(-step, fmaf(beta, auxf[j], alpha * __uint_as_float(r[j])), w[j] * decay);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) w[j] = fmaf(-step, alpha * __uint_as_float(r[j]), w[j] * decay);
     }
     // The parameter buffer of this chunk: free once at most the previous
     // chunk's stores are still reading shared memory.
