@@ -491,14 +491,15 @@ namespace dmuon {
 // warp counts the W boxes it has requested (w_issued) and consumed
 // (w_used) over all its tiles: box g goes to buffer g % kFusedWBoxes and
 // is the (g / kFusedWBoxes)-th completion of that buffer's barrier.
-// fused_w_prefetch requests a tile's first two boxes before the epilogue
-// waits for the tile's accumulator (the main loop hides them) and, after
-// short main loops, prefetches the others into L2; the chunk loop requests
-// box cc + 2 after storing chunk cc, once the store of chunk cc - 1 (the
-// buffer's previous user) has finished reading it.
+// fused_w_prefetch requests a tile's first kFusedWAhead boxes before the
+// epilogue waits for the tile's accumulator (the main loop hides them) and,
+// after short main loops, prefetches the others into L2; the chunk loop
+// requests box cc + kFusedWAhead after storing chunk cc, once the store of
+// chunk cc - 1 (the buffer's previous user) has finished reading it.
 // Same arithmetic as ns_epilogue_tile<true>, so the results are
 // bit-identical to it.
 constexpr int kFusedWBoxes = 3;
+constexpr int kFusedWAhead = kFusedWBoxes - 1;  // boxes requested ahead of the one in use
 
 __device__ __forceinline__ void ld_shared_v4(uint32_t addr, float (&v)[4]) {
   asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
@@ -539,16 +540,18 @@ __device__ __forceinline__ void fused_w_prefetch(const NsLaunch& L, const NsProb
                                                  uint32_t& w_issued) {
   const FusedTile f = fused_tile(L, P, n0, m0 + row_in_tile);
   if (!f.any_row) return;
-  const int first = min(2, f.n_chunks);
+  const int first = min(kFusedWAhead, f.n_chunks);
   if ((threadIdx.x & 31) == 0) {
-    // Their buffers' previous users are boxes w_issued - 3 and - 2: at most
-    // the last store (box w_issued - 1) may still be reading.
+    // Their buffers' previous users are boxes w_issued - kFusedWBoxes up to
+    // w_issued - 2: at most the last store (box w_issued - 1) may still be
+    // reading.
     bulk_wait_group_read<1>();
     for (int cc = 0; cc < first; ++cc) fused_w_request(f, n0, cc, w_issued + cc, stage_smem, wbar0);
     // Main loops of up to 32 k-blocks are shorter than the fused epilogue,
     // whose W boxes then arrive late: the tile's other W boxes are brought
     // into L2 while the main loop runs, so their loads into shared memory
-    // (two chunks ahead) hit L2 (GPT-2 set -1.0 %, many-small -1.1 %).
+    // (kFusedWAhead chunks ahead) hit L2 (GPT-2 set -1.0 %, many-small
+    // -1.1 %).
     // Longer main loops hide the W loads already, and the extra requests
     // there only compete with the operand copies (Llama-3-8B +1 to +3 ms).
     if (P.K <= 32 * 64)
@@ -674,14 +677,14 @@ __device__ __forceinline__ bool ns_epilogue_tile_fused_tma(const NsLaunch& L, co
       if (map_p && ((cc & 1) || cc + 1 == n_chunks))
         tma_store_3d(map_p, pbuf, n0 + 64 * (cc >> 1), f.warp_row0, f.z);
       bulk_commit_group();
-      if (cc + 2 < n_chunks) {
-        // Box cc + 2 reuses the buffer of chunk cc - 1: wait until at most
-        // this chunk's stores are still reading.
+      if (cc + kFusedWAhead < n_chunks) {
+        // Box cc + kFusedWAhead reuses the buffer of chunk cc - 1: wait
+        // until at most this chunk's stores are still reading.
         bulk_wait_group_read<1>();
-        fused_w_request(f, n0, cc + 2, gbox + 2u, stage_smem, wbar0);
+        fused_w_request(f, n0, cc + kFusedWAhead, gbox + kFusedWAhead, stage_smem, wbar0);
       }
     }
-    if (cc + 2 < n_chunks) ++w_issued;
+    if (cc + kFusedWAhead < n_chunks) ++w_issued;
   }
   w_used += static_cast<uint32_t>(n_chunks);
   return true;
