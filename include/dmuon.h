@@ -418,8 +418,8 @@ DMUON_API int dmuon_selftest_wait_timeout(dmuon_context* ctx, int32_t timeout_us
  *          tiles average at least `value` 64-deep k-blocks runs 256 x 512
  *          tiles wherever two adjacent column blocks exist (0..1e6, default
  *          128; 0 = never).  Results do not depend on the setting.
- * Results never depend on keys 3, 4, 6, 9, 10, 11 and 12 (bit for bit); key
- * 2 changes the kernel and key 7 and 8 the rounding points, all within the
+ * Results never depend on keys 3, 4, 6, 8, 9, 10, 11 and 12 (bit for bit);
+ * key 2 changes the kernel and key 7 the rounding points, both within the
  * documented tolerances.
  * Returns DMUON_ERR_INVALID_ARG for an unknown key or a value out of range
  * (nothing changes then).  Thread-safe (the defaults are guarded by a lock).

@@ -54,15 +54,18 @@ def _free_port():
         return s.getsockname()[1]
 
 
-def _worker(rank, world, port, q):
+def _worker(rank, world, port, q, backend="gloo"):
     import sys
 
     sys.path.insert(0, ROOT)
     os.environ["MASTER_ADDR"] = "127.0.0.1"
     os.environ["MASTER_PORT"] = str(port)
+    os.environ["NCCL_NVLS_ENABLE"] = "0"
     import torch.distributed as dist
 
-    dist.init_process_group("gloo", rank=rank, world_size=world)
+    if backend == "nccl":
+        torch.cuda.set_device(0)
+    dist.init_process_group(backend, rank=rank, world_size=world)
     try:
         torch.cuda.set_device(0)
         from matrix_optimizer_step_gb300.owner_dist import DistributedOwnerStep, OwnerLayout
@@ -97,17 +100,11 @@ def _frob(x, y):
     return float(np.linalg.norm(x - y) / (d if d > 0 else 1.0))
 
 
-def test_two_ranks_on_one_gpu_equal_one_process(cuda_lib):
-    mos = cuda_lib
-    from matrix_optimizer_step_gb300.owner_dist import OwnerLayout
-    from oracle import adamw as oadamw
-    from oracle import muon as omuon
-
-    world = 2
+def _run_ranks(world, backend):
     ctx = mp.get_context("spawn")
     q = ctx.Queue()
     port = _free_port()
-    procs = [ctx.Process(target=_worker, args=(r, world, port, q)) for r in range(world)]
+    procs = [ctx.Process(target=_worker, args=(r, world, port, q, backend)) for r in range(world)]
     for p in procs:
         p.start()
     out = sorted((q.get(timeout=600) for _ in procs), key=lambda o: o[0])
@@ -115,7 +112,29 @@ def test_two_ranks_on_one_gpu_equal_one_process(cuda_lib):
         p.join(timeout=120)
     assert all(o[1] is not None and not isinstance(o[1], str) for o in out), [o[1] for o in out]
     assert all(p.exitcode == 0 for p in procs)
+    return out
+
+
+def test_two_ranks_on_one_gpu_equal_one_process(cuda_lib):
+    out = _run_ranks(2, "gloo")
     assert np.array_equal(out[0][1], out[1][1]) and np.array_equal(out[0][2], out[1][2])
+    _check_against_one_process(cuda_lib, out, 2)
+
+
+def test_nccl_group_of_one_equals_one_process(cuda_lib):
+    """The NCCL branch of the collectives (mean by ReduceOp.AVG, in-place
+    reduce_scatter and all_gather on views of the flat buffers, broadcast)
+    on a group of one rank: the only NCCL group one GPU can hold without
+    ranks that wait on one another.  Every collective is then an identity,
+    so the step must equal one process stepping every tensor, bit for bit."""
+    out = _run_ranks(1, "nccl")
+    _check_against_one_process(cuda_lib, out, 1)
+
+
+def _check_against_one_process(mos, out, world):
+    from matrix_optimizer_step_gb300.owner_dist import OwnerLayout
+    from oracle import adamw as oadamw
+    from oracle import muon as omuon
 
     L = OwnerLayout.build(MUON, ADAMW, SHARDED, world)
     n_muon, n_own = len(MUON), len(MUON) + len(ADAMW)

@@ -435,6 +435,37 @@ def test_wide_tiles_bit_identical_to_narrow(cuda_lib):
         assert torch.equal(a_, b_)
 
 
+@pytest.mark.parametrize("extra", [(), ((1000, 130),)])
+def test_epilogue_warp_count_bit_identical(cuda_lib, extra):
+    """4 or 8 epilogue warps (key 8 = 0: 4 in every launch; 1e6: 8 in every
+    launch but the fused last Combine; default: 8 where main loops are
+    short) drain the same accumulators with the same arithmetic, so all
+    three give the same bits, with the update fused and, with an n = 130
+    tensor in the call, in the streaming pass."""
+    shapes = [(520, 520), (300, 700), (2, 300, 600), (96, 1024), (1536, 768)] + list(extra)
+    outs = []
+    for warps in (0, 1000000, 32):
+        cuda_lib.dmuon_set_tuning(8, warps)
+        try:
+            g = torch.Generator().manual_seed(13)
+            W = [(torch.randn(s, generator=g) * 0.02).cuda() for s in shapes]
+            Bf = [torch.zeros(s).cuda() for s in shapes]
+            G = [torch.randn(s, generator=g).to(torch.bfloat16).cuda() for s in shapes]
+            Pd = [torch.empty(s, device="cuda", dtype=torch.bfloat16) for s in shapes]
+            step = cuda_lib.OwnerStep(0)
+            step.set_muon(W, Bf, G, Pd)
+            for _ in range(2):
+                step.muon_step(0.02, 0.95, 0.01, 5, A, B, C)
+            step.sync()
+            step.close()
+            outs.append([w.cpu() for w in W] + [b.cpu() for b in Bf] + [p.cpu() for p in Pd])
+        finally:
+            cuda_lib.dmuon_set_tuning(8, TUNING_DEFAULTS[8])
+    for other in outs[1:]:
+        for a_, b_ in zip(outs[0], other):
+            assert torch.equal(a_, b_)
+
+
 def test_two_contexts_with_their_own_tiling_policy(cuda_lib):
     """Tuning is per context: one context on 256 x 512 tiles wherever they
     fit and one on 256 x 256 tiles only, stepped alternately in one process,
