@@ -398,9 +398,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_of<EPI>(), 1
         ns_epilogue_tile_staged_pipe(L, P, tm * TILE, sub_tn * TILE, row_in_tile, t_lane, my_staging, box_count,
                                      c_begin, c_end);
       else
-        ns_epilogue_tile_staged<EPI == 8>(L, P, tm * TILE, sub_tn * TILE, row_in_tile, t_lane,
-                                          !L.tri && P.sym && tm < sub_tn, my_staging, box_count, c_begin,
-                                          c_end);
+        ns_epilogue_tile_staged(L, P, tm * TILE, sub_tn * TILE, row_in_tile, t_lane, !L.tri && P.sym && tm < sub_tn,
+                                my_staging, box_count, c_begin, c_end);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {

@@ -250,7 +250,6 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
 // copy (when symmetric outputs are not kept as upper blocks) is still
 // stored directly.  The warp covers the
 // 32-column chunks [c_begin, c_end) of the tile (c_begin even: whole boxes).
-template <bool HOIST>
 __device__ __forceinline__ void ns_epilogue_tile_staged(const NsLaunch& L, const NsProblem& P, int m0, int n0,
                                                         int row_in_tile, uint32_t t_lane, bool mirror,
                                                         uint32_t stage_smem, uint32_t& box_count,
@@ -278,14 +277,10 @@ __device__ __forceinline__ void ns_epilogue_tile_staged(const NsLaunch& L, const
   const bool row_ok = row < P.M;
   const int warp_row0 = row - lane;
   if (warp_row0 >= P.M) return;  // no row of this warp is in the output
-  // HOIST: the problem's width and slice coordinate read once, not after
-  // every inline-asm statement (they clobber memory).  Used with 8 epilogue
-  // warps, whose launches run at the pace of the drain; the overlapped
-  // 4-warp epilogues keep the reloads (a faster drain there presses its
-  // stores against the operand copies: measured slower).
-  const int PN = HOIST ? P.N : 0, pz = HOIST ? P.z : 0;
-  auto width = [&]() { return HOIST ? PN : P.N; };
-  auto zcoord = [&]() { return HOIST ? pz : P.z; };
+  // The problem's width and slice coordinate, read once: every inline-asm
+  // statement below clobbers memory, so a field read through P inside the
+  // loop would be fetched again after each of them.
+  const int PN = P.N, pz = P.z;
   const uint16_t* aux_row = reinterpret_cast<const uint16_t*>(P.aux) + static_cast<int64_t>(row) * P.ld_aux;
   const uint16_t* auxlo_row = P.aux_lo ? P.aux_lo + static_cast<int64_t>(row) * P.ld_aux : nullptr;
   const CUtensorMap* map_out = L.maps + P.map_out;
@@ -299,7 +294,7 @@ __device__ __forceinline__ void ns_epilogue_tile_staged(const NsLaunch& L, const
   const bool need_aux = beta != 0.f && row_ok;
   auto load_aux = [&](int cc, uint4 (&q)[8]) {
     const int c0 = n0 + cc * 32;
-    if (!need_aux || c0 + 32 > width()) return;
+    if (!need_aux || c0 + 32 > PN) return;
     load_aux_chunk(aux_row, auxlo_row, c0, q);
   };
   uint4 aux_next[8];
@@ -314,14 +309,14 @@ __device__ __forceinline__ void ns_epilogue_tile_staged(const NsLaunch& L, const
     __syncwarp();
     uint32_t r[32];
     tmem_ld_32x32b_x32(t_lane + static_cast<uint32_t>(cc * 32), r);
-    const bool full_chunk = (col0 + 32 <= width());
+    const bool full_chunk = (col0 + 32 <= PN);
     float auxf[32];
     if (need_aux && full_chunk) {
       unpack_aux_chunk(aux_cur, auxlo_row != nullptr, auxf);
     } else if (need_aux) {
       for (int j = 0; j < 32; ++j) {
         const int c = col0 + j;
-        auxf[j] = (c < width()) ? bf16_bits_to_f32(aux_row[c]) + (auxlo_row ? bf16_bits_to_f32(auxlo_row[c]) : 0.f)
+        auxf[j] = (c < PN) ? bf16_bits_to_f32(aux_row[c]) + (auxlo_row ? bf16_bits_to_f32(auxlo_row[c]) : 0.f)
                             : 0.f;
       }
     }
@@ -369,8 +364,8 @@ __device__ __forceinline__ void ns_epilogue_tile_staged(const NsLaunch& L, const
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
-        tma_store_3d(map_out, buf, n0 + 64 * (cc >> 1), warp_row0, zcoord());
-        if (has_lo) tma_store_3d(map_out_lo, buf + 4096u, n0 + 64 * (cc >> 1), warp_row0, zcoord());
+        tma_store_3d(map_out, buf, n0 + 64 * (cc >> 1), warp_row0, pz);
+        if (has_lo) tma_store_3d(map_out_lo, buf + 4096u, n0 + 64 * (cc >> 1), warp_row0, pz);
         bulk_commit_group();
       }
       ++box_count;
