@@ -235,13 +235,15 @@ DMUON_API int dmuon_muon_step(dmuon_context* ctx, const dmuon_matrix* mats, int3
  * allocation through its own pool, code that must not grow its memory after
  * start-up, or code that must not risk the implicit device synchronisation
  * of cudaMalloc/cudaFree.  It computes what dmuon_muon_step computes for
- * `mat`, with the same precision policy (bf16 tensor cores for slices with
- * min(m, n) >= 64; the fp32 CUDA-core kernel for min(m, n) < 64 or with
- * DMUON_FLAG_FP32_NS), but needs no context: all scratch (Newton-Schulz
- * buffers, norm partials, descriptor tables, tensor maps, the device error
- * word) lives in one static device array of 64 MiB that every GPU loading
- * this library holds until the process exits, and the host tables are built
- * in a static 1 MiB host buffer.  No cudaMalloc, cudaFree or other
+ * `mat`, within the same tolerances and with the same precision policy
+ * (bf16 tensor cores for slices with min(m, n) >= 64; the fp32 CUDA-core
+ * kernel for min(m, n) < 64 or with DMUON_FLAG_FP32_NS), on the one-CTA
+ * tensor-core kernel and with the update in a separate pass (so its bits
+ * can differ from dmuon_muon_step's), but needs no context: all scratch
+ * (Newton-Schulz buffers, norm partials, descriptor tables, tensor maps,
+ * the device error word) lives in one static device array of 64 MiB that
+ * every GPU loading this library holds until the process exits, and the
+ * host tables are built in a static 1 MiB host buffer.  No cudaMalloc, cudaFree or other
  * allocating routine is called.
  *
  *   mat      host pointer to one descriptor (rank 2..4; leading dims are
