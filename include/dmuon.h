@@ -243,8 +243,8 @@ DMUON_API int dmuon_muon_step(dmuon_context* ctx, const dmuon_matrix* mats, int3
  * (Newton-Schulz buffers, norm partials, descriptor tables, tensor maps,
  * the device error word) lives in one static device array of 64 MiB that
  * every GPU loading this library holds until the process exits, and the
- * host tables are built in a static 1 MiB host buffer.  No cudaMalloc, cudaFree or other
- * allocating routine is called.
+ * host tables are built in a static 1 MiB host buffer.  No cudaMalloc,
+ * cudaFree or other allocating routine is called.
  *
  *   mat      host pointer to one descriptor (rank 2..4; leading dims are
  *            separate matrices), device tensors as for dmuon_muon_step
