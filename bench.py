@@ -752,9 +752,10 @@ def main():
     ap.add_argument("--overlap-adamw", action="store_true",
                     help="run the AdamW step on a side stream beside the Muon step (OwnerStep.step); "
                          "per-kernel AdamW times then include waiting for SMs")
-    ap.add_argument("--mode", choices=("owner", "replicas"), default="owner",
+    ap.add_argument("--mode", choices=("owner", "replicas"), default=None,
                     help="with --gpus N > 1: the owner-partitioned step of one model (default), or N "
-                         "independent replicas of the one-GPU step")
+                         "independent replicas of the one-GPU step; --mode owner under torchrun with one "
+                         "rank runs the owner step on a process group of one")
     ap.add_argument("--dist-backend", choices=("nccl", "gloo"), default="nccl",
                     help="process-group backend for N > 1 (gloo only to check the code path)")
     ap.add_argument("--tuning", action="append", default=[],
@@ -771,17 +772,23 @@ def main():
     if args.impl == "reference":
         run_reference(args, wl, rank, world)
         return
-    if world > 1:
+    # The owner-partitioned step: the default with several ranks; with one
+    # rank only when asked for under torchrun (a group of one).
+    owner = args.mode == "owner" or (args.mode is None and world > 1)
+    if owner and world == 1 and "MASTER_ADDR" not in os.environ:
+        ap.error("--mode owner with one rank needs torchrun (a process group of one)")
+    grouped = world > 1 or owner
+    if grouped:
         import torch.distributed as dist
 
         dist.init_process_group(args.dist_backend)
     try:
-        if world > 1 and args.mode == "owner":
+        if owner:
             run_owner(args, wl, rank, world, local_rank, dist)
         else:
             run_ours(args, wl, rank, world, local_rank)
     finally:
-        if world > 1:
+        if grouped:
             import torch.distributed as dist
 
             dist.destroy_process_group()

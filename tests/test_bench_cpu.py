@@ -32,3 +32,14 @@ def test_bench_rejects_short_warmup():
                           "single_256x512", "--steps", "1", "--warmup", "2"],
                          capture_output=True, text=True, timeout=120, cwd=ROOT)
     assert out.returncode != 0
+
+
+def test_bench_owner_mode_with_one_rank_needs_torchrun():
+    """--mode owner on a single process outside torchrun has no process
+    group to run on: rejected before any device work."""
+    env = {k: v for k, v in os.environ.items() if k not in ("MASTER_ADDR", "MASTER_PORT", "WORLD_SIZE", "RANK")}
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--mode", "owner", "--workload",
+                          "single_256x512", "--steps", "1", "--warmup", "3"],
+                         capture_output=True, text=True, timeout=120, cwd=ROOT, env=env)
+    assert out.returncode != 0
+    assert "needs torchrun" in out.stderr

@@ -239,3 +239,27 @@ def test_bench_owner_mode_on_two_ranks_of_one_gpu(cuda_lib):
     per = d["owner"]["per_rank"]
     assert len(per) == 2 and all(p["launches"] > 0 and p["ns_ms"] > 0 for p in per)
     assert all(n > 0 for n in d["owner"]["owned_elements"])
+
+
+def test_bench_owner_mode_on_an_nccl_group_of_one(cuda_lib):
+    """bench.py's owner-partitioned mode under torchrun with one rank on
+    NCCL: the process-group code of the mode (collectives of the step,
+    gathers of the per-rank statistics, barriers, the max over ranks) on
+    the NCCL backend, on the hardware (a group of one: nothing waits on
+    another rank)."""
+    import json
+    import subprocess
+    import sys
+
+    port = _free_port()
+    env = dict(os.environ, NCCL_NVLS_ENABLE="0")
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "1",
+           "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.join(ROOT, "bench.py"),
+           "--gpus", "1", "--mode", "owner", "--workload", "gpt2_small", "--steps", "2", "--warmup", "3"]
+    r = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=900, env=env)
+    assert r.returncode == 0, r.stderr[-3000:]
+    lines = [x for x in r.stdout.splitlines() if x.startswith("{")]
+    assert len(lines) == 1, r.stdout[-2000:]
+    d = json.loads(lines[0])
+    assert d["n_gpus"] == 1 and d["scaling"] == "strong" and d["ms_per_step"] > 0
+    assert d["config"]["backend"] == "nccl" and len(d["owner"]["per_rank"]) == 1
