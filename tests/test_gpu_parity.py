@@ -129,6 +129,20 @@ def test_fp32_validation_grouped_and_tall(cuda_lib):
         assert r["buf"] <= 1e-6 and r["O"] <= 1e-4, r
 
 
+def test_bf16_path_with_fp32_gradients(cuda_lib):
+    """fp32 gradients on the bf16 tensor-core path (the momentum pass reads
+    4-byte gradients, the Newton-Schulz operands stay bf16), with a nonzero
+    momentum buffer, on ragged tiles and both orientations; the update
+    fused (every tensor has TMA maps) and, with an n = 130 tensor in the
+    call, in the streaming pass."""
+    for shapes in ([(200, 328), (328, 200), (2, 96, 264)], [(200, 328), (1000, 130)]):
+        res = run_muon(cuda_lib, shapes, grad_dtype=torch.float32, seed=9, buf_scale=0.3, steps=2)
+        for errs in res:
+            for r in errs:
+                assert r["buf"] <= 1e-6 and r["param_exact"], r
+                assert max(r["O_slices"]) <= bf16_tol(r["shape"]), r
+
+
 def test_multi_step_state_carried(cuda_lib):
     steps = run_muon(cuda_lib, [(128, 320), (320, 128)], seed=4, steps=3)
     for errs in steps:
